@@ -1,0 +1,189 @@
+"""Pins for the oracle's forward: an independent dense brute force, closed forms,
+zero cases, a dense-MLP special case and permutation equivariance (CPU only)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workload as W
+
+TINY_MX = W.CONFIGS["tiny"]
+TINY_F8 = W.Config("tiny_f8", T=24, H=256, I=256, E=4, K=2, variant="f8", seed=11)
+
+
+# ------------------------------------------------------------------ independent brute force
+def _bits_e2m1(n: torch.Tensor) -> torch.Tensor:
+    s = 1 - 2 * ((n >> 3) & 1).double()
+    e = ((n >> 1) & 3).double()
+    m = (n & 1).double()
+    mag = torch.where(e == 0, 0.5 * m, (1 + 0.5 * m) * torch.exp2(e - 1))
+    return s * mag
+
+
+def _deq_all(cfg, inp):
+    """Dense dequantised x [T,H], W1 [E,2I,H], W2 [E,H,I] in torch fp64."""
+    x = inp["x"].view(torch.float8_e4m3fn).double()
+    if cfg.variant == "mx":
+        x = x * torch.exp2(inp["x_sf"].double() - 127).repeat_interleave(32, -1)
+        def wq(p, sf):
+            n = torch.stack([p & 0xF, p >> 4], -1).flatten(-2)
+            return _bits_e2m1(n) * torch.exp2(sf.double() - 127).repeat_interleave(32, -1)
+    else:
+        x = x * inp["x_sf"].double().repeat_interleave(128, -1)
+        def wq(c, sf):
+            s = sf.double().repeat_interleave(128, -2).repeat_interleave(128, -1)
+            return c.view(torch.float8_e4m3fn).double() * s
+    return x, wq(inp["w1"], inp["w1_sf"]), wq(inp["w2"], inp["w2_sf"])
+
+
+def _requant_torch(a32: torch.Tensor, variant: str) -> torch.Tensor:
+    """Independent requant: library e4m3 cast, frexp-based exponent."""
+    n = a32.shape[-1]
+    if variant == "mx":
+        b = a32.reshape(*a32.shape[:-1], n // 32, 32)
+        amax = b.abs().amax(-1).clamp_min(1e-10)
+        m, ex = torch.frexp(amax)
+        e = torch.where(m <= 0.875, ex - 9, ex - 8).clamp(-127, 127).double()
+        q = (b.double() * torch.exp2(-e)[..., None]).float().to(torch.float8_e4m3fn)
+        return (q.double() * torch.exp2(e)[..., None]).reshape(a32.shape)
+    b = a32.reshape(*a32.shape[:-1], n // 128, 128)
+    s = b.abs().amax(-1).clamp_min(1e-10) / 448.0
+    q = (b / s[..., None]).to(torch.float8_e4m3fn)
+    return (q.double() * s.double()[..., None]).reshape(a32.shape)
+
+
+def brute_force(cfg, inp):
+    x, W1, W2 = _deq_all(cfg, inp)
+    idx, w = inp["topk_idx"].long(), inp["topk_w"].double()
+    T, I = cfg.T, cfg.I
+    out = torch.zeros(T, cfg.H, dtype=torch.float64)
+    for k in range(cfg.K):
+        valid = (idx[:, k] >= 0) & (idx[:, k] < cfg.E)
+        e = idx[:, k].clamp(0, cfg.E - 1)
+        h = torch.einsum("tnh,th->tn", W1[e], x)
+        g, u = h[:, :I], h[:, I:]
+        a = torch.nn.functional.silu(g) * u * w[:, k:k + 1]
+        ah = _requant_torch(a.float(), cfg.variant)
+        y = torch.einsum("thi,ti->th", W2[e], ah)
+        out += torch.where(valid[:, None], y, torch.zeros_like(y))
+    return out
+
+
+def run_oracle(cfg, inp, rows=None):
+    npi = W.to_numpy(inp)
+    rows = np.arange(cfg.T) if rows is None else rows
+    out, inter = O.forward(rows, npi["x"], npi["x_sf"], npi["topk_idx"], npi["topk_w"],
+                           O.expert_from_arrays(npi["w1"], npi["w1_sf"], npi["w2"], npi["w2_sf"]),
+                           cfg.H, cfg.I, cfg.E, cfg.variant, keep_intermediate=True)
+    return out, inter
+
+
+@pytest.mark.parametrize("cfg", [TINY_MX, TINY_F8, TINY_MX.with_(seed=5, K=3)], ids=["mx", "f8", "mx_k3"])
+def test_oracle_matches_dense_brute_force(cfg):
+    inp = W.make_inputs(cfg, "cpu")
+    out, _ = run_oracle(cfg, inp)
+    ref = O.bf16_rne(brute_force(cfg, inp).numpy())
+    assert np.isfinite(out).all() and np.abs(out).max() > 0
+    exact = np.mean(out == ref)
+    assert exact > 0.999, exact
+    assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
+
+
+def test_oracle_identity_weights_closed_form():
+    """W1 gate = 2*[I|0], up = [I|0] and W2 = [I;0] (exact in e2m1 with UE8M0 scales):
+    out[t, j<I] = bf16(sum_k deq(q(silu(2 x_j) * x_j * w_k))) and out[t, j>=I] = 0."""
+    cfg = TINY_MX.with_(seed=3)
+    inp = W.make_inputs(cfg, "cpu", with_weights=False)
+    E, H, I = cfg.E, cfg.H, cfg.I
+    eye = torch.zeros(I, H)
+    eye[:, :I] = torch.eye(I)
+    w1 = torch.cat([2.0 * eye, eye], 0)
+    w2 = torch.zeros(H, I)
+    w2[:I] = torch.eye(I)
+    p1, s1 = W.quant_e2m1_ue8m0(w1)
+    p2, s2 = W.quant_e2m1_ue8m0(w2)
+    inp.update(w1=p1.expand(E, -1, -1).contiguous(), w1_sf=s1.expand(E, -1, -1).contiguous(),
+               w2=p2.expand(E, -1, -1).contiguous(), w2_sf=s2.expand(E, -1, -1).contiguous())
+    out, _ = run_oracle(cfg, inp)
+    npi = W.to_numpy(inp)
+    for t in range(cfg.T):
+        xh = O.e4m3_decode(npi["x"][t]) * np.repeat(2.0 ** (npi["x_sf"][t].astype(int) - 127), 32)
+        acc = np.zeros(H)
+        for k in range(cfg.K):
+            xj = xh[:I]
+            a = (2 * xj) / (1 + np.exp(-2 * xj)) * xj * float(npi["topk_w"][t, k])
+            _, _, ah = O.requant_mx(a.astype(np.float32), 32)
+            acc[:I] += ah
+        assert np.array_equal(out[t], O.bf16_rne(acc))
+    assert np.all(out[:, I:] == 0)
+
+
+@pytest.mark.parametrize("zero", ["x", "w", "w2"])
+def test_oracle_zero_cases(zero):
+    cfg = TINY_MX.with_(seed=4)
+    inp = W.make_inputs(cfg, "cpu")
+    if zero == "x":
+        inp["x"].zero_()
+    elif zero == "w":
+        inp["topk_w"].zero_()
+    else:
+        inp["w2"].zero_()
+    out, inter = run_oracle(cfg, inp)
+    assert np.all(out == 0)
+
+
+def test_oracle_dense_mlp_special_case():
+    """E=1, K=1, w=1: a dense SwiGLU MLP with one requantisation of the hidden layer."""
+    cfg = W.Config("mlp", T=16, H=256, I=128, E=1, K=1, seed=9)
+    inp = W.make_inputs(cfg, "cpu")
+    inp["topk_w"].fill_(1.0)
+    out, _ = run_oracle(cfg, inp)
+    x, W1, W2 = _deq_all(cfg, inp)
+    h = x @ W1[0].T
+    a = torch.nn.functional.silu(h[:, :cfg.I]) * h[:, cfg.I:]
+    ref = _requant_torch(a.float(), "mx") @ W2[0].T
+    assert np.mean(out == O.bf16_rne(ref.numpy())) > 0.999
+
+
+def test_oracle_masked_slots_contribute_nothing():
+    cfg = TINY_MX.with_(seed=6, K=2)
+    inp = W.make_inputs(cfg, "cpu")
+    base, _ = run_oracle(cfg, inp)
+    inp2 = {k: v.clone() for k, v in inp.items()}
+    inp2["topk_idx"][:, 1] = -1
+    only0, _ = run_oracle(cfg, inp2)
+    inp3 = {k: v.clone() for k, v in inp.items()}
+    inp3["topk_idx"][:, 0] = -1
+    only1, _ = run_oracle(cfg, inp3)
+    assert not np.array_equal(base, only0)
+    # removing a slot removes exactly its contribution (up to the final bf16 rounding)
+    assert np.max(np.abs(O.bf16_rne(only0 + only1) - base)) <= 2.0 ** -6 * np.abs(base).max()
+    inp2["topk_idx"][:, 0] = -1
+    none, _ = run_oracle(cfg, inp2)
+    assert np.all(none == 0)
+
+
+def test_oracle_permutation_equivariance():
+    cfg = TINY_MX.with_(seed=8)
+    inp = W.make_inputs(cfg, "cpu")
+    out, _ = run_oracle(cfg, inp)
+    perm = torch.randperm(cfg.T, generator=torch.Generator().manual_seed(0))
+    inp2 = dict(inp)
+    for k in ("x", "x_sf", "topk_idx", "topk_w"):
+        inp2[k] = inp[k][perm].contiguous()
+    out2, _ = run_oracle(cfg, inp2)
+    assert np.array_equal(out2, out[perm.numpy()])
+
+
+def test_oracle_intermediate_codes_are_the_requant_of_the_activation():
+    cfg = TINY_MX.with_(seed=12)
+    inp = W.make_inputs(cfg, "cpu")
+    _, inter = run_oracle(cfg, inp)
+    x, W1, _ = _deq_all(cfg, inp)
+    t, k = 5, 1
+    e = int(inp["topk_idx"][t, k])
+    h = W1[e] @ x[t]
+    a = torch.nn.functional.silu(h[:cfg.I]) * h[cfg.I:] * float(inp["topk_w"][t, k])
+    codes, sf = inter[(t, k)]
+    assert np.array_equal(O.e4m3_decode(codes) * np.repeat(2.0 ** (sf.astype(int) - 127), 32),
+                          _requant_torch(a.float()[None], "mx")[0].numpy())
