@@ -1,0 +1,164 @@
+/*
+ * mm_moe.h — C ABI of the GB300 (sm_103a) MoE-layer forward.
+ *
+ * One call computes the forward of one MoE layer on one GPU, with every expert
+ * local (the MegaMoE data path of llm-infra-atlas "07 · MegaMoE", §1–§9,
+ * without its cross-GPU dispatch and scatter):
+ *   a1 dispatch    routing histogram, per-expert segment offsets, and a slot
+ *                  for every (token, k) pair, ascending token order inside an
+ *                  expert ("07 · MegaMoE" §4 and §7; nxmr.cn walkthrough §二.2.4);
+ *   a2 gather      activation rows and their scales copied into the pool;
+ *   a3 L1 GEMM     gate|up = x_hat · W1_hat^T per expert, block-scaled;
+ *   a4 L1 epilogue a = silu(gate) · up · topk_w, requantised to e4m3
+ *                  ("07 · MegaMoE" §8; MEGAMOE_SM90_DESIGN.md §10.1);
+ *   a5 L2 GEMM     y = a_hat · W2_hat^T per expert;
+ *   a6 L2 epilogue y written as fp32 partials [K][T][H];
+ *   a7 combine     out[t] = bf16(sum over k = 0..K-1 of the partials), fixed order
+ *                  (MEGAMOE_SM90_DESIGN.md §11.2).
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers to row-major, contiguous memory,
+ *     owned by the caller.  The library allocates no device memory and keeps no
+ *     state beyond a per-device cache of properties and kernel attributes.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: a return of MM_MOE_OK means the work was
+ *     enqueued.  Errors found on the device (wait timeouts, bad routing) are
+ *     reported by mm_moe_sync_status().
+ *   - Inputs are read-only.  `out` is fully overwritten.
+ *
+ * Numeric formats ("variant"):
+ *   MM_MOE_VARIANT_MX  e4m3 activations x e2m1 weights, one UE8M0 scale byte
+ *                      (value 2^(b-127)) per 32 contiguous elements along the
+ *                      contraction dimension; tcgen05 kind::mxf8f6f4.
+ *   MM_MOE_VARIANT_F8  e4m3 activations with one fp32 scale per 1x128, e4m3
+ *                      weights with one fp32 scale per 128x128 block; the
+ *                      intermediate is requantised per 128 with a raw fp32
+ *                      scale amax/448 (DeepGEMM PR #440, "Why the order and not
+ *                      the pool size"); tcgen05 kind::f8f6f4.
+ *
+ * Layouts (T tokens, H hidden, I intermediate, E experts, K top-k):
+ *   x        u8  [T, H]          e4m3 codes
+ *   x_sf     MX: u8 [T, H/32]    F8: f32 [T, H/128]
+ *   topk_idx i32 [T, K]          expert of slot k; any value < 0 masks the slot;
+ *                                values >= E are treated as masked and flagged
+ *                                (MM_MOE_ERR_BAD_ROUTING from mm_moe_sync_status)
+ *   topk_w   f32 [T, K]          router weight of slot k
+ *   w1       MX: u8 [E, 2I, H/2] (two e2m1 per byte, low nibble = even column)
+ *            F8: u8 [E, 2I, H]; rows [0, I) are the gate projection, [I, 2I) up
+ *   w2       MX: u8 [E, H, I/2]  F8: u8 [E, H, I]
+ *   w1_sf/w2_sf (canonical, input of mm_moe_prepare_weights only)
+ *            MX: u8 [E, 2I, H/32] and u8 [E, H, I/32]
+ *            F8: f32 [E, 2I/128, H/128] and f32 [E, H/128, I/128]
+ *   w1_sfp/w2_sfp  the scales in the layout the kernels read, written by
+ *            mm_moe_prepare_weights (sizes from mm_moe_weight_sf_size)
+ *   out      bf16 [T, H]
+ * Shape limits: H % 128 == 0, I % 128 == 0, 1 <= K <= 16, K <= E <= 1024,
+ * T >= 0 (T = 0 is a no-op).  w1/w2 must be 32-byte aligned, x/workspace
+ * 256-byte aligned.
+ */
+#ifndef MM_MOE_H_
+#define MM_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MM_MOE_OK 0
+#define MM_MOE_ERR_INVALID_ARG 1          /* null pointer, bad shape, misalignment */
+#define MM_MOE_ERR_UNSUPPORTED 2          /* not an sm_103a/sm_100-family device, or option not built */
+#define MM_MOE_ERR_CUDA 3                 /* a CUDA runtime/driver call failed */
+#define MM_MOE_ERR_TIMEOUT 4              /* a device wait passed its deadline (sync_status only) */
+#define MM_MOE_ERR_BAD_ROUTING 5          /* topk_idx held values >= E (sync_status only) */
+#define MM_MOE_ERR_WORKSPACE_TOO_SMALL 6
+
+#define MM_MOE_VARIANT_MX 0
+#define MM_MOE_VARIANT_F8 1
+
+typedef struct mm_moe_options {
+  int variant;                  /* MM_MOE_VARIANT_MX (default) or MM_MOE_VARIANT_F8 */
+  int fused;                    /* 1 (default): one persistent kernel runs gather, L1 and L2 as one
+                                   lag-ordered task stream; 0: separate gather / L1 / L2 launches */
+  int lag_units;                /* fused path: lag of L2 behind L1 in units of 8 M-blocks; -1 = auto */
+  int retain_intermediate;      /* keep the whole requantised intermediate readable after the call
+                                   (mm_moe_read_intermediate) */
+  unsigned wait_timeout_ms;     /* deadline of every device-side wait; 0 = default (2000 ms) */
+  int num_sms;                  /* persistent grid size; 0 = all SMs */
+  int debug_flags;              /* bit 0: the L1 epilogue also writes its raw fp32 gate|up accumulators
+                                   to the DEBUG workspace region ([P, 2I], pool-row order) and the
+                                   call stops after L1; 0 for normal use */
+  int reserved[7];
+} mm_moe_options;
+
+/* Fill `opt` with the defaults. */
+void mm_moe_default_options(mm_moe_options* opt);
+
+/* Bytes of workspace mm_moe_forward needs for this shape (opt may be NULL = defaults). */
+int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E, int K, size_t* bytes);
+
+/* Bytes of the prepared scale buffers w1_sfp / w2_sfp. */
+int mm_moe_weight_sf_size(const mm_moe_options* opt, int H, int I, int E, size_t* w1_sfp_bytes,
+                          size_t* w2_sfp_bytes);
+
+/* One-time relayout of the weight scales into the layout the GEMM kernels
+ * stream (MX: 512-byte blocks, one per 128 weight rows x 128 K, in the
+ * tensor-memory scale-factor order; the L1 blocks pair 64 gate rows with the
+ * matching 64 up rows).  The codes w1/w2 are used as given.
+ * (llm-infra-atlas "07 · MegaMoE" §11: the weights are transformed once before use.) */
+int mm_moe_prepare_weights(const mm_moe_options* opt, const void* w1_sf, const void* w2_sf, int H, int I,
+                           int E, void* w1_sfp, void* w2_sfp, void* stream);
+
+/* The forward (steps a1–a7 above).  `workspace` must hold mm_moe_workspace_size()
+ * bytes; its contents need no initialisation and are overwritten. */
+int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w,
+                   const void* w1, const void* w1_sfp, const void* w2, const void* w2_sfp, void* out, int T,
+                   int H, int I, int E, int K, void* workspace, size_t workspace_bytes,
+                   const mm_moe_options* opt, void* stream);
+
+/* Step a1 alone, into caller buffers: cnt[E], blk_off[E+1] (in blocks of
+ * block_m rows), slot[T*K] (pool row or -1), src[src_capacity] (t*K+k or -1 for
+ * padding rows; rows past blk_off[E]*block_m are left untouched).  block_m must
+ * be a multiple of 16 in [16, 256]; src_capacity >= T*K + E*(block_m-1).
+ * `status` is a device int[4], zeroed by the caller, that receives
+ * MM_MOE_ERR_BAD_ROUTING when topk_idx holds values >= E. */
+int mm_moe_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
+                    int32_t* blk_off, int32_t* slot, int32_t* src, int64_t src_capacity, int32_t* status,
+                    void* stream);
+
+/* Copy the routing of the last forward out of a workspace (same shapes as mm_moe_dispatch;
+ * block_m is reported through *block_m). */
+int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
+                        int32_t* cnt, int32_t* blk_off, int32_t* slot, int32_t* src, int* block_m,
+                        void* stream);
+
+/* Copy the requantised intermediate (step a4) of pool rows [0, rows) out of a
+ * workspace: codes u8 [rows, I] and scales (MX: u8 [rows, I/32]; F8: f32
+ * [rows, I/128]).  Needs opt->retain_intermediate on the forward call when the
+ * fused path recycles its activation ring. */
+int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E,
+                             int K, int64_t rows, uint8_t* codes, void* sf, void* stream);
+
+/* Diagnostics: device address and size of one internal region of a
+ * workspace laid out for this shape and these options.  region: 0 status,
+ * 1 cnt, 2 blk_off, 3 slot, 4 src, 5 pooled activations, 6 their scales,
+ * 7 intermediate codes, 8 intermediate scales, 9 fp32 partials [K, T, H],
+ * 10 debug accumulators (debug_flags bit 0 only). */
+int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
+                            int region, void** ptr, size_t* bytes);
+
+/* Synchronise `stream`, then read the device status word of `workspace`.
+ * Returns MM_MOE_OK, MM_MOE_ERR_TIMEOUT, MM_MOE_ERR_BAD_ROUTING or
+ * MM_MOE_ERR_CUDA; *where (if non-NULL) receives the code of the check that
+ * fired.  The word is cleared by the next forward. */
+int mm_moe_sync_status(const void* workspace, void* stream, int* where);
+
+/* Human-readable name of a return code. */
+const char* mm_moe_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MM_MOE_H_ */

@@ -1,0 +1,216 @@
+"""Python binding of libmm_moe.so (the GB300 MoE-layer forward).
+
+Argument marshalling only: every step of the forward runs in the library's CUDA
+kernels.  The C entry points are exposed under their own names (taking integer
+device pointers); the tensor helpers below only turn torch tensors into
+pointers and raise on a non-zero status.  There is no fallback: importing the
+binding fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmm_moe.so")
+
+MM_MOE_OK = 0
+MM_MOE_ERR_INVALID_ARG = 1
+MM_MOE_ERR_UNSUPPORTED = 2
+MM_MOE_ERR_CUDA = 3
+MM_MOE_ERR_TIMEOUT = 4
+MM_MOE_ERR_BAD_ROUTING = 5
+MM_MOE_ERR_WORKSPACE_TOO_SMALL = 6
+MM_MOE_VARIANT_MX = 0
+MM_MOE_VARIANT_F8 = 1
+
+# every symbol include/mm_moe.h declares
+EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_size", "mm_moe_prepare_weights",
+           "mm_moe_forward", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
+           "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region"]
+
+
+class mm_moe_options(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("fused", ctypes.c_int), ("lag_units", ctypes.c_int),
+                ("retain_intermediate", ctypes.c_int), ("wait_timeout_ms", ctypes.c_uint),
+                ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+
+
+class MMError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {mm_moe_status_string(code)} ({code})")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_OPT = ctypes.POINTER(mm_moe_options)
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with moe_expert_forward_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "mm_moe_default_options": (None, [_OPT]),
+            "mm_moe_workspace_size": (_I, [_OPT, _I, _I, _I, _I, _I, ctypes.POINTER(_SZ)]),
+            "mm_moe_weight_sf_size": (_I, [_OPT, _I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+            "mm_moe_prepare_weights": (_I, [_OPT, _P, _P, _I, _I, _I, _P, _P, _P]),
+            "mm_moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _OPT, _P]),
+            "mm_moe_dispatch": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
+            "mm_moe_read_routing": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P]),
+            "mm_moe_read_intermediate": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _I64, _P, _P, _P]),
+            "mm_moe_sync_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
+            "mm_moe_status_string": (ctypes.c_char_p, [_I]),
+            "mm_moe_workspace_region": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P),
+                                             ctypes.POINTER(_SZ)]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ C entry points, same names
+def mm_moe_default_options(opt: Optional[mm_moe_options] = None) -> mm_moe_options:
+    opt = opt or mm_moe_options()
+    lib().mm_moe_default_options(ctypes.byref(opt))
+    return opt
+
+
+def mm_moe_workspace_size(opt, T, H, I, E, K) -> int:
+    n = _SZ(0)
+    _check(lib().mm_moe_workspace_size(_opt(opt), T, H, I, E, K, ctypes.byref(n)), "mm_moe_workspace_size")
+    return n.value
+
+
+def mm_moe_weight_sf_size(opt, H, I, E):
+    a, b = _SZ(0), _SZ(0)
+    _check(lib().mm_moe_weight_sf_size(_opt(opt), H, I, E, ctypes.byref(a), ctypes.byref(b)), "mm_moe_weight_sf_size")
+    return a.value, b.value
+
+
+def mm_moe_prepare_weights(opt, w1_sf, w2_sf, H, I, E, w1_sfp, w2_sfp, stream) -> int:
+    return lib().mm_moe_prepare_weights(_opt(opt), w1_sf, w2_sf, H, I, E, w1_sfp, w2_sfp, stream)
+
+
+def mm_moe_forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, T, H, I, E, K, workspace, ws_bytes,
+                   opt, stream) -> int:
+    return lib().mm_moe_forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, T, H, I, E, K, workspace,
+                                ws_bytes, _opt(opt), stream)
+
+
+def mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, status, stream) -> int:
+    return lib().mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, status, stream)
+
+
+def mm_moe_read_routing(workspace, opt, T, H, I, E, K, cnt, blk_off, slot, src, stream):
+    bm = _I(0)
+    r = lib().mm_moe_read_routing(workspace, _opt(opt), T, H, I, E, K, cnt, blk_off, slot, src, ctypes.byref(bm),
+                                  stream)
+    return r, bm.value
+
+
+def mm_moe_read_intermediate(workspace, opt, T, H, I, E, K, rows, codes, sf, stream) -> int:
+    return lib().mm_moe_read_intermediate(workspace, _opt(opt), T, H, I, E, K, rows, codes, sf, stream)
+
+
+def mm_moe_sync_status(workspace, stream):
+    where = _I(0)
+    r = lib().mm_moe_sync_status(workspace, stream, ctypes.byref(where))
+    return r, where.value
+
+
+def mm_moe_status_string(code: int) -> str:
+    try:
+        return lib().mm_moe_status_string(code).decode()
+    except ImportError:
+        return f"status {code}"
+
+
+def mm_moe_workspace_region(workspace, opt, T, H, I, E, K, region):
+    p, n = _P(0), _SZ(0)
+    _check(lib().mm_moe_workspace_region(workspace, _opt(opt), T, H, I, E, K, region, ctypes.byref(p),
+                                         ctypes.byref(n)), "mm_moe_workspace_region")
+    return p.value or 0, n.value
+
+
+REGIONS = {"status": 0, "cnt": 1, "blk_off": 2, "slot": 3, "src": 4, "pool_x": 5, "pool_x_sf": 6, "pool2": 7,
+           "pool2_sf": 8, "partials": 9, "debug": 10}
+
+
+def workspace_view(workspace, opt, T, H, I, E, K, region: str, dtype=None):
+    """A torch view of one workspace region (diagnostics and tests)."""
+    import torch
+    p, n = mm_moe_workspace_region(_ptr(workspace), opt, T, H, I, E, K, REGIONS[region])
+    off = p - workspace.data_ptr()
+    v = workspace[off:off + n]
+    return v.view(dtype) if dtype is not None else v
+
+
+def _opt(opt):
+    return ctypes.byref(opt) if opt is not None else None
+
+
+def _check(code: int, what: str):
+    if code != MM_MOE_OK:
+        raise MMError(code, what)
+
+
+# ------------------------------------------------------------------ torch-tensor marshalling
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def options(variant: int = MM_MOE_VARIANT_MX, **kw) -> mm_moe_options:
+    o = mm_moe_default_options()
+    o.variant = variant
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def prepare_weights(w1_sf, w2_sf, H, I, E, opt=None, stream=None):
+    """Return (w1_sfp, w2_sfp) device tensors in the kernels' scale layout."""
+    import torch
+    opt = opt or options()
+    n1, n2 = mm_moe_weight_sf_size(opt, H, I, E)
+    a = torch.empty(n1, dtype=torch.uint8, device=w1_sf.device)
+    b = torch.empty(n2, dtype=torch.uint8, device=w1_sf.device)
+    _check(mm_moe_prepare_weights(opt, _ptr(w1_sf), _ptr(w2_sf), H, I, E, _ptr(a), _ptr(b), _stream(stream)),
+           "mm_moe_prepare_weights")
+    return a, b
+
+
+def alloc_workspace(T, H, I, E, K, opt=None, device="cuda"):
+    import torch
+    n = mm_moe_workspace_size(opt or options(), T, H, I, E, K)
+    return torch.empty(max(n, 1024), dtype=torch.uint8, device=device)
+
+
+def forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, H, I, E, workspace, opt=None, stream=None):
+    T, K = topk_idx.shape
+    _check(mm_moe_forward(_ptr(x), _ptr(x_sf), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w1_sfp), _ptr(w2),
+                          _ptr(w2_sfp), _ptr(out), T, H, I, E, K, _ptr(workspace), workspace.numel(),
+                          opt or options(), _stream(stream)), "mm_moe_forward")
+    return out
+
+
+def sync_status(workspace, stream=None):
+    code, where = mm_moe_sync_status(_ptr(workspace), _stream(stream))
+    return code, where

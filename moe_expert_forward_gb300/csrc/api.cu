@@ -1,0 +1,338 @@
+// Host side of the C ABI: argument checks, workspace layout, TMA descriptors
+// and the launch sequence of one forward.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace mm {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags) {
+  Layout L{};
+  L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = kBT;
+  const int64_t pairs = static_cast<int64_t>(T) * K;
+  const int64_t live_experts = pairs < E ? pairs : E;
+  L.P = static_cast<int64_t>(align_up(static_cast<size_t>(pairs + live_experts * (kBT - 1)), kBT));
+  L.nblk_cap = L.P / kBT;
+  L.KB1 = H / 128;
+  L.KB2 = I / 128;
+  size_t o = 0;
+  L.status = o; o += 256;
+  L.cnt = o; o = align_up(o + sizeof(int) * E, 256);
+  L.blk_off = o; o = align_up(o + sizeof(int) * (E + 1), 256);
+  L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
+  L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
+  L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
+  L.pool_x_sf = o;
+  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? static_cast<size_t>(L.P) * H / 32
+                                                 : static_cast<size_t>(L.P) * (H / 128) * sizeof(float)), 1024);
+  L.pool2 = o; o = align_up(o + static_cast<size_t>(L.P) * I, 1024);
+  L.pool2_sf = o;
+  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? static_cast<size_t>(L.P) * I / 32
+                                                 : static_cast<size_t>(L.P) * (I / 128) * sizeof(float)), 1024);
+  L.part = o; o = align_up(o + static_cast<size_t>(pairs) * H * sizeof(float), 1024);
+  L.dbg = o;
+  L.dbg_bytes = (debug_flags & 1) ? static_cast<size_t>(L.P) * 2 * I * sizeof(float) : 0;
+  o = align_up(o + L.dbg_bytes, 1024);
+  L.total = o;
+  return L;
+}
+
+WsPtrs ws_ptrs(void* ws, const Layout& L) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  WsPtrs W;
+  W.status = reinterpret_cast<int*>(b + L.status);
+  W.cnt = reinterpret_cast<int*>(b + L.cnt);
+  W.blk_off = reinterpret_cast<int*>(b + L.blk_off);
+  W.slot = reinterpret_cast<int*>(b + L.slot);
+  W.src = reinterpret_cast<int*>(b + L.src);
+  W.pool_x = b + L.pool_x;
+  W.pool_x_sf = b + L.pool_x_sf;
+  W.pool2 = b + L.pool2;
+  W.pool2_sf = b + L.pool2_sf;
+  W.part = reinterpret_cast<float*>(b + L.part);
+  W.dbg = L.dbg_bytes ? reinterpret_cast<float*>(b + L.dbg) : nullptr;
+  return W;
+}
+
+const DevInfo& dev_info() {
+  static DevInfo infos[64];
+  static bool have[64] = {false};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  std::lock_guard<std::mutex> g(mu);
+  if (!have[dev]) {
+    cudaDeviceProp p;
+    cudaGetDeviceProperties(&p, dev);
+    infos[dev].sms = p.multiProcessorCount;
+    infos[dev].cc_major = p.major;
+    infos[dev].cc_minor = p.minor;
+    infos[dev].smem_optin = p.sharedMemPerBlockOptin;
+    have[dev] = true;
+  }
+  return infos[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS && getenv("MM_MOE_DEBUG"))
+    fprintf(stderr, "mm_moe: cuTensorMapEncodeTiled(dt=%d inner=%llu outer=%llu stride=%llu box=%u x %u) = %d\n",
+            static_cast<int>(dt), (unsigned long long)inner, (unsigned long long)outer,
+            (unsigned long long)row_stride_bytes, box_inner, box_outer, static_cast<int>(r));
+  return r;
+}
+
+}  // namespace mm
+
+using namespace mm;
+
+namespace {
+
+mm_moe_options resolve(const mm_moe_options* opt) {
+  mm_moe_options o;
+  if (opt) o = *opt; else mm_moe_default_options(&o);
+  if (o.wait_timeout_ms == 0) o.wait_timeout_ms = 2000;
+  return o;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int T, int H, int I, int E, int K) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || K <= 0) return MM_MOE_ERR_INVALID_ARG;
+  if (H % 128 || I % 128) return MM_MOE_ERR_INVALID_ARG;
+  if (K > kMaxK || K > E || E > kMaxE) return MM_MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t(1) << 30)) return MM_MOE_ERR_INVALID_ARG;
+  return MM_MOE_OK;
+}
+
+int device_supported() {
+  const DevInfo& d = dev_info();
+  return (d.cc_major == 10 && d.cc_minor == 3) ? MM_MOE_OK : MM_MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+void mm_moe_default_options(mm_moe_options* opt) {
+  if (!opt) return;
+  memset(opt, 0, sizeof(*opt));
+  opt->variant = MM_MOE_VARIANT_MX;
+  opt->fused = 0;
+  opt->lag_units = -1;
+  opt->retain_intermediate = 0;
+  opt->wait_timeout_ms = 2000;
+  opt->num_sms = 0;
+}
+
+int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E, int K, size_t* bytes) {
+  if (!bytes) return MM_MOE_ERR_INVALID_ARG;
+  const mm_moe_options o = resolve(opt);
+  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(T, H, I, E, K, o.variant, o.debug_flags).total;
+  return MM_MOE_OK;
+}
+
+int mm_moe_weight_sf_size(const mm_moe_options* opt, int H, int I, int E, size_t* w1b, size_t* w2b) {
+  const mm_moe_options o = resolve(opt);
+  if (!w1b || !w2b) return MM_MOE_ERR_INVALID_ARG;
+  if (int r = check_shape(0, H, I, E, 1)) return r;
+  if (o.variant == MM_MOE_VARIANT_MX) {
+    *w1b = static_cast<size_t>(E) * 2 * I * (H / 32);
+    *w2b = static_cast<size_t>(E) * H * (I / 32);
+  } else {
+    *w1b = static_cast<size_t>(E) * (2 * I / 128) * (H / 128) * sizeof(float);
+    *w2b = static_cast<size_t>(E) * (H / 128) * (I / 128) * sizeof(float);
+  }
+  return MM_MOE_OK;
+}
+
+int mm_moe_prepare_weights(const mm_moe_options* opt, const void* w1_sf, const void* w2_sf, int H, int I, int E,
+                           void* w1_sfp, void* w2_sfp, void* stream) {
+  const mm_moe_options o = resolve(opt);
+  if (!w1_sf || !w2_sf || !w1_sfp || !w2_sfp) return MM_MOE_ERR_INVALID_ARG;
+  if (int r = check_shape(0, H, I, E, 1)) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (o.variant == MM_MOE_VARIANT_MX) {
+    if (!aligned(w1_sf, 4) || !aligned(w2_sf, 4) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
+      return MM_MOE_ERR_INVALID_ARG;
+    e = launch_prepare_sf_mx(static_cast<const uint8_t*>(w1_sf), static_cast<const uint8_t*>(w2_sf), H, I, E,
+                             static_cast<uint8_t*>(w1_sfp), static_cast<uint8_t*>(w2_sfp), s);
+  } else {
+    size_t b1, b2;
+    mm_moe_weight_sf_size(&o, H, I, E, &b1, &b2);
+    e = cudaMemcpyAsync(w1_sfp, w1_sf, b1, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(w2_sfp, w2_sf, b2, cudaMemcpyDeviceToDevice, s);
+  }
+  return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt, int32_t* blk_off,
+                    int32_t* slot, int32_t* src, int64_t src_capacity, int32_t* status, void* stream) {
+  if (check_shape(T, 128, 128, E, K)) return MM_MOE_ERR_INVALID_ARG;
+  if (block_m < 16 || block_m > 256 || block_m % 16) return MM_MOE_ERR_INVALID_ARG;
+  if (!cnt || !blk_off || !status || (T > 0 && (!topk_idx || !slot || !src))) return MM_MOE_ERR_INVALID_ARG;
+  const int64_t pairs = static_cast<int64_t>(T) * K;
+  const int64_t live = pairs < E ? pairs : E;
+  if (src_capacity < pairs + live * (block_m - 1)) return MM_MOE_ERR_INVALID_ARG;
+  if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
+  cudaError_t e = launch_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, status,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, const float* topk_w, const void* w1,
+                   const void* w1_sfp, const void* w2, const void* w2_sfp, void* out, int T, int H, int I, int E,
+                   int K, void* workspace, size_t workspace_bytes, const mm_moe_options* opt, void* stream) {
+  const mm_moe_options o = resolve(opt);
+  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
+  if (T == 0) return MM_MOE_OK;
+  if (!x || !x_sf || !topk_idx || !topk_w || !w1 || !w1_sfp || !w2 || !w2_sfp || !out || !workspace)
+    return MM_MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x_sf, 4) || !aligned(w1, 32) || !aligned(w2, 32) || !aligned(out, 16) ||
+      !aligned(workspace, 1024) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
+    return MM_MOE_ERR_INVALID_ARG;
+  if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
+  if (o.variant != MM_MOE_VARIANT_MX || o.fused) return MM_MOE_ERR_UNSUPPORTED;
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
+  const WsPtrs W = ws_ptrs(workspace, L);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
+
+  cudaError_t e = cudaMemsetAsync(W.status, 0, 16, s);
+  if (e == cudaSuccess) e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, s);
+  if (e == cudaSuccess) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, s);
+  GemmLaunch g{&L, &W, nullptr, nullptr, topk_w, W.dbg, static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull, grid};
+  if (e == cudaSuccess) {
+    g.w = static_cast<const uint8_t*>(w1);
+    g.wsfp = static_cast<const uint8_t*>(w1_sfp);
+    e = launch_gemm_mx_l1(g, s);
+  }
+  if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+  if (e == cudaSuccess) {
+    g.w = static_cast<const uint8_t*>(w2);
+    g.wsfp = static_cast<const uint8_t*>(w2_sfp);
+    e = launch_gemm_mx_l2(g, s);
+  }
+  if (e == cudaSuccess) e = launch_combine(L, W, topk_idx, out, s);
+  if (e != cudaSuccess) {
+    if (getenv("MM_MOE_DEBUG")) fprintf(stderr, "mm_moe_forward: %s\n", cudaGetErrorString(e));
+    return MM_MOE_ERR_CUDA;
+  }
+  return MM_MOE_OK;
+}
+
+int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
+                        int32_t* cnt, int32_t* blk_off, int32_t* slot, int32_t* src, int* block_m, void* stream) {
+  const mm_moe_options o = resolve(opt);
+  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (!workspace) return MM_MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (cnt) e = cudaMemcpyAsync(cnt, W.cnt, sizeof(int) * E, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && blk_off) e = cudaMemcpyAsync(blk_off, W.blk_off, sizeof(int) * (E + 1), cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && slot && T > 0)
+    e = cudaMemcpyAsync(slot, W.slot, sizeof(int) * static_cast<size_t>(T) * K, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && src && L.P > 0)
+    e = cudaMemcpyAsync(src, W.src, sizeof(int) * static_cast<size_t>(L.P), cudaMemcpyDeviceToDevice, s);
+  if (block_m) *block_m = L.BT;
+  return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
+                             int64_t rows, uint8_t* codes, void* sf, void* stream) {
+  const mm_moe_options o = resolve(opt);
+  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (!workspace || !codes || !sf || rows < 0) return MM_MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  if (rows > L.P) return MM_MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MM_MOE_OK;
+  const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
+  cudaError_t e = launch_read_intermediate(L, W, rows, codes, sf, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
+                            int region, void** ptr, size_t* bytes) {
+  const mm_moe_options o = resolve(opt);
+  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (!ptr || !bytes) return MM_MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  const size_t offs[12] = {L.status, L.cnt, L.blk_off, L.slot, L.src, L.pool_x, L.pool_x_sf, L.pool2, L.pool2_sf,
+                           L.part, L.dbg, L.total};
+  if (region < 0 || region > 10) return MM_MOE_ERR_INVALID_ARG;
+  size_t n;
+  if (region == 10) n = L.dbg_bytes;
+  else if (region == 0) n = 16;
+  else if (region == 1) n = sizeof(int) * E;
+  else if (region == 2) n = sizeof(int) * (E + 1);
+  else if (region == 3) n = sizeof(int) * static_cast<size_t>(T) * K;
+  else if (region == 4) n = sizeof(int) * static_cast<size_t>(L.P);
+  else if (region == 9) n = sizeof(float) * static_cast<size_t>(T) * K * H;
+  else n = offs[region + 1] - offs[region];
+  *ptr = static_cast<uint8_t*>(const_cast<void*>(workspace)) + offs[region];
+  *bytes = n;
+  return MM_MOE_OK;
+}
+
+int mm_moe_sync_status(const void* workspace, void* stream, int* where) {
+  if (!workspace) return MM_MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MM_MOE_ERR_CUDA;
+  int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MM_MOE_ERR_CUDA;
+  if (where) *where = h[1];
+  return h[0];
+}
+
+const char* mm_moe_status_string(int code) {
+  switch (code) {
+    case MM_MOE_OK: return "ok";
+    case MM_MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MM_MOE_ERR_UNSUPPORTED: return "unsupported device or option";
+    case MM_MOE_ERR_CUDA: return "CUDA error";
+    case MM_MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MM_MOE_ERR_BAD_ROUTING: return "topk_idx holds expert ids >= E";
+    case MM_MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

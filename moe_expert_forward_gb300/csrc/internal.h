@@ -1,0 +1,82 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mm_moe.h"
+
+namespace mm {
+
+constexpr int kBT = 128;        // tokens per pool block (MMA N upper bound; one scale chunk)
+constexpr int kBK = 128;        // contraction elements per pipeline stage
+constexpr int kSFChunk = 512;   // bytes of one 128-row x 128-K scale chunk (MX)
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 16;
+
+// Byte offsets of every buffer inside the caller's workspace.
+struct Layout {
+  int T, H, I, E, K, variant, BT;
+  int64_t P;                 // pool row capacity (multiple of BT)
+  int64_t nblk_cap;          // P / BT
+  int KB1, KB2;              // H/128, I/128
+  size_t status, cnt, blk_off, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, total;
+};
+
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0);
+
+// Device pointers resolved from a workspace.
+struct WsPtrs {
+  int* status;
+  int* cnt;
+  int* blk_off;
+  int* slot;
+  int* src;
+  uint8_t* pool_x;
+  uint8_t* pool_x_sf;
+  uint8_t* pool2;
+  uint8_t* pool2_sf;
+  float* part;
+  float* dbg;
+};
+WsPtrs ws_ptrs(void* ws, const Layout& L);
+
+struct DevInfo {
+  int sms;
+  int cc_major, cc_minor;
+  size_t smem_optin;
+};
+const DevInfo& dev_info();
+
+// ---- launchers (return cudaError_t of the launch)
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
+                            int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, cudaStream_t s);
+cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
+                          cudaStream_t s);
+cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out,
+                           cudaStream_t s);
+cudaError_t launch_prepare_sf_mx(const uint8_t* w1_sf, const uint8_t* w2_sf, int H, int I, int E,
+                                 uint8_t* w1_sfp, uint8_t* w2_sfp, cudaStream_t s);
+cudaError_t launch_read_intermediate(const Layout& L, const WsPtrs& W, int64_t rows, uint8_t* codes,
+                                     void* sf, cudaStream_t s);
+
+struct GemmLaunch {
+  const Layout* L;
+  const WsPtrs* W;
+  const uint8_t* w;          // weights (w1 or w2)
+  const uint8_t* wsfp;       // prepared weight scales
+  const float* topk_w;
+  float* dbg;               // L1 raw accumulators (debug_flags bit 0) or null
+  uint64_t timeout_ns;
+  int grid;
+};
+cudaError_t launch_gemm_mx_l1(const GemmLaunch& g, cudaStream_t s);
+cudaError_t launch_gemm_mx_l2(const GemmLaunch& g, cudaStream_t s);
+
+// TMA descriptor creation through the driver entry point.
+CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle swz);
+
+}  // namespace mm

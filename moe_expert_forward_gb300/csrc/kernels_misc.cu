@@ -1,0 +1,300 @@
+// Dispatch (routing histogram, segment offsets, stable slots), gather into the
+// pool, fixed-order combine, weight-scale relayout and intermediate read-back.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mm {
+
+// Byte offset of (row r, 32-element scale block kk in 0..3) inside a 512-byte
+// scale chunk that covers 128 rows x 128 contraction elements.  The chunk is the
+// source of one tcgen05.cp.32x128b.warpx4: 16-byte line (r % 32) holds the four
+// words of rows r%32, r%32+32, r%32+64, r%32+96; word byte kk is the scale of
+// contraction block kk.
+__host__ __device__ __forceinline__ int sf_chunk_offset(int r, int kk) {
+  return (r & 31) * 16 + (r >> 5) * 4 + kk;
+}
+
+// ----------------------------------------------------------------------------- dispatch
+// One CTA of 1024 threads.  Flat pairs p = t*K + k are split into 32 contiguous
+// ranges, one per warp.  Pass 1 counts per (warp, expert); an exclusive scan over
+// warps gives each warp its starting rank inside every expert; pass 2 re-walks
+// the same pairs and ranks equal experts inside each 32-pair step with
+// __match_any_sync, so the slot order is ascending p (= ascending token, then k).
+__global__ void __launch_bounds__(1024, 1)
+    dispatch_kernel(const int32_t* __restrict__ idx, int T, int K, int E, int BT, int32_t* __restrict__ cnt,
+                    int32_t* __restrict__ blk_off, int32_t* __restrict__ slot, int32_t* __restrict__ src,
+                    int32_t* __restrict__ status) {
+  extern __shared__ int wc[];               // [32][E]
+  __shared__ int s_blk[kMaxE + 1];
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_wsum[32];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int64_t TK = static_cast<int64_t>(T) * K;
+  for (int i = tid; i < 32 * E; i += blockDim.x) wc[i] = 0;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  const int64_t per = ((TK + 1023) / 1024) * 32;
+  const int64_t beg = static_cast<int64_t>(w) * per;
+  const int64_t end = (beg + per < TK) ? beg + per : TK;
+  int* my = wc + w * E;
+  for (int64_t base = beg; base < end; base += 32) {
+    const int64_t p = base + lane;
+    const int e = (p < end) ? __ldg(idx + p) : -1;
+    const bool valid = (e >= 0) && (e < E);
+    if (p < end && (e >= E || e < -1)) s_bad = 1;
+    const unsigned m = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid && lane == __ffs(m) - 1) my[e] += __popc(m);
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // counts and per-warp exclusive offsets inside each expert
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int ww = 0; ww < 32; ++ww) {
+      const int c = wc[ww * E + e];
+      wc[ww * E + e] = run;
+      run += c;
+    }
+    cnt[e] = run;
+    s_cnt[e] = run;
+    s_blk[e] = (run + BT - 1) / BT;
+  }
+  __syncthreads();
+
+  // exclusive scan of blocks per expert (E <= 1024: one value per thread)
+  {
+    int v = (tid < E) ? s_blk[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wsum[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      int ws = s_wsum[lane];
+      int wi = ws;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += n;
+      }
+      s_wsum[lane] = wi - ws;       // exclusive warp prefix
+    }
+    __syncthreads();
+    const int excl = incl - v + s_wsum[w];
+    __syncthreads();
+    if (tid < E) s_blk[tid] = excl;
+    if (tid == E - 1) s_blk[E] = excl + v;
+    __syncthreads();
+  }
+  for (int e = tid; e <= E; e += blockDim.x) blk_off[e] = s_blk[e];
+
+  // pass 2: slots and inverse map
+  for (int64_t base = beg; base < end; base += 32) {
+    const int64_t p = base + lane;
+    const int e = (p < end) ? __ldg(idx + p) : -1;
+    const bool valid = (e >= 0) && (e < E);
+    const unsigned m = __match_any_sync(0xffffffffu, valid ? e : -1);
+    int before = 0;
+    if (valid) before = my[e];
+    __syncwarp();
+    if (valid) {
+      const int rank = __popc(m & ((1u << lane) - 1u));
+      const int64_t pos = static_cast<int64_t>(s_blk[e]) * BT + before + rank;
+      slot[p] = static_cast<int32_t>(pos);
+      src[pos] = static_cast<int32_t>(p);
+      if (lane == __ffs(m) - 1) my[e] = before + __popc(m);
+    } else if (p < end) {
+      slot[p] = -1;
+    }
+    __syncwarp();
+  }
+  // padding rows of every segment
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int64_t lo = static_cast<int64_t>(s_blk[e]) * BT + s_cnt[e];
+    const int64_t hi = static_cast<int64_t>(s_blk[e + 1]) * BT;
+    for (int64_t r = lo; r < hi; ++r) src[r] = -1;
+  }
+  if (tid == 0 && s_bad) atomicCAS(status, 0, MM_MOE_ERR_BAD_ROUTING);
+}
+
+cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
+                            int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(32) * E * sizeof(int);
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         32 * kMaxE * static_cast<int>(sizeof(int)));
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  dispatch_kernel<<<1, 1024, smem, s>>>(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, status);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- gather
+// One warp per pool row: copies the token's H code bytes and its scales.  MX
+// scales go to the 512-byte chunk layout the MMA consumes; F8 scales to a plain
+// [P, H/128] fp32 array.
+__global__ void __launch_bounds__(256)
+    gather_kernel(const int32_t* __restrict__ blk_off_end, const int32_t* __restrict__ src, int K, int H,
+                  int BT, int variant, const uint8_t* __restrict__ x, const void* __restrict__ x_sf,
+                  uint8_t* __restrict__ pool_x, uint8_t* __restrict__ pool_x_sf) {
+  const int64_t rows = static_cast<int64_t>(*blk_off_end) * BT;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int KB = H / 128;
+  for (int64_t r = warp0; r < rows; r += nwarps) {
+    const int s = __ldg(src + r);
+    if (s < 0) continue;
+    const int64_t t = s / K;
+    const uint4* srow = reinterpret_cast<const uint4*>(x + t * H);
+    uint4* drow = reinterpret_cast<uint4*>(pool_x + r * H);
+    for (int i = lane; i < H / 16; i += 32) drow[i] = __ldg(srow + i);
+    if (variant == MM_MOE_VARIANT_MX) {
+      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(x_sf) + t * (H / 32));
+      const int rr = static_cast<int>(r % BT);
+      const int64_t blk = r / BT;
+      for (int kb = lane; kb < KB; kb += 32)
+        *reinterpret_cast<uint32_t*>(pool_x_sf + (blk * KB + kb) * kSFChunk + sf_chunk_offset(rr, 0)) =
+            __ldg(ssf + kb);
+    } else {
+      const float* ssf = static_cast<const float*>(x_sf) + t * KB;
+      float* dsf = reinterpret_cast<float*>(pool_x_sf) + r * KB;
+      for (int kb = lane; kb < KB; kb += 32) dsf[kb] = __ldg(ssf + kb);
+    }
+  }
+}
+
+cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
+                          cudaStream_t s) {
+  const int grid = dev_info().sms * 4;
+  gather_kernel<<<grid, 256, 0, s>>>(W.blk_off + L.E, W.src, L.K, L.H, L.BT, L.variant, x, x_sf, W.pool_x,
+                                     W.pool_x_sf);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- combine
+// out[t, h] = bf16_rn( sum_{k=0..K-1, slot valid} part[k][t][h] ), summed in k order in fp32.
+__global__ void __launch_bounds__(256)
+    combine_kernel(const float* __restrict__ part, const int32_t* __restrict__ idx, int T, int K, int E, int H,
+                   __nv_bfloat16* __restrict__ out) {
+  const int64_t groups = static_cast<int64_t>(T) * (H / 8);
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = g / (H / 8);
+    const int h = static_cast<int>(g % (H / 8)) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < K; ++k) {
+      const int e = __ldg(idx + t * K + k);
+      if (e < 0 || e >= E) continue;
+      const float4* p = reinterpret_cast<const float4*>(part + ((static_cast<int64_t>(k) * T + t) * H + h));
+      const float4 a = __ldcs(p), b = __ldcs(p + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    uint4 o;
+    __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[0], acc[1]);
+    __nv_bfloat162 v1 = __floats2bfloat162_rn(acc[2], acc[3]);
+    __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[4], acc[5]);
+    __nv_bfloat162 v3 = __floats2bfloat162_rn(acc[6], acc[7]);
+    o.x = *reinterpret_cast<uint32_t*>(&v0);
+    o.y = *reinterpret_cast<uint32_t*>(&v1);
+    o.z = *reinterpret_cast<uint32_t*>(&v2);
+    o.w = *reinterpret_cast<uint32_t*>(&v3);
+    *reinterpret_cast<uint4*>(out + t * H + h) = o;
+  }
+}
+
+cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out,
+                           cudaStream_t s) {
+  const int64_t groups = static_cast<int64_t>(L.T) * (L.H / 8);
+  int64_t blocks = (groups + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(dev_info().sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  combine_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(W.part, topk_idx, L.T, L.K, L.E, L.H,
+                                                          static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- weight scales (MX)
+// W1 chunk ((e*(I/64) + n)*(H/128) + kb): rows r < 64 are gate rows n*64+r, rows
+// r >= 64 the matching up rows I + n*64 + (r-64).  W2 chunk ((e*(H/128) + n)*(I/128) + kb):
+// rows n*128 + r.  One thread moves one 4-byte word (4 scale blocks of one row).
+__global__ void prepare_sf_mx_kernel(const uint8_t* __restrict__ w1_sf, const uint8_t* __restrict__ w2_sf,
+                                     int H, int I, int E, uint8_t* __restrict__ w1_sfp,
+                                     uint8_t* __restrict__ w2_sfp) {
+  const int NB1 = I / 64, KB1 = H / 128, NB2 = H / 128, KB2 = I / 128;
+  const int64_t n1 = static_cast<int64_t>(E) * NB1 * KB1 * 128;
+  const int64_t n2 = static_cast<int64_t>(E) * NB2 * KB2 * 128;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n1 + n2;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (g < n1) {
+      const int r = static_cast<int>(g & 127);
+      const int64_t chunk = g >> 7;
+      const int kb = static_cast<int>(chunk % KB1);
+      const int n = static_cast<int>((chunk / KB1) % NB1);
+      const int64_t e = chunk / (static_cast<int64_t>(KB1) * NB1);
+      const int row = (r < 64) ? n * 64 + r : I + n * 64 + (r - 64);
+      const uint32_t word =
+          *reinterpret_cast<const uint32_t*>(w1_sf + (e * 2 * I + row) * (H / 32) + kb * 4);
+      *reinterpret_cast<uint32_t*>(w1_sfp + chunk * kSFChunk + sf_chunk_offset(r, 0)) = word;
+    } else {
+      const int64_t h = g - n1;
+      const int r = static_cast<int>(h & 127);
+      const int64_t chunk = h >> 7;
+      const int kb = static_cast<int>(chunk % KB2);
+      const int n = static_cast<int>((chunk / KB2) % NB2);
+      const int64_t e = chunk / (static_cast<int64_t>(KB2) * NB2);
+      const int row = n * 128 + r;
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(w2_sf + (e * H + row) * (I / 32) + kb * 4);
+      *reinterpret_cast<uint32_t*>(w2_sfp + chunk * kSFChunk + sf_chunk_offset(r, 0)) = word;
+    }
+  }
+}
+
+cudaError_t launch_prepare_sf_mx(const uint8_t* w1_sf, const uint8_t* w2_sf, int H, int I, int E,
+                                 uint8_t* w1_sfp, uint8_t* w2_sfp, cudaStream_t s) {
+  prepare_sf_mx_kernel<<<dev_info().sms * 8, 256, 0, s>>>(w1_sf, w2_sf, H, I, E, w1_sfp, w2_sfp);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- intermediate read-back
+__global__ void read_sf_mx_kernel(const uint8_t* __restrict__ pool2_sf, int64_t rows, int I, int BT,
+                                  uint8_t* __restrict__ sf) {
+  const int KB32 = I / 32;
+  const int KB = I / 128;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < rows * KB32;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = g / KB32;
+    const int j = static_cast<int>(g % KB32);
+    const int64_t blk = r / BT;
+    const int rr = static_cast<int>(r % BT);
+    sf[g] = pool2_sf[(blk * KB + j / 4) * kSFChunk + sf_chunk_offset(rr, j & 3)];
+  }
+}
+
+cudaError_t launch_read_intermediate(const Layout& L, const WsPtrs& W, int64_t rows, uint8_t* codes,
+                                     void* sf, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(codes, W.pool2, static_cast<size_t>(rows) * L.I, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return e;
+  if (L.variant == MM_MOE_VARIANT_MX) {
+    read_sf_mx_kernel<<<dev_info().sms * 4, 256, 0, s>>>(W.pool2_sf, rows, L.I, L.BT, static_cast<uint8_t*>(sf));
+    return cudaGetLastError();
+  }
+  return cudaMemcpyAsync(sf, W.pool2_sf, static_cast<size_t>(rows) * (L.I / 128) * sizeof(float),
+                         cudaMemcpyDeviceToDevice, s);
+}
+
+}  // namespace mm

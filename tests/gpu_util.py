@@ -1,0 +1,111 @@
+"""Shared helpers of the GPU parity tests: run the library through its C ABI on
+seeded workload inputs, run the oracle on the same bytes, apply the criteria."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+import workload as W
+
+
+def calc_diff(x, y) -> float:
+    """1 - 2<x,y> / (|x|^2 + |y|^2) in fp64 (DeepGEMM's calc_diff)."""
+    x = np.asarray(x, dtype=np.float64).ravel()
+    y = np.asarray(y, dtype=np.float64).ravel()
+    den = float(np.dot(x, x) + np.dot(y, y))
+    return 0.0 if den == 0 else 1.0 - 2.0 * float(np.dot(x, y)) / den
+
+
+def check_output(got: np.ndarray, ref: np.ndarray, label: str = "") -> dict:
+    """Criteria: calc_diff <= 1e-4 and every |got - ref| <= 2e-2 x that row's RMS
+    (rows whose reference is all zero must be exactly zero)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{label}: non-finite output"
+    cd = calc_diff(got, ref)
+    rms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    err = np.abs(got - ref)
+    ratio = np.where(rms > 0, err / np.where(rms > 0, rms, 1), np.where(err > 0, np.inf, 0))
+    worst = float(ratio.max()) if ratio.size else 0.0
+    assert cd <= 1e-4, f"{label}: calc_diff {cd:.3e} > 1e-4"
+    assert worst <= 2e-2, f"{label}: max |err|/row_rms {worst:.3e} > 2e-2"
+    return {"calc_diff": cd, "max_err_over_rms": worst}
+
+
+def to_dev(inp: dict, device="cuda") -> dict:
+    return {k: v.to(device) for k, v in inp.items()}
+
+
+def run_forward(M, cfg, dev_inp: dict, opt=None, ws=None, out=None, prepared=None):
+    """One forward through the C ABI.  Returns (out, ws, prepared, status)."""
+    opt = opt or M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
+    if prepared is None:
+        prepared = M.prepare_weights(dev_inp["w1_sf"], dev_inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
+    if ws is None:
+        ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt)
+    if out is None:
+        out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    M.forward(dev_inp["x"], dev_inp["x_sf"], dev_inp["topk_idx"], dev_inp["topk_w"], dev_inp["w1"], prepared[0],
+              dev_inp["w2"], prepared[1], out, cfg.H, cfg.I, cfg.E, ws, opt)
+    status = M.sync_status(ws)
+    return out, ws, prepared, status
+
+
+def host_experts(dev_inp: dict):
+    """Per-expert host copies of the (device) weights, fetched lazily for the oracle."""
+    cache = {}
+
+    def get(e):
+        if e not in cache:
+            cache[e] = tuple(dev_inp[k][e].cpu().numpy() for k in ("w1", "w1_sf", "w2", "w2_sf"))
+        return cache[e]
+    return get
+
+
+def oracle_rows(cfg, dev_inp: dict, rows, keep_intermediate=True):
+    x = dev_inp["x"].cpu().numpy()
+    x_sf = dev_inp["x_sf"].cpu().numpy()
+    idx = dev_inp["topk_idx"].cpu().numpy()
+    w = dev_inp["topk_w"].cpu().numpy()
+    return O.forward(rows, x, x_sf, idx, w, host_experts(dev_inp), cfg.H, cfg.I, cfg.E, cfg.variant,
+                     keep_intermediate=keep_intermediate)
+
+
+def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict) -> float:
+    """Fraction of intermediate e4m3 codes equal (by value) to the oracle's, with
+    every code of a block whose scale differs counted as a mismatch."""
+    rows = int(M.mm_moe_workspace_region(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, 4)[1] // 4)
+    codes = torch.empty(rows, cfg.I, dtype=torch.uint8, device="cuda")
+    bs = 32 if cfg.variant == "mx" else 128
+    sf = torch.empty(rows, cfg.I // bs, dtype=torch.uint8 if cfg.variant == "mx" else torch.float32, device="cuda")
+    r = M.mm_moe_read_intermediate(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, rows, codes.data_ptr(),
+                                   sf.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert r == 0
+    torch.cuda.synchronize()
+    codes = codes.cpu().numpy()
+    sf = sf.cpu().numpy()
+    total = match = 0
+    for (t, k), (oc, osf) in inter.items():
+        row = int(slot[t, k])
+        assert row >= 0
+        same_sf = np.repeat(sf[row] == osf, bs)
+        same = same_sf & (O.e4m3_decode(codes[row]) == O.e4m3_decode(oc))
+        total += same.size
+        match += int(same.sum())
+    return match / max(total, 1)
+
+
+def read_routing(M, cfg, ws, opt):
+    cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    blk = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    slot = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device="cuda")
+    nsrc = M.mm_moe_workspace_region(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, 4)[1] // 4
+    src = torch.empty(nsrc, dtype=torch.int32, device="cuda")
+    r, bm = M.mm_moe_read_routing(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cnt.data_ptr(),
+                                  blk.data_ptr(), slot.data_ptr(), src.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+    assert r == 0
+    torch.cuda.synchronize()
+    return cnt.cpu().numpy(), blk.cpu().numpy(), slot.cpu().numpy(), src.cpu().numpy(), bm

@@ -1,0 +1,68 @@
+"""The C-ABI library builds, loads and exports every entry point include/mm_moe.h
+declares; host-side argument checks and workspace sizing (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def M():
+    from moe_expert_forward_gb300 import build
+    build.build()
+    import moe_expert_forward_gb300 as M
+    return M
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "mm_moe.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(mm_moe_[a-z_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_binding_exports(M):
+    assert _declared() == sorted(M.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(M):
+    lib = ctypes.CDLL(M.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(M):
+    for c in range(7):
+        assert M.mm_moe_status_string(c)
+
+
+def test_workspace_size_and_shape_checks(M):
+    opt = M.options()
+    n = M.mm_moe_workspace_size(opt, 64, 256, 128, 8, 2)
+    assert n > 64 * 256
+    n_big = M.mm_moe_workspace_size(opt, 2048, 4096, 2048, 256, 6)
+    # pool capacity T*K + E*(128-1) rows of H bytes at least
+    assert n_big >= (2048 * 6 + 256 * 127) * 4096
+    for bad in [(64, 200, 128, 8, 2), (64, 256, 100, 8, 2), (64, 256, 128, 8, 0), (64, 256, 128, 2, 4),
+                (-1, 256, 128, 8, 2), (64, 256, 128, 2000, 2), (64, 256, 128, 32, 17)]:
+        with pytest.raises(M.MMError) as ei:
+            M.mm_moe_workspace_size(opt, *bad)
+        assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG
+
+
+def test_forward_rejects_null_and_small_workspace_without_touching_the_gpu(M):
+    opt = M.options()
+    # null inputs are rejected before any device call
+    r = M.mm_moe_forward(0, 0, 0, 0, 0, 0, 0, 0, 0, 64, 256, 128, 8, 2, 0, 0, opt, 0)
+    assert r == M.MM_MOE_ERR_INVALID_ARG
+    # T = 0 is a no-op that succeeds without pointers
+    assert M.mm_moe_forward(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 256, 128, 8, 2, 0, 0, opt, 0) == M.MM_MOE_OK
+
+
+def test_weight_sf_sizes(M):
+    a, b = M.mm_moe_weight_sf_size(M.options(), 4096, 2048, 256)
+    assert a == 256 * 4096 * 4096 // 32 and b == 256 * 4096 * 2048 // 32
+    a, b = M.mm_moe_weight_sf_size(M.options(M.MM_MOE_VARIANT_F8), 4096, 2048, 256)
+    assert a == 256 * 32 * 32 * 4 and b == 256 * 32 * 16 * 4

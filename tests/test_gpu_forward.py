@@ -1,0 +1,105 @@
+"""End-to-end parity of the forward (MX format) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workload as W
+from gpu_util import (check_output, intermediate_match, oracle_rows, read_routing, run_forward, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    from moe_expert_forward_gb300 import build
+    build.build()
+    import moe_expert_forward_gb300 as M
+    return M
+
+
+SMALL = {
+    "tiny": W.CONFIGS["tiny"],
+    # several token blocks per expert, ragged tails (not multiples of 16/32), 3 L1 weight tiles per 128 rows
+    "ragged": W.Config("ragged", T=300, H=512, I=384, E=5, K=2, seed=21),
+    "k1": W.Config("k1", T=77, H=384, I=256, E=3, K=1, seed=22),
+    "manyexp": W.Config("manyexp", T=40, H=256, I=128, E=64, K=6, seed=23),
+}
+
+
+def _full_check(M, cfg, inp, opt=None):
+    dev = to_dev(inp)
+    out, ws, prepared, (code, where) = run_forward(M, cfg, dev, opt)
+    assert code == 0, f"device status {code} at site {where}"
+    cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt or M.options())
+    ref_route = O.route(inp["topk_idx"].numpy(), cfg.E, bm)
+    assert np.array_equal(slot, ref_route["slot"])
+    rows = np.arange(cfg.T)
+    ref, inter = oracle_rows(cfg, dev, rows)
+    got = out.float().cpu().numpy()
+    stats = check_output(got, ref, cfg.name)
+    frac = intermediate_match(M, cfg, ws, opt or M.options(), slot, inter)
+    assert frac >= 0.999, f"intermediate code match {frac:.5f}"
+    return out, stats
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small_configs(M, name):
+    cfg = SMALL[name]
+    _full_check(M, cfg, W.make_inputs(cfg, "cpu"))
+
+
+def test_forward_masked_slots(M):
+    cfg = SMALL["ragged"].with_(seed=31)
+    inp = W.make_inputs(cfg, "cpu")
+    g = torch.Generator().manual_seed(5)
+    mask = torch.rand(cfg.T, cfg.K, generator=g) < 0.2
+    inp["topk_idx"][mask] = -1
+    inp["topk_idx"][7, :] = -1                       # a token with no expert at all
+    out, _ = _full_check(M, cfg, inp)
+    assert torch.all(out[7] == 0)
+
+
+def test_forward_repeatable_and_grid_independent(M):
+    cfg = SMALL["ragged"].with_(seed=41)
+    dev = to_dev(W.make_inputs(cfg, "cpu"))
+    out1, ws, prep, st = run_forward(M, cfg, dev)
+    out1 = out1.clone()
+    out2, _, _, _ = run_forward(M, cfg, dev, ws=ws, prepared=prep)
+    assert torch.equal(out1, out2)
+    out3, _, _, st3 = run_forward(M, cfg, dev, opt=M.options(num_sms=7), prepared=prep)
+    assert st3[0] == 0 and torch.equal(out1, out3)
+
+
+def test_forward_zero_weights_gives_zero(M):
+    cfg = SMALL["tiny"].with_(seed=51)
+    inp = W.make_inputs(cfg, "cpu")
+    inp["w2"].zero_()
+    dev = to_dev(inp)
+    out, ws, _, (code, _) = run_forward(M, cfg, dev)
+    assert code == 0 and torch.all(out == 0)
+
+
+def test_forward_l1_accumulators_match_oracle(M):
+    """Debug mode: the raw fp32 gate|up accumulators of the L1 GEMM against the
+    oracle's fp64 gate|up for every routed pair."""
+    cfg = SMALL["ragged"]
+    inp = W.make_inputs(cfg, "cpu")
+    dev = to_dev(inp)
+    opt = M.options(debug_flags=1)
+    out, ws, _, (code, where) = run_forward(M, cfg, dev, opt)
+    assert code == 0, where
+    dbg = M.workspace_view(ws, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "debug", torch.float32)
+    dbg = dbg.view(-1, 2 * cfg.I).cpu().numpy().astype(np.float64)
+    _, _, slot, _, _ = read_routing(M, cfg, ws, opt)
+    npi = {k: v.numpy() for k, v in inp.items()}
+    errs = []
+    for t in range(0, cfg.T, 7):
+        xh = O.dequant_x(npi["x"][t], npi["x_sf"][t], "mx")
+        for k in range(cfg.K):
+            e = int(npi["topk_idx"][t, k])
+            W1 = O.dequant_weight(npi["w1"][e], npi["w1_sf"][e], "mx")
+            ref = W1 @ xh
+            got = dbg[slot[t, k]]
+            errs.append(np.max(np.abs(got - ref)) / (np.max(np.abs(ref)) + 1e-30))
+    assert max(errs) < 1e-5, max(errs)
