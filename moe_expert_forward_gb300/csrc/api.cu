@@ -225,7 +225,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (!x || !x_sf || !topk_idx || !topk_w || !w1 || !w1_sfp || !w2 || !w2_sfp || !out || !workspace)
     return MM_MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(x_sf, 4) || !aligned(w1, 32) || !aligned(w2, 32) || !aligned(out, 16) ||
-      !aligned(workspace, 1024) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
+      !aligned(workspace, 256) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
     return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
   if (o.variant != MM_MOE_VARIANT_MX || o.fused) return MM_MOE_ERR_UNSUPPORTED;
@@ -319,6 +319,8 @@ int mm_moe_sync_status(const void* workspace, void* stream, int* where) {
   int h[4] = {0, 0, 0, 0};
   if (cudaMemcpy(h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MM_MOE_ERR_CUDA;
   if (where) *where = h[1];
+  if (h[0] && getenv("MM_MOE_DEBUG"))
+    fprintf(stderr, "mm_moe: device status %d at site %d (detail %08x %08x)\n", h[0], h[1], h[2], h[3]);
   return h[0];
 }
 

@@ -29,6 +29,10 @@ namespace {
 constexpr int kStages = 5;
 constexpr int kThreads = 192;
 constexpr int kABytes = 128 * kBK;     // 128 weight rows x 128 K, 1 byte per element in smem
+// A 16U4_ALIGN16B tile load completes the mbarrier transaction count with the
+// PACKED bytes it read from global memory (half a byte per element), not with
+// the unpacked bytes it wrote to shared memory (measured on GB300).
+constexpr int kATxBytes = kABytes / 2;
 constexpr int kBBytes = kBT * kBK;     // 128 token rows x 128 K
 constexpr int kTmemCols = 512;
 constexpr int kSfCol0 = 2 * kBT;       // scale-factor columns after the two accumulators
@@ -53,6 +57,7 @@ struct Args {
   float* dbg;           // L1: raw gate|up accumulators [P, 2I] or null
   int* status;
   uint64_t timeout_ns;
+  int a_tx_bytes;       // transaction bytes the weight tile's TMA reports (kATxBytes)
 };
 
 struct SmemLayout {
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int e, n, b, valid;
         decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
         const int boxes = (valid + 31) >> 5;
-        const uint32_t bytes = kABytes + boxes * 32 * kBK + 2 * kSFChunk;
+        const uint32_t bytes = args.a_tx_bytes + boxes * 32 * kBK + 2 * kSFChunk;
         const uint8_t* sfa = args.sfa + (static_cast<size_t>(e) * args.nblocks + n) * KB * kSFChunk;
         const uint8_t* sfb = args.sfb + static_cast<size_t>(b) * KB * kSFChunk;
         for (int kb = 0; kb < KB; ++kb) {
@@ -359,6 +364,7 @@ cudaError_t launch_impl(const GemmLaunch& g, cudaStream_t s) {
   a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;
   a.sfa = g.wsfp; a.status = W.status; a.timeout_ns = g.timeout_ns;
   a.dbg = PHASE == 1 ? g.dbg : nullptr;
+  a.a_tx_bytes = kATxBytes;
   CUresult r;
   if (PHASE == 1) {
     a.kblocks = L.H / 128;

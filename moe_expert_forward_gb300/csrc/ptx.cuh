@@ -75,7 +75,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
       if (mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > st.timeout_ns) {
-      report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, where);
+      uint64_t raw;
+      asm volatile("ld.shared.b64 %0, [%1];" : "=l"(raw) : "r"(a));
+      if (atomicCAS(st.word, 0, 4 /*MM_MOE_ERR_TIMEOUT*/) == 0) {
+        st.word[1] = where;
+        st.word[2] = static_cast<int>(raw & 0xffffffffu);
+        st.word[3] = static_cast<int>(raw >> 32);
+      }
       *abort = 1;
       return false;
     }
