@@ -1,0 +1,395 @@
+"""Benchmark of the MoE-layer forward on GB300 (one JSON line on rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config flash] [--impl ours|reference]
+
+A step is one forward of one MoE layer (dispatch, gather, L1 GEMM + SwiGLU +
+requant, L2 GEMM, combine) over one batch of T tokens of the named workload,
+inputs resident in HBM.  The L2 cache is flushed (a 512 MiB write) between
+timed steps, outside the timed events.  Per-kernel times come from CUDA events
+the library records between its kernels on the launching stream.
+
+--impl reference times the CPU oracle (fp64 numpy) on the host cores on a
+bounded token sample of the same workload; it is the slow reference arm.
+
+Under torchrun with N > 1 every rank runs an independent replica of the
+workload (weak scaling; tokens are independent, so there is no collective on
+the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workload as W  # noqa: E402
+
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0          # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ distributed (replicas only)
+def dist_setup(n):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.start_wall = time.time()
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for ln in out.strip().splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                             "hw": f[5], "hwt": f[6], "swt": f[7], "pcap": f[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # samples are ~100 ms apart; keep those taken while the GPU was busy (highest power third)
+        pw = np.array([r["power"] for r in rows])
+        busy = [r for r in rows if r["power"] >= np.percentile(pw, 66)] or rows
+        reasons = set()
+        for r in busy:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": float(np.median([r["sm"] for r in busy])), "sm_max_mhz": busy[0]["max"],
+                "reasons": sorted(reasons), "samples": len(busy), "power_w_max": float(pw.max())}
+
+
+# ------------------------------------------------------------------ accounting
+def workload_accounting(cfg, idx: np.ndarray):
+    """Algorithmic bytes / FLOPs of one step and of the two GEMM kernels."""
+    T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
+    valid = (idx >= 0) & (idx < E)
+    touched = int(np.unique(idx[valid]).size)
+    pairs = int(valid.sum())
+    if cfg.variant == "mx":
+        w1_b = 2 * I * H * (0.5 + 1 / 32)
+        w2_b = H * I * (0.5 + 1 / 32)
+        x_b = H * (1 + 1 / 32)
+        a_b = I * (1 + 1 / 32)
+    else:
+        w1_b = 2 * I * H + (2 * I // 128) * (H // 128) * 4
+        w2_b = H * I + (H // 128) * (I // 128) * 4
+        x_b = H + (H // 128) * 4
+        a_b = I + (I // 128) * 4
+    step_bytes = touched * (w1_b + w2_b) + T * x_b + T * K * 8 + T * H * 2
+    flops = 6.0 * pairs * H * I
+    l1_bytes = touched * w1_b + pairs * x_b + pairs * a_b
+    l2_bytes = touched * w2_b + pairs * a_b + pairs * H * 4
+    return {"touched_experts": touched, "pairs": pairs, "step_bytes": step_bytes, "flops": flops,
+            "l1_bytes": l1_bytes, "l2_bytes": l2_bytes, "l1_flops": 4.0 * pairs * H * I,
+            "l2_flops": 2.0 * pairs * H * I}
+
+
+def kernel_traffic(kernel: str, cfg_name: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source (hash match); else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(f"{kernel}:{cfg_name}")
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "moe_expert_forward_gb300", "csrc", ent.get("source", "gemm_mx.cu"))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent["dram_bytes_per_launch"] if h == ent.get("source_sha") else None
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, ws_n, rank, local):
+    from moe_expert_forward_gb300 import build as B
+    B.build()
+    import moe_expert_forward_gb300 as M
+
+    cfg = W.CONFIGS[args.config]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = W.make_inputs(cfg, dev)
+    opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
+    w1p, w2p = M.prepare_weights(inp["w1_sf"], inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
+    ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt, dev)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd(o, x=None, x_sf=None, idx=None, w=None):
+        M.forward(inp["x"] if x is None else x, inp["x_sf"] if x_sf is None else x_sf,
+                  inp["topk_idx"] if idx is None else idx, inp["topk_w"] if w is None else w,
+                  inp["w1"], w1p, inp["w2"], w2p, out, cfg.H, cfg.I, cfg.E, ws, o)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        fwd(opt)
+    code, where = M.sync_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {where}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(M.MM_MOE_NUM_TIMING_EVENTS)] for _ in range(K)]
+    for row in evs:                  # torch creates the CUDA event on first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    import ctypes
+    arrays = [(ctypes.c_void_p * M.MM_MOE_NUM_TIMING_EVENTS)(*[e.cuda_event for e in row]) for row in evs]
+    assert all(h for arr in arrays for h in arr)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        o = M.options(opt.variant)
+        o.timing_events = ctypes.cast(arrays[i], ctypes.c_void_p)
+        fwd(o)
+    torch.cuda.synchronize()
+    barrier(ws_n)
+    code, where = M.sync_status(ws)
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {where}")
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(K)])
+    step_ms_local = float(stage_ms.sum(1).mean())
+    step_ms = max_over_ranks(step_ms_local, ws_n)
+
+    # end to end: pinned host inputs -> device, forward, output -> pinned host, every step
+    host = {k: inp[k].cpu().pin_memory() for k in ("x", "x_sf", "topk_idx", "topk_w")}
+    dbuf = {k: torch.empty_like(inp[k]) for k in host}
+    hout = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = hout.numel() * hout.element_size()
+    e2e_ms = []
+    for i in range(max(3, min(K, 50)) + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        fwd(opt, dbuf["x"], dbuf["x_sf"], dbuf["topk_idx"], dbuf["topk_w"])
+        hout.copy_(out, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    code, _ = M.sync_status(ws)
+    assert code == 0
+    assert torch.equal(hout, out.cpu())
+    e2e_step_ms = max_over_ranks(float(np.mean(e2e_ms)), ws_n)
+    clk = clocks.stop()
+
+    idx_np = inp["topk_idx"].cpu().numpy()
+    acc = workload_accounting(cfg, idx_np)
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    fp8 = float(pk["bf16_tflops"]) * FP8_OVER_BF16
+    stage_mean = stage_ms.mean(0)
+    l1_ms, l2_ms = float(stage_mean[2]), float(stage_mean[3])
+    # dominant kernel: the one with the largest share of the step
+    dom = "l1" if l1_ms >= l2_ms else "l2"
+    dom_ms = l1_ms if dom == "l1" else l2_ms
+    dom_bytes = acc["l1_bytes"] if dom == "l1" else acc["l2_bytes"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    t_roof = max(acc["flops"] / (fp8 * 1e12), acc["step_bytes"] / (hbm * 1e9))
+    tokens_per_s = ws_n * cfg.T / (step_ms * 1e-3)
+
+    result = {
+        "metric": "MoE-layer tokens/s (one MoE layer forward, 1 GPU per replica)",
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": ws_n,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3xe2m1->fp32acc" if cfg.variant == "mx" else "e4m3xe4m3->fp32acc",
+        "data": "synthetic (seeded workload generator; random weights, no checkpoint)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.K} "
+                               f"{'uniform' if cfg.routing == 'uniform' else 'Zipf(1.1)'} routing, "
+                               f"{'MX e4m3 x e2m1 UE8M0/32' if cfg.variant == 'mx' else 'FP8 e4m3 per-128'}",
+                   "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K, "seed": cfg.seed,
+                   "l2_policy": "L2 flushed (512 MiB write) before every timed step; weights 3+ GB >> L2",
+                   "parallelism": f"replicas x{ws_n} (no data-path collective)"},
+        "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
+        "path_roofline": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (step_ms * 1e-3),
+                          "bytes": acc["step_bytes"], "flops": acc["flops"],
+                          "touched_experts": acc["touched_experts"],
+                          "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8, "source": pk_src,
+                                    "fp8_from": "bf16_tflops x 2 (nominal fp8/bf16 ratio)"}},
+        "stages_ms": {s: float(v) for s, v in zip(M.STAGES, stage_mean)},
+        "roofline": {"kernel": f"gemm_mx_kernel<{1 if dom == 'l1' else 2}> ({dom.upper()} grouped GEMM)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": kernel_traffic(dom, cfg.name),
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "peak_source": f"{pk_src} hbm_gbs (STREAM-style copy)"},
+        "e2e": {"value": ws_n * cfg.T / (e2e_step_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
+        "gpu_launches": 5 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_tokens)
+    return result
+
+
+# ------------------------------------------------------------------ oracle (CPU) runs
+def oracle_tokens(cfg, inp, rows):
+    import oracle as O
+    x = inp["x"][rows].cpu().numpy()
+    x_sf = inp["x_sf"][rows].cpu().numpy()
+    idx = inp["topk_idx"][rows].cpu().numpy()
+    w = inp["topk_w"][rows].cpu().numpy()
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            cache[e] = tuple(inp[k][e].cpu().numpy() for k in ("w1", "w1_sf", "w2", "w2_sf"))
+        return cache[e]
+    # fetch the weights first so that only the oracle's arithmetic is timed
+    for e in np.unique(idx[idx >= 0]):
+        experts(int(e))
+    t0 = time.perf_counter()
+    O.forward(range(len(rows)), x, x_sf, idx, w, experts, cfg.H, cfg.I, cfg.E, cfg.variant)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, inp, n_tokens):
+    rows = list(range(min(n_tokens, cfg.T)))
+    dt = oracle_tokens(cfg, inp, rows)
+    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": f"first {len(rows)} tokens of the {cfg.name} workload "
+                                        f"({len(rows) * cfg.K} routed pairs), fp64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args, ws_n, rank):
+    cfg = W.CONFIGS[args.config]
+    if rank != 0:
+        return None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_inputs(cfg, dev, with_weights=False)
+    # only the experts the sampled tokens use are materialised
+    n = args.cpu_tokens
+    rows = list(range(min(n, cfg.T)))
+    used = sorted(set(int(e) for e in inp["topk_idx"][rows].cpu().numpy().ravel() if e >= 0))
+    inp.update(W.make_weights(cfg, dev, experts=used))
+    times = []
+    for i in range(max(args.warmup, 0) + args.steps):
+        dt = oracle_tokens(cfg, inp, rows)
+        if i >= args.warmup:
+            times.append(dt)
+    step_s = float(np.mean(times))
+    v = len(rows) / step_s
+    cores = len(os.sched_getaffinity(0))
+    return {"impl": "reference", "metric": "MoE-layer tokens/s (one MoE layer forward, 1 GPU per replica)",
+            "value": v, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded workload generator)",
+            "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.K}",
+                       "sample_tokens": len(rows)},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"first {len(rows)} tokens per step ({len(rows) * cfg.K} pairs)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="flash", choices=list(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws_n, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, ws_n, rank)
+    else:
+        res = run_ours(args, ws_n, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

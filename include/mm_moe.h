@@ -89,9 +89,17 @@ typedef struct mm_moe_options {
   int num_sms;                  /* persistent grid size; 0 = all SMs */
   int debug_flags;              /* bit 0: the L1 epilogue also writes its raw fp32 gate|up accumulators
                                    to the DEBUG workspace region ([P, 2I], pool-row order) and the
-                                   call stops after L1; 0 for normal use */
+                                   call stops after L1; bit 1: the GEMM kernels record per-CTA
+                                   wait/busy times of their roles into the PROF workspace region;
+                                   0 for normal use */
   int reserved[7];
+  void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
+                                   caller) that mm_moe_forward records on `stream` at the start, between
+                                   its kernels and at the end: [0] start, [1] dispatch done, [2] gather
+                                   done, [3] L1 done, [4] L2 done, [5] combine done; NULL = none */
 } mm_moe_options;
+
+#define MM_MOE_NUM_TIMING_EVENTS 6
 
 /* Fill `opt` with the defaults. */
 void mm_moe_default_options(mm_moe_options* opt);
@@ -121,12 +129,16 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
 /* Step a1 alone, into caller buffers: cnt[E], blk_off[E+1] (in blocks of
  * block_m rows), slot[T*K] (pool row or -1), src[src_capacity] (t*K+k or -1 for
  * padding rows; rows past blk_off[E]*block_m are left untouched).  block_m must
- * be a multiple of 16 in [16, 256]; src_capacity >= T*K + E*(block_m-1).
- * `status` is a device int[4], zeroed by the caller, that receives
- * MM_MOE_ERR_BAD_ROUTING when topk_idx holds values >= E. */
+ * be a multiple of 16 in [16, 256]; src_capacity >= T*K + min(T*K, E)*(block_m-1).
+ * `scratch` (device, 4-byte aligned, at least 4*E bytes; mm_moe_dispatch_scratch_size
+ * gives the size that lets the work spread over all SMs) receives per-CTA
+ * expert counts; fewer bytes only means fewer CTAs.  `status` is a device
+ * int[4], zeroed by the caller, that receives MM_MOE_ERR_BAD_ROUTING when
+ * topk_idx holds values >= E or < -1. */
+int mm_moe_dispatch_scratch_size(int T, int K, int E, size_t* bytes);
 int mm_moe_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
-                    int32_t* blk_off, int32_t* slot, int32_t* src, int64_t src_capacity, int32_t* status,
-                    void* stream);
+                    int32_t* blk_off, int32_t* slot, int32_t* src, int64_t src_capacity, void* scratch,
+                    size_t scratch_bytes, int32_t* status, void* stream);
 
 /* Copy the routing of the last forward out of a workspace (same shapes as mm_moe_dispatch;
  * block_m is reported through *block_m). */
@@ -145,7 +157,8 @@ int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, i
  * workspace laid out for this shape and these options.  region: 0 status,
  * 1 cnt, 2 blk_off, 3 slot, 4 src, 5 pooled activations, 6 their scales,
  * 7 intermediate codes, 8 intermediate scales, 9 fp32 partials [K, T, H],
- * 10 debug accumulators (debug_flags bit 0 only). */
+ * 10 debug accumulators (debug_flags bit 0 only), 11 per-CTA role timings of the two
+ * GEMM kernels (debug_flags bit 1 only: uint64 [2][grid][8] nanoseconds and counts). */
 int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
                             int region, void** ptr, size_t* bytes);
 

@@ -24,17 +24,20 @@ MM_MOE_ERR_BAD_ROUTING = 5
 MM_MOE_ERR_WORKSPACE_TOO_SMALL = 6
 MM_MOE_VARIANT_MX = 0
 MM_MOE_VARIANT_F8 = 1
+MM_MOE_NUM_TIMING_EVENTS = 6
+STAGES = ["dispatch", "gather", "l1", "l2", "combine"]
 
 # every symbol include/mm_moe.h declares
 EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_size", "mm_moe_prepare_weights",
-           "mm_moe_forward", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
+           "mm_moe_forward", "mm_moe_dispatch_scratch_size", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
            "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region"]
 
 
 class mm_moe_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("fused", ctypes.c_int), ("lag_units", ctypes.c_int),
                 ("retain_intermediate", ctypes.c_int), ("wait_timeout_ms", ctypes.c_uint),
-                ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+                ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("reserved", ctypes.c_int * 7),
+                ("timing_events", ctypes.c_void_p)]
 
 
 class MMError(RuntimeError):
@@ -63,7 +66,8 @@ def lib() -> ctypes.CDLL:
             "mm_moe_weight_sf_size": (_I, [_OPT, _I, _I, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
             "mm_moe_prepare_weights": (_I, [_OPT, _P, _P, _I, _I, _I, _P, _P, _P]),
             "mm_moe_forward": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _OPT, _P]),
-            "mm_moe_dispatch": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
+            "mm_moe_dispatch_scratch_size": (_I, [_I, _I, _I, ctypes.POINTER(_SZ)]),
+            "mm_moe_dispatch": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _SZ, _P, _P]),
             "mm_moe_read_routing": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _P, _P, _P, _P, ctypes.POINTER(_I), _P]),
             "mm_moe_read_intermediate": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _I64, _P, _P, _P]),
             "mm_moe_sync_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
@@ -108,8 +112,16 @@ def mm_moe_forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, T, H,
                                 ws_bytes, _opt(opt), stream)
 
 
-def mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, status, stream) -> int:
-    return lib().mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, status, stream)
+def mm_moe_dispatch_scratch_size(T, K, E) -> int:
+    n = _SZ(0)
+    _check(lib().mm_moe_dispatch_scratch_size(T, K, E, ctypes.byref(n)), "mm_moe_dispatch_scratch_size")
+    return n.value
+
+
+def mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, scratch, scratch_bytes,
+                    status, stream) -> int:
+    return lib().mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, scratch,
+                                 scratch_bytes, status, stream)
 
 
 def mm_moe_read_routing(workspace, opt, T, H, I, E, K, cnt, blk_off, slot, src, stream):
@@ -144,7 +156,7 @@ def mm_moe_workspace_region(workspace, opt, T, H, I, E, K, region):
 
 
 REGIONS = {"status": 0, "cnt": 1, "blk_off": 2, "slot": 3, "src": 4, "pool_x": 5, "pool_x_sf": 6, "pool2": 7,
-           "pool2_sf": 8, "partials": 9, "debug": 10}
+           "pool2_sf": 8, "partials": 9, "debug": 10, "prof": 11}
 
 
 def workspace_view(workspace, opt, T, H, I, E, K, region: str, dtype=None):

@@ -24,6 +24,7 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.status = o; o += 256;
   L.cnt = o; o = align_up(o + sizeof(int) * E, 256);
   L.blk_off = o; o = align_up(o + sizeof(int) * (E + 1), 256);
+  L.dscr = o; o = align_up(o + sizeof(int) * static_cast<size_t>(kDispatchMaxCtas) * E, 256);
   L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
   L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
   L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
@@ -38,6 +39,8 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.dbg = o;
   L.dbg_bytes = (debug_flags & 1) ? static_cast<size_t>(L.P) * 2 * I * sizeof(float) : 0;
   o = align_up(o + L.dbg_bytes, 1024);
+  L.prof = o;
+  o = align_up(o + ((debug_flags & 2) ? 2 * 8 * 1024 * sizeof(unsigned long long) : 0), 1024);
   L.total = o;
   return L;
 }
@@ -48,6 +51,7 @@ WsPtrs ws_ptrs(void* ws, const Layout& L) {
   W.status = reinterpret_cast<int*>(b + L.status);
   W.cnt = reinterpret_cast<int*>(b + L.cnt);
   W.blk_off = reinterpret_cast<int*>(b + L.blk_off);
+  W.dscr = reinterpret_cast<int*>(b + L.dscr);
   W.slot = reinterpret_cast<int*>(b + L.slot);
   W.src = reinterpret_cast<int*>(b + L.src);
   W.pool_x = b + L.pool_x;
@@ -56,6 +60,7 @@ WsPtrs ws_ptrs(void* ws, const Layout& L) {
   W.pool2_sf = b + L.pool2_sf;
   W.part = reinterpret_cast<float*>(b + L.part);
   W.dbg = L.dbg_bytes ? reinterpret_cast<float*>(b + L.dbg) : nullptr;
+  W.prof = (L.total > L.prof) ? reinterpret_cast<unsigned long long*>(b + L.prof) : nullptr;
   return W;
 }
 
@@ -95,6 +100,26 @@ static EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+CUresult encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  CUresult r = fn(m, dt, rank, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS && getenv("MM_MOE_DEBUG"))
+    fprintf(stderr, "mm_moe: cuTensorMapEncodeTiled(dt=%d rank=%d) = %d\n", static_cast<int>(dt), rank,
+            static_cast<int>(r));
+  return r;
 }
 
 CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
@@ -172,7 +197,7 @@ int mm_moe_weight_sf_size(const mm_moe_options* opt, int H, int I, int E, size_t
   if (int r = check_shape(0, H, I, E, 1)) return r;
   if (o.variant == MM_MOE_VARIANT_MX) {
     *w1b = static_cast<size_t>(E) * 2 * I * (H / 32);
-    *w2b = static_cast<size_t>(E) * H * (I / 32);
+    *w2b = static_cast<size_t>(E) * ((H + 255) / 256) * 256 * (I / 32);
   } else {
     *w1b = static_cast<size_t>(E) * (2 * I / 128) * (H / 128) * sizeof(float);
     *w2b = static_cast<size_t>(E) * (H / 128) * (I / 128) * sizeof(float);
@@ -201,16 +226,26 @@ int mm_moe_prepare_weights(const mm_moe_options* opt, const void* w1_sf, const v
   return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
 }
 
+int mm_moe_dispatch_scratch_size(int T, int K, int E, size_t* bytes) {
+  if (!bytes || check_shape(T, 128, 128, E, K)) return MM_MOE_ERR_INVALID_ARG;
+  *bytes = sizeof(int32_t) * static_cast<size_t>(kDispatchMaxCtas) * E;
+  return MM_MOE_OK;
+}
+
 int mm_moe_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt, int32_t* blk_off,
-                    int32_t* slot, int32_t* src, int64_t src_capacity, int32_t* status, void* stream) {
+                    int32_t* slot, int32_t* src, int64_t src_capacity, void* scratch, size_t scratch_bytes,
+                    int32_t* status, void* stream) {
   if (check_shape(T, 128, 128, E, K)) return MM_MOE_ERR_INVALID_ARG;
   if (block_m < 16 || block_m > 256 || block_m % 16) return MM_MOE_ERR_INVALID_ARG;
-  if (!cnt || !blk_off || !status || (T > 0 && (!topk_idx || !slot || !src))) return MM_MOE_ERR_INVALID_ARG;
+  if (!cnt || !blk_off || !status || !scratch || (T > 0 && (!topk_idx || !slot || !src)))
+    return MM_MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < sizeof(int32_t) * static_cast<size_t>(E) || !aligned(scratch, 4)) return MM_MOE_ERR_INVALID_ARG;
   const int64_t pairs = static_cast<int64_t>(T) * K;
   const int64_t live = pairs < E ? pairs : E;
   if (src_capacity < pairs + live * (block_m - 1)) return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
   cudaError_t e = launch_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, status,
+                                  static_cast<int32_t*>(scratch), static_cast<int64_t>(scratch_bytes / 4),
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
 }
@@ -235,22 +270,35 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
 
-  cudaError_t e = cudaMemsetAsync(W.status, 0, 16, s);
-  if (e == cudaSuccess) e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, s);
+  cudaEvent_t* ev = static_cast<cudaEvent_t*>(o.timing_events);
+  auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(W.status, 0, 16, s);
+  if (e == cudaSuccess)
+    e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, W.dscr,
+                        static_cast<int64_t>(kDispatchMaxCtas) * E, s);
+  if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, s);
-  GemmLaunch g{&L, &W, nullptr, nullptr, topk_w, W.dbg, static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull, grid};
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
+  GemmLaunch g{&L, &W, nullptr, nullptr, topk_w, W.dbg, W.prof, static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull,
+               grid};
   if (e == cudaSuccess) {
     g.w = static_cast<const uint8_t*>(w1);
     g.wsfp = static_cast<const uint8_t*>(w1_sfp);
     e = launch_gemm_mx_l1(g, s);
   }
+  if (e == cudaSuccess) e = mark(3);
   if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
   if (e == cudaSuccess) {
     g.w = static_cast<const uint8_t*>(w2);
     g.wsfp = static_cast<const uint8_t*>(w2_sfp);
     e = launch_gemm_mx_l2(g, s);
   }
+  if (e == cudaSuccess) e = mark(4);
   if (e == cudaSuccess) e = launch_combine(L, W, topk_idx, out, s);
+  if (e == cudaSuccess) e = mark(5);
   if (e != cudaSuccess) {
     if (getenv("MM_MOE_DEBUG")) fprintf(stderr, "mm_moe_forward: %s\n", cudaGetErrorString(e));
     return MM_MOE_ERR_CUDA;
@@ -296,11 +344,12 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!ptr || !bytes) return MM_MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
-  const size_t offs[12] = {L.status, L.cnt, L.blk_off, L.slot, L.src, L.pool_x, L.pool_x_sf, L.pool2, L.pool2_sf,
-                           L.part, L.dbg, L.total};
-  if (region < 0 || region > 10) return MM_MOE_ERR_INVALID_ARG;
+  const size_t offs[13] = {L.status, L.cnt, L.blk_off, L.slot, L.src, L.pool_x, L.pool_x_sf, L.pool2, L.pool2_sf,
+                           L.part, L.dbg, L.prof, L.total};
+  if (region < 0 || region > 11) return MM_MOE_ERR_INVALID_ARG;
   size_t n;
   if (region == 10) n = L.dbg_bytes;
+  else if (region == 11) n = L.total - L.prof;
   else if (region == 0) n = 16;
   else if (region == 1) n = sizeof(int) * E;
   else if (region == 2) n = sizeof(int) * (E + 1);

@@ -21,7 +21,7 @@ struct Layout {
   int64_t P;                 // pool row capacity (multiple of BT)
   int64_t nblk_cap;          // P / BT
   int KB1, KB2;              // H/128, I/128
-  size_t status, cnt, blk_off, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, total;
+  size_t status, cnt, blk_off, dscr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
 };
 
 Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0);
@@ -31,6 +31,7 @@ struct WsPtrs {
   int* status;
   int* cnt;
   int* blk_off;
+  int* dscr;
   int* slot;
   int* src;
   uint8_t* pool_x;
@@ -39,6 +40,7 @@ struct WsPtrs {
   uint8_t* pool2_sf;
   float* part;
   float* dbg;
+  unsigned long long* prof;
 };
 WsPtrs ws_ptrs(void* ws, const Layout& L);
 
@@ -51,7 +53,9 @@ const DevInfo& dev_info();
 
 // ---- launchers (return cudaError_t of the launch)
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
-                            int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, cudaStream_t s);
+                            int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
+                            int64_t scratch_ints, cudaStream_t s);
+constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA counts [CTAs][E]
 cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
                           cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out,
@@ -68,6 +72,7 @@ struct GemmLaunch {
   const uint8_t* wsfp;       // prepared weight scales
   const float* topk_w;
   float* dbg;               // L1 raw accumulators (debug_flags bit 0) or null
+  unsigned long long* prof; // per-CTA role timings (debug_flags bit 1) or null
   uint64_t timeout_ns;
   int grid;
 };
@@ -75,6 +80,8 @@ cudaError_t launch_gemm_mx_l1(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_gemm_mx_l2(const GemmLaunch& g, cudaStream_t s);
 
 // TMA descriptor creation through the driver entry point.
+CUresult encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swz);
 CUresult encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
                         uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                         CUtensorMapSwizzle swz);

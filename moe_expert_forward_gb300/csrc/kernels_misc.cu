@@ -17,59 +17,77 @@ __host__ __device__ __forceinline__ int sf_chunk_offset(int r, int kk) {
 }
 
 // ----------------------------------------------------------------------------- dispatch
-// One CTA of 1024 threads.  Flat pairs p = t*K + k are split into 32 contiguous
-// ranges, one per warp.  Pass 1 counts per (warp, expert); an exclusive scan over
-// warps gives each warp its starting rank inside every expert; pass 2 re-walks
-// the same pairs and ranks equal experts inside each 32-pair step with
-// __match_any_sync, so the slot order is ascending p (= ascending token, then k).
-__global__ void __launch_bounds__(1024, 1)
-    dispatch_kernel(const int32_t* __restrict__ idx, int T, int K, int E, int BT, int32_t* __restrict__ cnt,
-                    int32_t* __restrict__ blk_off, int32_t* __restrict__ slot, int32_t* __restrict__ src,
-                    int32_t* __restrict__ status) {
-  extern __shared__ int wc[];               // [32][E]
-  __shared__ int s_blk[kMaxE + 1];
-  __shared__ int s_cnt[kMaxE];
-  __shared__ int s_wsum[32];
-  __shared__ int s_bad;
+// Two kernels over G CTAs; CTA g owns the contiguous flat pairs
+// p = t*K + k in [g*CH, (g+1)*CH).
+//   count:  per-CTA expert histogram cc[g][e] (shared-memory atomics).
+//   assign: every CTA rebuilds, from cc, the totals cnt[e], the segment offsets
+//           blk_off (exclusive scan of ceil(cnt/BT)) and its own starting rank
+//           inside each expert (sum of cc over earlier CTAs); its 8 warps then
+//           count their sub-ranges, take exclusive offsets over warps, and rank
+//           equal experts inside each 32-pair step with __match_any_sync.  The
+//           slot order is therefore ascending p (= ascending token, then k).
+//           CTA 0 publishes cnt/blk_off; padding rows are spread over CTAs.
+constexpr int kDispatchThreads = 256;
+constexpr int kDispatchWarps = kDispatchThreads / 32;
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_count_kernel(const int32_t* __restrict__ idx, int64_t TK, int E, int64_t CH, int32_t* __restrict__ cc,
+                          int32_t* __restrict__ status) {
+  extern __shared__ int sc[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sc[e] = 0;
+  __syncthreads();
+  const int64_t beg = static_cast<int64_t>(blockIdx.x) * CH;
+  const int64_t end = beg + CH < TK ? beg + CH : TK;
+  bool bad = false;
+  for (int64_t p = beg + threadIdx.x; p < end; p += blockDim.x) {
+    const int e = __ldg(idx + p);
+    if (e >= 0 && e < E) atomicAdd(&sc[e], 1);
+    else if (e >= E || e < -1) bad = true;
+  }
+  if (bad) atomicCAS(status, 0, MM_MOE_ERR_BAD_ROUTING);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cc[static_cast<int64_t>(blockIdx.x) * E + e] = sc[e];
+}
+
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_assign_kernel(const int32_t* __restrict__ idx, int64_t TK, int E, int BT, int64_t CH,
+                           const int32_t* __restrict__ cc, int32_t* __restrict__ cnt, int32_t* __restrict__ blk_off,
+                           int32_t* __restrict__ slot, int32_t* __restrict__ src) {
+  extern __shared__ int sm[];
+  int* wc = sm;                              // [8][E] per-warp counts, then offsets
+  int* s_base = wc + kDispatchWarps * E;     // [E] rank of this CTA's first pair inside each expert
+  int* s_cnt = s_base + E;                   // [E]
+  int* s_blk = s_cnt + E;                    // [E+1]
+  __shared__ int s_wsum[kDispatchWarps];
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int64_t TK = static_cast<int64_t>(T) * K;
-  for (int i = tid; i < 32 * E; i += blockDim.x) wc[i] = 0;
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
+  const int g = blockIdx.x, G = gridDim.x;
 
-  const int64_t per = ((TK + 1023) / 1024) * 32;
-  const int64_t beg = static_cast<int64_t>(w) * per;
-  const int64_t end = (beg + per < TK) ? beg + per : TK;
-  int* my = wc + w * E;
-  for (int64_t base = beg; base < end; base += 32) {
-    const int64_t p = base + lane;
-    const int e = (p < end) ? __ldg(idx + p) : -1;
-    const bool valid = (e >= 0) && (e < E);
-    if (p < end && (e >= E || e < -1)) s_bad = 1;
-    const unsigned m = __match_any_sync(0xffffffffu, valid ? e : -1);
-    if (valid && lane == __ffs(m) - 1) my[e] += __popc(m);
-    __syncwarp();
-  }
-  __syncthreads();
-
-  // counts and per-warp exclusive offsets inside each expert
+  for (int i = tid; i < kDispatchWarps * E; i += blockDim.x) wc[i] = 0;
   for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int ww = 0; ww < 32; ++ww) {
-      const int c = wc[ww * E + e];
-      wc[ww * E + e] = run;
-      run += c;
+    int base = 0, tot = 0;
+    for (int h = 0; h < G; ++h) {
+      const int c = __ldg(cc + static_cast<int64_t>(h) * E + e);
+      base += (h < g) ? c : 0;
+      tot += c;
     }
-    cnt[e] = run;
-    s_cnt[e] = run;
-    s_blk[e] = (run + BT - 1) / BT;
+    s_base[e] = base;
+    s_cnt[e] = tot;
+    s_blk[e] = (tot + BT - 1) / BT;
   }
   __syncthreads();
 
-  // exclusive scan of blocks per expert (E <= 1024: one value per thread)
+  // exclusive scan of blocks per expert: each thread owns up to 4 consecutive experts
   {
-    int v = (tid < E) ? s_blk[tid] : 0;
-    int incl = v;
+    constexpr int kPer = (kMaxE + kDispatchThreads - 1) / kDispatchThreads;
+    int v[kPer];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = tid * kPer + j;
+      v[j] = e < E ? s_blk[e] : 0;
+      sum += v[j];
+    }
+    int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, incl, o);
@@ -77,67 +95,125 @@ __global__ void __launch_bounds__(1024, 1)
     }
     if (lane == 31) s_wsum[w] = incl;
     __syncthreads();
-    if (w == 0) {
-      int ws = s_wsum[lane];
-      int wi = ws;
+    int wpre = 0;
+    for (int i = 0; i < w; ++i) wpre += s_wsum[i];
+    int run = wpre + incl - sum;
+    __syncthreads();
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += n;
-      }
-      s_wsum[lane] = wi - ws;       // exclusive warp prefix
+    for (int j = 0; j < kPer; ++j) {
+      const int e = tid * kPer + j;
+      if (e < E) s_blk[e] = run;
+      run += v[j];
     }
-    __syncthreads();
-    const int excl = incl - v + s_wsum[w];
-    __syncthreads();
-    if (tid < E) s_blk[tid] = excl;
-    if (tid == E - 1) s_blk[E] = excl + v;
+    if (tid == kDispatchThreads - 1) s_blk[E] = run;
     __syncthreads();
   }
-  for (int e = tid; e <= E; e += blockDim.x) blk_off[e] = s_blk[e];
+  if (g == 0) {
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = s_cnt[e];
+    for (int e = tid; e <= E; e += blockDim.x) blk_off[e] = s_blk[e];
+  }
 
-  // pass 2: slots and inverse map
-  for (int64_t base = beg; base < end; base += 32) {
-    const int64_t p = base + lane;
-    const int e = (p < end) ? __ldg(idx + p) : -1;
-    const bool valid = (e >= 0) && (e < E);
-    const unsigned m = __match_any_sync(0xffffffffu, valid ? e : -1);
-    int before = 0;
-    if (valid) before = my[e];
-    __syncwarp();
-    if (valid) {
-      const int rank = __popc(m & ((1u << lane) - 1u));
-      const int64_t pos = static_cast<int64_t>(s_blk[e]) * BT + before + rank;
-      slot[p] = static_cast<int32_t>(pos);
-      src[pos] = static_cast<int32_t>(p);
-      if (lane == __ffs(m) - 1) my[e] = before + __popc(m);
-    } else if (p < end) {
-      slot[p] = -1;
+  const int64_t per = CH / kDispatchWarps;   // multiple of 32
+  const int64_t beg = static_cast<int64_t>(g) * CH + w * per;
+  const int64_t end = beg + per < TK ? beg + per : TK;
+  int* my = wc + w * E;
+  constexpr int kBatch = 8;                  // independent idx loads in flight per lane
+  for (int64_t base0 = beg; base0 < end; base0 += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t p = base0 + j * 32 + lane;
+      ev[j] = (p < end) ? __ldg(idx + p) : -1;
     }
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (base0 + j * 32 >= end) break;      // warp-uniform
+      const int e = ev[j];
+      const bool valid = (e >= 0) && (e < E);
+      const unsigned m = __match_any_sync(0xffffffffu, valid ? e : -1);
+      if (valid && lane == __ffs(m) - 1) my[e] += __popc(m);
+      __syncwarp();
+    }
   }
-  // padding rows of every segment
+  __syncthreads();
   for (int e = tid; e < E; e += blockDim.x) {
+    int run = s_base[e];
+    for (int ww = 0; ww < kDispatchWarps; ++ww) {
+      const int c = wc[ww * E + e];
+      wc[ww * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int64_t base0 = beg; base0 < end; base0 += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t p = base0 + j * 32 + lane;
+      ev[j] = (p < end) ? __ldg(idx + p) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int64_t p = base0 + j * 32 + lane;
+      if (base0 + j * 32 >= end) break;      // warp-uniform
+      const int e = ev[j];
+      const bool valid = (e >= 0) && (e < E);
+      const unsigned m = __match_any_sync(0xffffffffu, valid ? e : -1);
+      int before = 0;
+      if (valid) before = my[e];
+      __syncwarp();
+      if (valid) {
+        const int rank = __popc(m & ((1u << lane) - 1u));
+        const int64_t pos = static_cast<int64_t>(s_blk[e]) * BT + before + rank;
+        slot[p] = static_cast<int32_t>(pos);
+        src[pos] = static_cast<int32_t>(p);
+        if (lane == __ffs(m) - 1) my[e] = before + __popc(m);
+      } else if (p < end) {
+        slot[p] = -1;
+      }
+      __syncwarp();
+    }
+  }
+  // padding rows of every segment: expert e is padded by CTA e % G, one warp per expert
+  for (int e = g + w * G; e < E; e += G * kDispatchWarps) {
     const int64_t lo = static_cast<int64_t>(s_blk[e]) * BT + s_cnt[e];
     const int64_t hi = static_cast<int64_t>(s_blk[e + 1]) * BT;
-    for (int64_t r = lo; r < hi; ++r) src[r] = -1;
+    for (int64_t r = lo + lane; r < hi; r += 32) src[r] = -1;
   }
-  if (tid == 0 && s_bad) atomicCAS(status, 0, MM_MOE_ERR_BAD_ROUTING);
+}
+
+int dispatch_ctas(int64_t TK, int E, int64_t scratch_ints) {
+  int64_t g = (TK + 511) / 512;
+  const int64_t cap_sm = dev_info().sms;
+  if (g > cap_sm) g = cap_sm;
+  if (g > scratch_ints / E) g = scratch_ints / E;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
 }
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
-                            int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(32) * E * sizeof(int);
+                            int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
+                            int64_t scratch_ints, cudaStream_t s) {
+  const int64_t TK = static_cast<int64_t>(T) * K;
+  const int G = dispatch_ctas(TK, E, scratch_ints);
+  int64_t CH = (TK + G - 1) / G;
+  CH = (CH + 32 * kDispatchWarps - 1) / (32 * kDispatchWarps) * (32 * kDispatchWarps);
+  if (CH == 0) CH = 32 * kDispatchWarps;
+  const size_t smem_assign = static_cast<size_t>(kDispatchWarps + 3) * E * sizeof(int) + 16;
   static int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         32 * kMaxE * static_cast<int>(sizeof(int)));
+    cudaError_t e = cudaFuncSetAttribute(dispatch_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (kDispatchWarps + 3) * kMaxE * static_cast<int>(sizeof(int)) + 16);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  dispatch_kernel<<<1, 1024, smem, s>>>(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, status);
+  dispatch_count_kernel<<<G, kDispatchThreads, E * sizeof(int), s>>>(topk_idx, TK, E, CH, scratch, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dispatch_assign_kernel<<<G, kDispatchThreads, smem_assign, s>>>(topk_idx, TK, E, block_m, CH, scratch, cnt,
+                                                                   blk_off, slot, src);
   return cudaGetLastError();
 }
 
@@ -229,37 +305,44 @@ cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk
 }
 
 // ----------------------------------------------------------------------------- weight scales (MX)
-// W1 chunk ((e*(I/64) + n)*(H/128) + kb): rows r < 64 are gate rows n*64+r, rows
-// r >= 64 the matching up rows I + n*64 + (r-64).  W2 chunk ((e*(H/128) + n)*(I/128) + kb):
-// rows n*128 + r.  One thread moves one 4-byte word (4 scale blocks of one row).
+// The GEMMs stream weights in tiles of 256 rows x 128 K; each tile's scales are
+// two 512-byte chunks (rows 0..127, rows 128..255), stored tile after tile:
+//   W1 tile ((e*(I/128) + n)*(H/128) + kb): chunk 0 = gate rows n*128 + r,
+//                                          chunk 1 = up rows I + n*128 + r;
+//   W2 tile ((e*ceil(H/256) + n)*(I/128) + kb): chunk c = rows n*256 + c*128 + r
+//                                          (rows past H are zero).
+// One thread moves one 4-byte word (the 4 scale blocks of one row in one tile).
 __global__ void prepare_sf_mx_kernel(const uint8_t* __restrict__ w1_sf, const uint8_t* __restrict__ w2_sf,
                                      int H, int I, int E, uint8_t* __restrict__ w1_sfp,
                                      uint8_t* __restrict__ w2_sfp) {
-  const int NB1 = I / 64, KB1 = H / 128, NB2 = H / 128, KB2 = I / 128;
-  const int64_t n1 = static_cast<int64_t>(E) * NB1 * KB1 * 128;
-  const int64_t n2 = static_cast<int64_t>(E) * NB2 * KB2 * 128;
+  const int NB1 = I / 128, KB1 = H / 128, NB2 = (H + 255) / 256, KB2 = I / 128;
+  const int64_t n1 = static_cast<int64_t>(E) * NB1 * KB1 * 256;
+  const int64_t n2 = static_cast<int64_t>(E) * NB2 * KB2 * 256;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n1 + n2;
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     if (g < n1) {
-      const int r = static_cast<int>(g & 127);
-      const int64_t chunk = g >> 7;
-      const int kb = static_cast<int>(chunk % KB1);
-      const int n = static_cast<int>((chunk / KB1) % NB1);
-      const int64_t e = chunk / (static_cast<int64_t>(KB1) * NB1);
-      const int row = (r < 64) ? n * 64 + r : I + n * 64 + (r - 64);
+      const int r = static_cast<int>(g & 255);
+      const int64_t tile = g >> 8;
+      const int kb = static_cast<int>(tile % KB1);
+      const int n = static_cast<int>((tile / KB1) % NB1);
+      const int64_t e = tile / (static_cast<int64_t>(KB1) * NB1);
+      const int row = (r < 128) ? n * 128 + r : I + n * 128 + (r - 128);
       const uint32_t word =
           *reinterpret_cast<const uint32_t*>(w1_sf + (e * 2 * I + row) * (H / 32) + kb * 4);
-      *reinterpret_cast<uint32_t*>(w1_sfp + chunk * kSFChunk + sf_chunk_offset(r, 0)) = word;
+      *reinterpret_cast<uint32_t*>(w1_sfp + tile * 2 * kSFChunk + (r >> 7) * kSFChunk + sf_chunk_offset(r & 127, 0)) =
+          word;
     } else {
       const int64_t h = g - n1;
-      const int r = static_cast<int>(h & 127);
-      const int64_t chunk = h >> 7;
-      const int kb = static_cast<int>(chunk % KB2);
-      const int n = static_cast<int>((chunk / KB2) % NB2);
-      const int64_t e = chunk / (static_cast<int64_t>(KB2) * NB2);
-      const int row = n * 128 + r;
-      const uint32_t word = *reinterpret_cast<const uint32_t*>(w2_sf + (e * H + row) * (I / 32) + kb * 4);
-      *reinterpret_cast<uint32_t*>(w2_sfp + chunk * kSFChunk + sf_chunk_offset(r, 0)) = word;
+      const int r = static_cast<int>(h & 255);
+      const int64_t tile = h >> 8;
+      const int kb = static_cast<int>(tile % KB2);
+      const int n = static_cast<int>((tile / KB2) % NB2);
+      const int64_t e = tile / (static_cast<int64_t>(KB2) * NB2);
+      const int row = n * 256 + r;
+      const uint32_t word =
+          row < H ? *reinterpret_cast<const uint32_t*>(w2_sf + (e * H + row) * (I / 32) + kb * 4) : 0u;
+      *reinterpret_cast<uint32_t*>(w2_sfp + tile * 2 * kSFChunk + (r >> 7) * kSFChunk + sf_chunk_offset(r & 127, 0)) =
+          word;
     }
   }
 }

@@ -17,7 +17,7 @@ def M():
     return M
 
 
-def _dispatch(M, idx: np.ndarray, E: int, block: int):
+def _dispatch(M, idx: np.ndarray, E: int, block: int, scratch_bytes=None):
     T, K = idx.shape
     d_idx = torch.from_numpy(idx.astype(np.int32)).cuda()
     cap = T * K + min(T * K, E) * (block - 1) + 1
@@ -26,8 +26,11 @@ def _dispatch(M, idx: np.ndarray, E: int, block: int):
     slot = torch.full((max(T * K, 1),), -7, dtype=torch.int32, device="cuda")
     src = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
     status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    nscr = M.mm_moe_dispatch_scratch_size(T, K, E) if scratch_bytes is None else scratch_bytes
+    scratch = torch.empty(max(nscr, 4), dtype=torch.uint8, device="cuda")
     r = M.mm_moe_dispatch(d_idx.data_ptr(), T, K, E, block, cnt.data_ptr(), blk.data_ptr(), slot.data_ptr(),
-                          src.data_ptr(), cap, status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+                          src.data_ptr(), cap, scratch.data_ptr(), nscr, status.data_ptr(),
+                          torch.cuda.current_stream().cuda_stream)
     assert r == 0
     torch.cuda.synchronize()
     return cnt.cpu().numpy(), blk.cpu().numpy(), slot.cpu().numpy()[:T * K].reshape(T, K), src.cpu().numpy(), \
@@ -72,6 +75,18 @@ def test_dispatch_flags_out_of_range_experts(M):
     ref = O.route(idx, 4, 16)
     assert st == M.MM_MOE_ERR_BAD_ROUTING
     assert np.array_equal(slot, ref["slot"]) and np.array_equal(cnt, ref["cnt"])
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 17])
+def test_dispatch_fewer_ctas_same_result(M, ctas):
+    """A smaller scratch means fewer CTAs; the routing must not change."""
+    cfg = W.CONFIGS["flash"]
+    idx, _ = W.make_routing(cfg, "cpu")
+    idx = idx.numpy()
+    full = _dispatch(M, idx, cfg.E, 128)
+    part = _dispatch(M, idx, cfg.E, 128, scratch_bytes=4 * cfg.E * ctas)
+    for a, b in zip(full, part):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
 
 
 def test_dispatch_skewed_all_one_expert(M):
