@@ -140,6 +140,28 @@ int mm_moe_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, i
                     int32_t* blk_off, int32_t* slot, int32_t* src, int64_t src_capacity, void* scratch,
                     size_t scratch_bytes, int32_t* status, void* stream);
 
+/* mm_moe_dispatch for callers that cannot allocate device memory: no
+ * counterpart in the MegaMoE pages; it exists for the integration.  Some
+ * callers have no way to hand the library scratch: their runtime owns every
+ * device allocation (pre-reserved pools, no cudaMalloc after start-up) or the
+ * call sits on a latency path where an allocation could synchronise the
+ * device.  This entry point takes the same arguments as mm_moe_dispatch minus
+ * the scratch and calls no allocator; its per-CTA counts live in one fixed
+ * 256 KiB device array inside the library, which every GPU that loads the
+ * library holds until the process exits.
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - The array holds min(#SMs, ceil(T*K/512)) x E counts at most 65536
+ *     entries; larger requests return MM_MOE_ERR_WORKSPACE_TOO_SMALL before
+ *     any work is enqueued.
+ *   - All calls share the array and each call rewrites the entries it reads,
+ *     so calls that may overlap on the GPU (other streams, other host
+ *     threads) race with one another: serialise them. */
+int mm_moe_dispatch_noalloc(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
+                            int32_t* blk_off, int32_t* slot, int32_t* src, int64_t src_capacity,
+                            int32_t* status, void* stream);
+
 /* Copy the routing of the last forward out of a workspace (same shapes as mm_moe_dispatch;
  * block_m is reported through *block_m). */
 int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,

@@ -30,7 +30,8 @@ STAGES = ["dispatch", "gather", "l1", "l2", "combine"]
 # every symbol include/mm_moe.h declares
 EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_size", "mm_moe_prepare_weights",
            "mm_moe_forward", "mm_moe_dispatch_scratch_size", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
-           "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region"]
+           "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region",
+           "mm_moe_dispatch_noalloc"]
 
 
 class mm_moe_options(ctypes.Structure):
@@ -72,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "mm_moe_read_intermediate": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _I64, _P, _P, _P]),
             "mm_moe_sync_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
             "mm_moe_status_string": (ctypes.c_char_p, [_I]),
+            "mm_moe_dispatch_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
             "mm_moe_workspace_region": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P),
                                              ctypes.POINTER(_SZ)]),
         }
@@ -122,6 +124,13 @@ def mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_cap
                     status, stream) -> int:
     return lib().mm_moe_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, scratch,
                                  scratch_bytes, status, stream)
+
+
+def mm_moe_dispatch_noalloc(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, status,
+                            stream) -> int:
+    """Routing without caller scratch: for callers that cannot allocate device memory."""
+    return lib().mm_moe_dispatch_noalloc(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, src_capacity, status,
+                                         stream)
 
 
 def mm_moe_read_routing(workspace, opt, T, H, I, E, K, cnt, blk_off, slot, src, stream):

@@ -1,0 +1,74 @@
+// mm_moe_dispatch_noalloc: the routing step (a1) for callers that cannot hand
+// the library any scratch memory.  The per-CTA expert counts that
+// mm_moe_dispatch keeps in caller scratch live here in a fixed file-scope
+// device array instead, so this entry point performs no allocation at all.
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "internal.h"
+
+namespace mm {
+namespace {
+
+// Per-CTA expert counts [CTAs][E] of one call.  Every GPU that loads the
+// library holds these 256 KiB until the process exits.
+constexpr int64_t kNoallocScratchInts = 64 * 1024;
+static __device__ __align__(256) int32_t g_dispatch_scratch[kNoallocScratchInts];
+
+constexpr int kMaxDevices = 64;
+int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
+std::mutex g_scratch_mu;
+
+// Device address of g_dispatch_scratch on the current device, looked up once per device.
+cudaError_t scratch_for_current_device(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace mm
+
+extern "C" int mm_moe_dispatch_noalloc(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
+                                       int32_t* blk_off, int32_t* slot, int32_t* src, int64_t src_capacity,
+                                       int32_t* status, void* stream) {
+  using namespace mm;
+  if (T < 0 || K <= 0 || E <= 0 || K > kMaxK || K > E || E > kMaxE) return MM_MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t(1) << 30)) return MM_MOE_ERR_INVALID_ARG;
+  if (block_m < 16 || block_m > 256 || block_m % 16) return MM_MOE_ERR_INVALID_ARG;
+  if (!cnt || !blk_off || !status || (T > 0 && (!topk_idx || !slot || !src))) return MM_MOE_ERR_INVALID_ARG;
+  const int64_t pairs = static_cast<int64_t>(T) * K;
+  const int64_t live = pairs < E ? pairs : E;
+  if (src_capacity < pairs + live * (block_m - 1)) return MM_MOE_ERR_INVALID_ARG;
+  const DevInfo& d = dev_info();
+  if (!(d.cc_major == 10 && d.cc_minor == 3)) return MM_MOE_ERR_UNSUPPORTED;
+  // The work is split over as many CTAs as mm_moe_dispatch would use with a
+  // full-size scratch; their counts must fit the fixed array.
+  int64_t ctas = (pairs + 511) / 512;
+  if (ctas > d.sms) ctas = d.sms;
+  if (ctas < 1) ctas = 1;
+  if (ctas * E > kNoallocScratchInts) {
+    if (getenv("MM_MOE_DEBUG"))
+      fprintf(stderr, "mm_moe_dispatch_noalloc: %lld CTAs x %d experts exceed the %lld-entry static scratch\n",
+              static_cast<long long>(ctas), E, static_cast<long long>(kNoallocScratchInts));
+    return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  int32_t* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return MM_MOE_ERR_CUDA;
+  // The count kernel rewrites all ctas x E entries before the assign kernel
+  // reads them, so nothing in the array has to be cleared between calls.
+  const cudaError_t e = launch_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, status, scratch,
+                                        ctas * E, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
