@@ -263,7 +263,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       !aligned(workspace, 256) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
     return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
-  if (o.variant != MM_MOE_VARIANT_MX || o.fused) return MM_MOE_ERR_UNSUPPORTED;
+  if (o.fused) return MM_MOE_ERR_UNSUPPORTED;
   const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
   if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
   const WsPtrs W = ws_ptrs(workspace, L);
@@ -282,19 +282,31 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (e == cudaSuccess) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
-  GemmLaunch g{&L, &W, nullptr, nullptr, topk_w, W.dbg, W.prof, static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull,
-               grid};
-  if (e == cudaSuccess) {
-    g.w = static_cast<const uint8_t*>(w1);
-    g.wsfp = static_cast<const uint8_t*>(w1_sfp);
-    e = launch_gemm_mx_l1(g, s);
-  }
-  if (e == cudaSuccess) e = mark(3);
-  if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
-  if (e == cudaSuccess) {
-    g.w = static_cast<const uint8_t*>(w2);
-    g.wsfp = static_cast<const uint8_t*>(w2_sfp);
-    e = launch_gemm_mx_l2(g, s);
+  const uint64_t timeout_ns = static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull;
+  if (o.variant == MM_MOE_VARIANT_MX) {
+    GemmLaunch g{&L, &W, nullptr, nullptr, topk_w, W.dbg, W.prof, timeout_ns, grid};
+    if (e == cudaSuccess) {
+      g.w = static_cast<const uint8_t*>(w1);
+      g.wsfp = static_cast<const uint8_t*>(w1_sfp);
+      e = launch_gemm_mx_l1(g, s);
+    }
+    if (e == cudaSuccess) e = mark(3);
+    if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+    if (e == cudaSuccess) {
+      g.w = static_cast<const uint8_t*>(w2);
+      g.wsfp = static_cast<const uint8_t*>(w2_sfp);
+      e = launch_gemm_mx_l2(g, s);
+    }
+  } else {
+    GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,
+                   grid};
+    if (e == cudaSuccess) e = launch_gemm_f8_l1(g, s);
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess) {
+      g.w = static_cast<const uint8_t*>(w2);
+      g.wsf = static_cast<const float*>(w2_sfp);
+      e = launch_gemm_f8_l2(g, s);
+    }
   }
   if (e == cudaSuccess) e = mark(4);
   if (e == cudaSuccess) e = launch_combine(L, W, topk_idx, out, s);

@@ -1,0 +1,408 @@
+// Grouped GEMMs of the FP8 x FP8 variant on tcgen05 (kind::f8f6f4): e4m3
+// activations with one fp32 scale per 1x128, e4m3 weights with one fp32 scale
+// per 128x128 block, intermediate requantised per 128 with the raw scale
+// amax/448 (DeepGEMM PR #440, "Why the order and not the pool size";
+// MEGAMOE_SM90_DESIGN.md §10.1).
+//
+// fp32 scales cannot ride the MMA, so each 128-K block is multiplied into a
+// fresh TMEM partial and the epilogue promotes it: acc += partial * sx[row,kb]
+// * sw[rows,kb] (the design doc's register-side scale application, §5.3).
+// Tile: 128 pool rows x 256 weight rows (L1: 128 gate + 128 up rows).
+//
+// One CTA per SM, 512 threads in four warpgroups:
+//   WG0 (warps 0..3)   TMA producers, warp p owns pipeline stage p
+//   WG1, WG2 (4..11)   epilogue: two warps per TMEM lane quadrant, each thread
+//                      one pool row and 128 fp32 running sums in registers
+//                      (L1: gate and up columns of the same 64 intermediate
+//                      columns, so SwiGLU stays thread-local)
+//   WG3 (warps 12..15) warp 12: TMEM allocator + single-thread MMA issuer
+// setmaxnreg moves registers from WG0/WG3 (56 each) to WG1/WG2 (200 each);
+// the host refuses to launch unless the kernel was built with exactly 128
+// registers per thread, the total the split assumes.
+// TMEM: two 256-column partial buffers, alternating by k-block, so the MMAs of
+// block kb+1 overlap the promotion of block kb.  Every wait is bounded.
+#include <cuda.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mm {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 512;
+constexpr int kLaunchRegs = 128;       // 65536 / 512
+constexpr int kSmallRegs = 56;         // producers, MMA warpgroup
+constexpr int kEpiRegs = 200;          // epilogue warpgroups
+static_assert(2 * 128 * kSmallRegs + 2 * 128 * kEpiRegs == kThreads * kLaunchRegs, "register split");
+constexpr int kBN = 256;
+constexpr int kTokBytes = kBT * kBK;
+constexpr int kWgtBytes = kBN * kBK;
+constexpr int kTmemCols = 512;
+
+enum : int { kSiteEmpty = 201, kSiteFull = 202, kSitePEmpty = 203, kSitePFull = 204, kSiteAmax = 205 };
+
+struct Args {
+  int T, H, I, E, K;
+  int kblocks;
+  int nblocks;
+  const int* cnt;
+  const int* blk_off;
+  const int* src;
+  const float* topk_w;
+  const float* sw;      // weight scales [E, rows/128, kdim/128]
+  const float* sx;      // token scales [P, kdim/128]
+  uint8_t* out_codes;   // L1: intermediate codes [P, I]
+  float* out_sf;        // L1: intermediate scales [P, I/128]
+  float* partials;      // L2: [K, T, H]
+  int* status;
+  uint64_t timeout_ns;
+};
+
+struct TokenMaps {
+  CUtensorMap b32, b64, b128;
+};
+
+struct SmemLayout {
+  static constexpr int tok = 0;
+  static constexpr int wgt = tok + kStages * kTokBytes;
+  static constexpr int amax = wgt + kStages * kWgtBytes;              // [2][128] fp32
+  static constexpr int meta = amax + 2 * 128 * 4;
+  static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
+  // full[S], empty[S], pfull[2], pempty[2], epi
+  static constexpr int nbars = 2 * kStages + 5;
+  static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
+};
+static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void decode_tile(int tile, int nblocks, const int* blk_off, const int* cnt, int E,
+                                            int& e, int& n, int& b, int& valid) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (blk_off[mid] * nblocks <= tile) lo = mid; else hi = mid - 1;
+  }
+  e = lo;
+  const int nb = blk_off[e + 1] - blk_off[e];
+  const int local = tile - blk_off[e] * nblocks;
+  n = local / nb;
+  const int bl = local - n * nb;
+  b = blk_off[e] + bl;
+  const int rem = cnt[e] - bl * kBT;
+  valid = rem < kBT ? rem : kBT;
+}
+
+// kind::f8f6f4 instruction descriptor: fp32 accumulator (bits [5:4] = 1),
+// A = B = e4m3 (0), both K-major, N>>3 in [22:17], M>>4 in [28:24].
+__device__ __forceinline__ uint32_t make_idesc() {
+  return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
+
+template <int PHASE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ TokenMaps tmT, const Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int E = args.E;
+  int* s_blk = reinterpret_cast<int*>(smem + SmemLayout::meta);
+  int* s_cnt = s_blk + E + 1;
+  float* s_amax = reinterpret_cast<float*>(smem + SmemLayout::amax);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars_after_meta(E));
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* pfull = bars + 2 * kStages;
+  uint64_t* pempty = pfull + 2;
+  uint64_t* epibar = pempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
+  const Status st{args.status, args.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], 8);
+    }
+    mbar_init(epibar, 256);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp < kStages && lane == 0) {
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmT.b32);
+    prefetch_tmap(&tmT.b64);
+    prefetch_tmap(&tmT.b128);
+  }
+  if (warp == 12) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i <= E; i += kThreads) s_blk[i] = args.blk_off[i];
+  for (int i = threadIdx.x; i < E; i += kThreads) s_cnt[i] = args.cnt[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const int total = s_blk[E] * args.nblocks;
+  const int KB = args.kblocks;
+
+  if (wg == 0) {
+    regs_dec();
+    // ------------------------------------------------------------------ TMA producers
+    if (lane == 0) {
+      const int p = warp;
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_t = policy_evict_last();
+      uint8_t* tk = smem + SmemLayout::tok + p * kTokBytes;
+      uint8_t* wgp = smem + SmemLayout::wgt + p * kWgtBytes;
+      int step = 0;
+      for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
+        int e, n, b, valid;
+        decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
+        const CUtensorMap* tt = valid <= 32 ? &tmT.b32 : (valid <= 64 ? &tmT.b64 : &tmT.b128);
+        const int rows = valid <= 32 ? 32 : (valid <= 64 ? 64 : 128);
+        const uint32_t bytes = rows * kBK + kWgtBytes;
+        int kb = ((p - step) % kStages + kStages) % kStages;
+        for (; kb < KB; kb += kStages) {
+          const uint32_t phase = ((step + kb) / kStages) & 1;
+          if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
+          mbar_arrive_expect_tx(&full[p], bytes);
+          const int kc = kb * kBK;
+          tma_load_2d(tk, tt, &full[p], kc, b * kBT, pol_t);
+          if (PHASE == 1) tma_load_3d(wgp, &tmW, &full[p], kc, e * 2 * args.I + n * 128, 0, pol_w);
+          else tma_load_2d(wgp, &tmW, &full[p], kc, e * args.H + n * kBN, pol_w);
+        }
+        step += KB;
+      }
+    }
+  } else if (wg == 3) {
+    regs_dec();
+    // ------------------------------------------------------------------ MMA issuer
+    if (warp == 12 && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0;                                 // global k-block counter: partial buffer g & 1
+      for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int pb = g & 1;
+          if (!mbar_wait(&pempty[pb], ((g >> 1) & 1) ^ 1, st, s_abort, kSitePEmpty)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, st, s_abort, kSiteFull)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + SmemLayout::tok + stage * kTokBytes);
+          const uint32_t b0 = smem_u32(smem + SmemLayout::wgt + stage * kWgtBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_f8f6f4(tmem + pb * kBN, make_smem_desc(a0 + kk * 32, 16, 1024, 2),
+                          make_smem_desc(b0 + kk * 32, 16, 1024, 2), make_idesc(), kk != 0);
+          tc_commit(&empty[stage]);
+          tc_commit(&pfull[pb]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else {
+    regs_inc();
+    // ------------------------------------------------------------------ epilogue (8 warps)
+    const int q = warp & 3;
+    const int half = wg - 1;                    // 0 or 1
+    const int m = q * 32 + lane;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    // TMEM columns this thread accumulates: L1 gate [64h, 64h+64) and up
+    // [128+64h, 128+64h+64); L2 [128h, 128h+128)
+    const int c0 = PHASE == 1 ? 64 * half : 128 * half;
+    const int c1 = PHASE == 1 ? 128 + 64 * half : 128 * half + 64;
+    int g = 0;
+    uint32_t ephase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, n, b, valid;
+      decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
+      const bool live = m < valid;
+      const size_t row = static_cast<size_t>(b) * kBT + m;
+      const int s = live ? __ldg(args.src + row) : 0;
+      const float w = (PHASE == 1 && live) ? __ldg(args.topk_w + s) : 0.f;
+      // weight scale rows (in blocks of 128) of the two column groups
+      int wr0, wr1, wrows;
+      if (PHASE == 1) { wr0 = n; wr1 = (args.I >> 7) + n; wrows = 2 * args.I / 128; }
+      else {
+        wrows = args.H / 128;
+        wr0 = 2 * n + half < wrows ? 2 * n + half : wrows - 1;   // a half past H is never stored
+        wr1 = wr0;
+      }
+      const float* swe = args.sw + static_cast<size_t>(e) * wrows * KB;
+      const float* sxr = args.sx + row * KB;
+      float acc0[64], acc1[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
+      bool ok = true;
+      float sx_next = live ? __ldg(sxr) : 0.f;
+      for (int kb = 0; kb < KB; ++kb, ++g) {
+        const float sxk = sx_next;
+        if (kb + 1 < KB) sx_next = live ? __ldg(sxr + kb + 1) : 0.f;
+        const float f0 = sxk * __ldg(swe + static_cast<size_t>(wr0) * KB + kb);
+        const float f1 = sxk * __ldg(swe + static_cast<size_t>(wr1) * KB + kb);
+        const int pb = g & 1;
+        if (!mbar_wait(&pfull[pb], (g >> 1) & 1, st, s_abort, kSitePFull)) { ok = false; break; }
+        tc_fence_after();
+        // one 32-column slice at a time keeps at most 128 sums + 32 loaded values live
+        const uint32_t tb = tlane + pb * kBN;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tb + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc0[j] = fmaf(__uint_as_float(v[j]), f0, acc0[j]);
+        tmem_ld_32x32b_x32(tb + c0 + 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc0[32 + j] = fmaf(__uint_as_float(v[j]), f0, acc0[32 + j]);
+        tmem_ld_32x32b_x32(tb + c1, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc1[j] = fmaf(__uint_as_float(v[j]), f1, acc1[j]);
+        tmem_ld_32x32b_x32(tb + c1 + 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc1[32 + j] = fmaf(__uint_as_float(v[j]), f1, acc1[32 + j]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[pb]);
+      }
+      if (!ok) break;
+      if (PHASE == 1) {
+        // a = silu(gate) * up * w over this thread's 64 intermediate columns
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float gv = acc0[j];
+          acc0[j] = gv * __frcp_rn(1.0f + __expf(-gv)) * acc1[j] * w;
+          amax = fmaxf(amax, fabsf(acc0[j]));
+        }
+        // the 128-column requant block spans both halves: exchange row amax
+        s_amax[half * 128 + m] = amax;
+        mbar_arrive(epibar);
+        if (!mbar_wait(epibar, ephase, st, s_abort, kSiteAmax)) break;
+        ephase ^= 1;
+        amax = fmaxf(amax, s_amax[(half ^ 1) * 128 + m]);
+        if (live) {
+          const float sf = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t lo = cvt_e4m3x2(__fdiv_rn(acc0[4 * i], sf), __fdiv_rn(acc0[4 * i + 1], sf));
+            const uint32_t hi = cvt_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sf), __fdiv_rn(acc0[4 * i + 3], sf));
+            packed[i] = lo | (hi << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(args.out_codes + row * args.I + n * 128 + 64 * half);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          if (half == 0) args.out_sf[row * (args.I / 128) + n] = sf;
+        }
+        // second rendezvous: s_amax may be overwritten by the next tile only after both halves read it
+        mbar_arrive(epibar);
+        if (!mbar_wait(epibar, ephase, st, s_abort, kSiteAmax)) break;
+        ephase ^= 1;
+      } else {
+        if (live && n * kBN + 128 * half < args.H) {
+          const int t = s / args.K;
+          const int k = s - t * args.K;
+          float4* dst = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(k) * args.T + t) * args.H +
+                                                  n * kBN + 128 * half);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            dst[i] = make_float4(acc0[4 * i], acc0[4 * i + 1], acc0[4 * i + 2], acc0[4 * i + 3]);
+            dst[16 + i] = make_float4(acc1[4 * i], acc1[4 * i + 1], acc1[4 * i + 2], acc1[4 * i + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*s_abort) {
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 200000) {}
+  }
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int PHASE>
+cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
+  const Layout& L = *g.L;
+  const WsPtrs& W = *g.W;
+  // The register split assumes the kernel starts with exactly kLaunchRegs per thread.
+  static int checked[2] = {0, 0};
+  if (!checked[PHASE - 1]) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_f8_kernel<PHASE>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(gemm_f8_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SmemLayout::total(kMaxE) + 1024);
+    if (e != cudaSuccess) return e;
+    checked[PHASE - 1] = 1;
+  }
+  CUtensorMap tmW;
+  TokenMaps tmT;
+  Args a{};
+  a.T = L.T; a.H = L.H; a.I = L.I; a.E = L.E; a.K = L.K;
+  a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;
+  a.status = W.status; a.timeout_ns = g.timeout_ns;
+  a.sw = g.wsf;
+  const uint8_t* pool;
+  int kdim;
+  if (PHASE == 1) {
+    a.kblocks = L.H / 128;
+    a.nblocks = L.I / 128;
+    a.sx = reinterpret_cast<const float*>(W.pool_x_sf);
+    a.out_codes = W.pool2;
+    a.out_sf = reinterpret_cast<float*>(W.pool2_sf);
+    const uint64_t dims[3] = {static_cast<uint64_t>(L.H), static_cast<uint64_t>(L.E) * 2 * L.I - L.I, 2};
+    const uint64_t strides[2] = {static_cast<uint64_t>(L.H), static_cast<uint64_t>(L.I) * L.H};
+    const uint32_t box[3] = {128, 128, 2};
+    if (encode_tmap(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    pool = W.pool_x;
+    kdim = L.H;
+  } else {
+    a.kblocks = L.I / 128;
+    a.nblocks = (L.H + kBN - 1) / kBN;
+    a.sx = reinterpret_cast<const float*>(W.pool2_sf);
+    a.partials = W.part;
+    if (encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.w, L.I, static_cast<uint64_t>(L.E) * L.H, L.I, 128,
+                       kBN, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    pool = W.pool2;
+    kdim = L.I;
+  }
+  CUtensorMap* maps[3] = {&tmT.b32, &tmT.b64, &tmT.b128};
+  for (int i = 0; i < 3; ++i)
+    if (encode_tmap_2d(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, pool, kdim, L.P, kdim, 128, 32u << i,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  gemm_f8_kernel<PHASE><<<g.grid, kThreads, SmemLayout::total(L.E) + 1024, s>>>(tmW, tmT, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s) { return launch_impl<1>(g, s); }
+cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s) { return launch_impl<2>(g, s); }
+
+}  // namespace mm

@@ -76,6 +76,17 @@ struct GemmLaunch {
   uint64_t timeout_ns;
   int grid;
 };
+struct GemmLaunchF8 {
+  const Layout* L;
+  const WsPtrs* W;
+  const uint8_t* w;          // e4m3 weights (w1 or w2)
+  const float* wsf;          // their fp32 128x128 block scales
+  const float* topk_w;
+  uint64_t timeout_ns;
+  int grid;
+};
+cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s);
+cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s);
 cudaError_t launch_gemm_mx_l1(const GemmLaunch& g, cudaStream_t s);
 cudaError_t launch_gemm_mx_l2(const GemmLaunch& g, cudaStream_t s);
 

@@ -75,7 +75,10 @@ def oracle_rows(cfg, dev_inp: dict, rows, keep_intermediate=True):
 
 def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict) -> float:
     """Fraction of intermediate e4m3 codes equal (by value) to the oracle's, with
-    every code of a block whose scale differs counted as a mismatch."""
+    every code of a block whose scale differs counted as a mismatch.  MX scales
+    are UE8M0 bytes and must be equal; FP8 scales are raw fp32 amax/448, which
+    moves with the last bit of the fp32 accumulation, so they must agree to a
+    relative 1e-5."""
     rows = int(M.mm_moe_workspace_region(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, 4)[1] // 4)
     codes = torch.empty(rows, cfg.I, dtype=torch.uint8, device="cuda")
     bs = 32 if cfg.variant == "mx" else 128
@@ -90,7 +93,10 @@ def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict) -> float:
     for (t, k), (oc, osf) in inter.items():
         row = int(slot[t, k])
         assert row >= 0
-        same_sf = np.repeat(sf[row] == osf, bs)
+        if cfg.variant == "mx":
+            same_sf = np.repeat(sf[row] == osf, bs)
+        else:
+            same_sf = np.repeat(np.abs(sf[row].astype(np.float64) / osf.astype(np.float64) - 1.0) < 1e-5, bs)
         same = same_sf & (O.e4m3_decode(codes[row]) == O.e4m3_decode(oc))
         total += same.size
         match += int(same.sum())

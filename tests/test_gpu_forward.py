@@ -24,21 +24,30 @@ SMALL = {
     "ragged": W.Config("ragged", T=300, H=512, I=384, E=5, K=2, seed=21),
     "k1": W.Config("k1", T=77, H=384, I=256, E=3, K=1, seed=22),
     "manyexp": W.Config("manyexp", T=40, H=256, I=128, E=64, K=6, seed=23),
+    # FP8 x FP8 with fp32 per-128 scales
+    "f8_tiny": W.Config("f8_tiny", T=24, H=256, I=256, E=4, K=2, variant="f8", seed=24),
+    "f8_ragged": W.Config("f8_ragged", T=300, H=512, I=384, E=5, K=2, variant="f8", seed=25),
+    "f8_wide": W.Config("f8_wide", T=150, H=384, I=512, E=3, K=3, variant="f8", seed=26),
 }
 
 
+def _opt_for(M, cfg, **kw):
+    return M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8, **kw)
+
+
 def _full_check(M, cfg, inp, opt=None):
+    opt = opt or _opt_for(M, cfg)
     dev = to_dev(inp)
     out, ws, prepared, (code, where) = run_forward(M, cfg, dev, opt)
     assert code == 0, f"device status {code} at site {where}"
-    cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt or M.options())
+    cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt)
     ref_route = O.route(inp["topk_idx"].numpy(), cfg.E, bm)
     assert np.array_equal(slot, ref_route["slot"])
     rows = np.arange(cfg.T)
     ref, inter = oracle_rows(cfg, dev, rows)
     got = out.float().cpu().numpy()
     stats = check_output(got, ref, cfg.name)
-    frac = intermediate_match(M, cfg, ws, opt or M.options(), slot, inter)
+    frac = intermediate_match(M, cfg, ws, opt, slot, inter)
     assert frac >= 0.999, f"intermediate code match {frac:.5f}"
     return out, stats
 

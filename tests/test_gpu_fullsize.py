@@ -14,7 +14,7 @@ from gpu_util import check_output, intermediate_match, oracle_rows, read_routing
 
 pytestmark = pytest.mark.gpu
 
-SAMPLE_ROWS = {"flash": 8, "pro": 4, "decode": 12}
+SAMPLE_ROWS = {"flash": 8, "pro": 4, "decode": 12, "f8": 4}
 
 
 @pytest.fixture(scope="module")
@@ -25,13 +25,13 @@ def M():
     return M
 
 
-@pytest.mark.parametrize("name", ["flash", "decode", "pro"])
+@pytest.mark.parametrize("name", ["flash", "decode", "pro", "f8"])
 def test_fullsize_sampled_rows(M, name):
     cfg = W.CONFIGS[name]
     dev = W.make_inputs(cfg, "cuda")
     out, ws, prepared, (code, where) = run_forward(M, cfg, dev)
     assert code == 0, f"device status {code} at site {where}"
-    opt = M.options()
+    opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
     cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt)
     ref_route = O.route(dev["topk_idx"].cpu().numpy(), cfg.E, bm)
     assert np.array_equal(cnt, ref_route["cnt"]) and np.array_equal(blk, ref_route["blk_off"])
