@@ -152,7 +152,9 @@ def workload_accounting(cfg, idx: np.ndarray):
     flops = 6.0 * pairs * H * I
     l1_bytes = touched * w1_b + pairs * x_b + pairs * a_b
     l2_bytes = touched * w2_b + pairs * a_b + pairs * H * 4
+    gather_bytes = pairs * x_b * 2           # read the token's row, write its pool row
     return {"touched_experts": touched, "pairs": pairs, "step_bytes": step_bytes, "flops": flops,
+            "gather_bytes": gather_bytes,
             "l1_bytes": l1_bytes, "l2_bytes": l2_bytes, "l1_flops": 4.0 * pairs * H * I,
             "l2_flops": 2.0 * pairs * H * I}
 
@@ -184,6 +186,9 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.set_device(dev)
     inp = W.make_inputs(cfg, dev)
     opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
+    if args.fused is not None:
+        opt.fused = args.fused
+    fused = bool(opt.fused) and cfg.variant == "mx"
     w1p, w2p = M.prepare_weights(inp["w1_sf"], inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
     ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt, dev)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
@@ -217,7 +222,7 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
-        o = M.options(opt.variant)
+        o = M.options(opt.variant, fused=opt.fused)
         o.timing_events = ctypes.cast(arrays[i], ctypes.c_void_p)
         fwd(o)
     torch.cuda.synchronize()
@@ -261,10 +266,15 @@ def run_ours(args, ws_n, rank, local):
     fp8 = float(pk["bf16_tflops"]) * FP8_OVER_BF16
     stage_mean = stage_ms.mean(0)
     l1_ms, l2_ms = float(stage_mean[2]), float(stage_mean[3])
-    # dominant kernel: the one with the largest share of the step
-    dom = "l1" if l1_ms >= l2_ms else "l2"
-    dom_ms = l1_ms if dom == "l1" else l2_ms
-    dom_bytes = acc["l1_bytes"] if dom == "l1" else acc["l2_bytes"]
+    if fused:
+        # one launch runs gather, L1 and L2: its bytes are all three
+        dom, dom_ms = "fused", l1_ms + l2_ms
+        dom_bytes = acc["l1_bytes"] + acc["l2_bytes"] + acc["gather_bytes"]
+    else:
+        # dominant kernel: the one with the largest share of the step
+        dom = "l1" if l1_ms >= l2_ms else "l2"
+        dom_ms = l1_ms if dom == "l1" else l2_ms
+        dom_bytes = acc["l1_bytes"] if dom == "l1" else acc["l2_bytes"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     t_roof = max(acc["flops"] / (fp8 * 1e12), acc["step_bytes"] / (hbm * 1e9))
     tokens_per_s = ws_n * cfg.T / (step_ms * 1e-3)
@@ -287,22 +297,26 @@ def run_ours(args, ws_n, rank, local):
                                f"{'MX e4m3 x e2m1 UE8M0/32' if cfg.variant == 'mx' else 'FP8 e4m3 per-128'}",
                    "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K, "seed": cfg.seed,
                    "l2_policy": "L2 flushed (512 MiB write) before every timed step; weights 3+ GB >> L2",
-                   "parallelism": f"replicas x{ws_n} (no data-path collective)"},
+                   "parallelism": f"replicas x{ws_n} (no data-path collective)",
+                   "fused_stream": fused},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
         "path_roofline": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (step_ms * 1e-3),
                           "bytes": acc["step_bytes"], "flops": acc["flops"],
                           "touched_experts": acc["touched_experts"],
                           "peaks": {"hbm_gbs": hbm, "fp8_tflops": fp8, "source": pk_src,
                                     "fp8_from": "bf16_tflops x 2 (nominal fp8/bf16 ratio)"}},
-        "stages_ms": {s: float(v) for s, v in zip(M.STAGES, stage_mean)},
-        "roofline": {"kernel": f"gemm_mx_kernel<{1 if dom == 'l1' else 2}> ({dom.upper()} grouped GEMM)",
+        "stages_ms": ({"dispatch": float(stage_mean[0]), "fused_gather_l1_l2": float(stage_mean[2] + stage_mean[3]),
+                       "combine": float(stage_mean[4])} if fused else
+                      {s: float(v) for s, v in zip(M.STAGES, stage_mean)}),
+        "roofline": {"kernel": ("gemm_mx_kernel (fused gather + L1 + L2 stream)" if fused else
+                                f"gemm_{'mx' if cfg.variant == 'mx' else 'f8'}_kernel ({dom.upper()} grouped GEMM)"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": kernel_traffic(dom, cfg.name),
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "peak_source": f"{pk_src} hbm_gbs (STREAM-style copy)"},
         "e2e": {"value": ws_n * cfg.T / (e2e_step_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
-        "gpu_launches": 5 * K,
+        "gpu_launches": (4 if fused else 6) * K,   # dispatch x2, [gather], GEMM(s), combine
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -378,6 +392,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", type=int, choices=[0, 1], default=None,
+                    help="1: gather + L1 + L2 as one lag-ordered persistent launch; default: the library's")
     args = ap.parse_args()
     ws_n, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":

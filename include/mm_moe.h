@@ -81,8 +81,11 @@ extern "C" {
 typedef struct mm_moe_options {
   int variant;                  /* MM_MOE_VARIANT_MX (default) or MM_MOE_VARIANT_F8 */
   int fused;                    /* 1 (default): one persistent kernel runs gather, L1 and L2 as one
-                                   lag-ordered task stream; 0: separate gather / L1 / L2 launches */
-  int lag_units;                /* fused path: lag of L2 behind L1 in units of 8 M-blocks; -1 = auto */
+                                   lag-ordered task stream (MX format; the F8 variant and the L1
+                                   debug dump always use separate launches); 0: separate gather /
+                                   L1 / L2 launches.  Both give bit-identical results. */
+  int lag_units;                /* fused stream: how many experts the L2 tiles trail the L1 tiles
+                                   (0..64); -1 = auto */
   int retain_intermediate;      /* keep the whole requantised intermediate readable after the call
                                    (mm_moe_read_intermediate) */
   unsigned wait_timeout_ms;     /* deadline of every device-side wait; 0 = default (2000 ms) */

@@ -25,6 +25,7 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.cnt = o; o = align_up(o + sizeof(int) * E, 256);
   L.blk_off = o; o = align_up(o + sizeof(int) * (E + 1), 256);
   L.dscr = o; o = align_up(o + sizeof(int) * static_cast<size_t>(kDispatchMaxCtas) * E, 256);
+  L.ctr = o; o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nblk_cap), 256);
   L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
   L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
   L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
@@ -52,6 +53,7 @@ WsPtrs ws_ptrs(void* ws, const Layout& L) {
   W.cnt = reinterpret_cast<int*>(b + L.cnt);
   W.blk_off = reinterpret_cast<int*>(b + L.blk_off);
   W.dscr = reinterpret_cast<int*>(b + L.dscr);
+  W.ctr = reinterpret_cast<int*>(b + L.ctr);
   W.slot = reinterpret_cast<int*>(b + L.slot);
   W.src = reinterpret_cast<int*>(b + L.src);
   W.pool_x = b + L.pool_x;
@@ -175,7 +177,7 @@ void mm_moe_default_options(mm_moe_options* opt) {
   if (!opt) return;
   memset(opt, 0, sizeof(*opt));
   opt->variant = MM_MOE_VARIANT_MX;
-  opt->fused = 0;
+  opt->fused = 1;
   opt->lag_units = -1;
   opt->retain_intermediate = 0;
   opt->wait_timeout_ms = 2000;
@@ -263,7 +265,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       !aligned(workspace, 256) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
     return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
-  if (o.fused) return MM_MOE_ERR_UNSUPPORTED;
+  // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
+  const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
   const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
   if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
   const WsPtrs W = ws_ptrs(workspace, L);
@@ -279,23 +282,25 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, W.dscr,
                         static_cast<int64_t>(kDispatchMaxCtas) * E, s);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, s);
+  if (e == cudaSuccess && !fused) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
   const uint64_t timeout_ns = static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull;
   if (o.variant == MM_MOE_VARIANT_MX) {
-    GemmLaunch g{&L, &W, nullptr, nullptr, topk_w, W.dbg, W.prof, timeout_ns, grid};
-    if (e == cudaSuccess) {
-      g.w = static_cast<const uint8_t*>(w1);
-      g.wsfp = static_cast<const uint8_t*>(w1_sfp);
-      e = launch_gemm_mx_l1(g, s);
-    }
-    if (e == cudaSuccess) e = mark(3);
-    if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
-    if (e == cudaSuccess) {
-      g.w = static_cast<const uint8_t*>(w2);
-      g.wsfp = static_cast<const uint8_t*>(w2_sfp);
-      e = launch_gemm_mx_l2(g, s);
+    GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
+                 static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
+                 static_cast<const uint8_t*>(x), x_sf, topk_w, W.dbg, W.prof, timeout_ns, grid};
+    if (fused) {
+      // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
+      if (e == cudaSuccess) e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * 2 * static_cast<size_t>(L.nblk_cap), s);
+      const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
+      if (e == cudaSuccess) e = launch_gemm_mx(g, 3, lag, s);
+      if (e == cudaSuccess) e = mark(3);
+    } else {
+      if (e == cudaSuccess) e = launch_gemm_mx(g, 1, 0, s);
+      if (e == cudaSuccess) e = mark(3);
+      if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+      if (e == cudaSuccess) e = launch_gemm_mx(g, 2, 0, s);
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,

@@ -3,33 +3,44 @@
 //
 // Tile: M = 128 pool rows (the tokens of one pool block of one expert) x
 // N = 256 weight rows x K in stages of 128.  On GB300 one M=128, K=32 tcgen05
-// MMA takes the same ~143 cycles of tensor-pipe time for every N up to 256
-// (measured), so the weights are the N operand at its full width and a block
-// with few tokens only wastes accumulator rows, not MMA issue slots.
-//   L1: the 256 rows are 128 gate rows and the matching 128 up rows, so a
-//       token's gate and up values for 128 intermediate columns sit in one
-//       TMEM lane and SwiGLU, the top-k weight and the per-32 UE8M0 requant
-//       are thread-local (llm-infra-atlas "07 · MegaMoE" §8).
-//   L2: 256 output columns; the epilogue writes fp32 partials part[k][t][h].
+// MMA takes the same tensor-pipe time for every N up to 256 (measured), so the
+// weights are the N operand at its full width and a block with few tokens
+// only wastes accumulator rows, not MMA issue slots.
+//   L1 task: the 256 rows are 128 gate rows and the matching 128 up rows, so a
+//            token's gate and up values for 128 intermediate columns sit in one
+//            TMEM lane and SwiGLU, the top-k weight and the per-32 UE8M0
+//            requant are thread-local (llm-infra-atlas "07 · MegaMoE" §8).
+//   L2 task: 256 output columns; the epilogue writes fp32 partials part[k][t][h].
 //
-// Persistent, warp-specialised, one CTA per SM (416 threads):
-//   warps 0..3   TMA producers, warp p owns pipeline stage p.  A TMA-issuing
-//                thread keeps only about four bulk-tensor copies in flight
-//                (measured on GB300), so each stage has its own issuer.  Per
-//                stage: one token tile (box of 32, 64 or 128 rows by the
-//                block's size), one weight tile (16U4_ALIGN16B, unpacked to
-//                1 byte per element in shared memory; L1 fetches the gate and
-//                the up rows with one 3-D copy) and the scale chunks.
-//   warps 4..11  epilogue: tcgen05.ld of the fp32 accumulator, one token row
-//                per thread; the two warps of a TMEM lane quadrant split the
-//                columns, so the accumulator is drained (and released to the
-//                next tile's MMAs) sooner.
-//   warp 12      TMEM allocator + single-thread MMA issuer (tcgen05.cp of the
-//                scales into TMEM, 4 MMAs of K=32 per stage).
-// The 128 x 256 fp32 accumulator takes half the TMEM; while the epilogue
-// drains it the producers keep filling the stages of the next tile.  Every
-// wait is bounded: on a deadline the kernel records MM_MOE_ERR_TIMEOUT and a
-// site code and returns.
+// One kernel, three task streams (mode):
+//   1  all L1 tiles, expert by expert (weight tile outer, pool block inner)
+//   2  all L2 tiles, same order
+//   3  one lag-ordered stream (DeepGEMM PR #440, "How it works"): segment u
+//      holds expert u's L1 tiles and then expert (u - lag)'s L2 tiles, so L2
+//      trails L1 by `lag` experts.  The pool rows are gathered in the kernel by
+//      two gather warps per CTA that publish per-block row counts; the L1
+//      epilogue publishes per-block tile counts; a producer waits on them
+//      (acquire, bounded) before it loads a block ("07 · MegaMoE" §6: per-block
+//      arrival counters instead of kernel boundaries).  Every wait points at a
+//      task earlier in the global order and every CTA is resident (one per
+//      SM, grid <= #SMs) and works its tasks in that order, so the stream
+//      cannot deadlock.
+//
+// Warps (480 threads, one CTA per SM):
+//   0..3    TMA producers, warp p owns pipeline stage p.  A TMA-issuing thread
+//           keeps only about four bulk-tensor copies in flight (measured on
+//           GB300), so each stage has its own issuer.  Per stage: one token
+//           tile (box of 32, 64 or 128 rows by the block's size), one weight
+//           tile (16U4_ALIGN16B, unpacked to 1 byte per element in shared
+//           memory; L1 fetches gate and up rows with one 3-D copy) and the
+//           scale chunks.
+//   4..11   epilogue: one token row per thread, the two warps of a TMEM lane
+//           quadrant split the columns.
+//   12      TMEM allocator + single-thread MMA issuer (tcgen05.cp of the scales
+//           into TMEM, 4 MMAs of K=32 per stage).
+//   13..14  gather warps (mode 3).
+// Every wait is bounded: on a deadline the kernel records MM_MOE_ERR_TIMEOUT
+// and a site code and returns.
 #include <cuda.h>
 
 #include "internal.h"
@@ -43,7 +54,9 @@ constexpr int kProducers = kStages;    // one issuing warp per stage
 constexpr int kEpiWarp0 = kProducers;  // eight epilogue warps, two per TMEM lane quadrant
 constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = kEpiWarp0 + kEpiWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kGatherWarp0 = kMmaWarp + 1;
+constexpr int kGatherWarps = 2;
+constexpr int kThreads = (kGatherWarp0 + kGatherWarps) * 32;
 constexpr int kBN = 256;               // weight rows per tile (MMA N)
 constexpr int kTokBytes = kBT * kBK;   // 128 token rows x 128 K
 constexpr int kWgtBytes = kBN * kBK;   // 256 weight rows x 128 K, 1 byte per element in smem
@@ -56,62 +69,105 @@ constexpr int kSfCol0 = kBN;           // scale-factor columns after the accumul
 constexpr int kSfColsPerStage = 12;    // 4 (tokens) + 8 (weights)
 
 // wait-site codes reported through the status word
-enum : int { kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104 };
+enum : int {
+  kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104,
+  kSiteGathered = 105, kSiteL1Done = 106
+};
 
 struct Args {
   int T, H, I, E, K;
-  int kblocks;        // contraction / 128
-  int nblocks;        // weight tiles per expert
+  int KB1, KB2, NB1, NB2;
+  int mode;            // 1, 2 or 3 (see above)
+  int lag;             // mode 3: experts by which L2 trails L1
   const int* cnt;
   const int* blk_off;
   const int* src;
   const float* topk_w;
-  const uint8_t* sfw;   // prepared weight scale chunks (two per tile and k-block)
-  const uint8_t* sft;   // token scale chunks (one per pool block and k-block)
-  uint8_t* out_codes;   // L1: intermediate codes [P, I]
-  uint8_t* out_sf;      // L1: intermediate scale chunks
-  float* partials;      // L2: [K, T, H]
-  float* dbg;           // L1: raw gate|up accumulators [P, 2I] or null
+  const uint8_t* x;          // mode 3 gather: activations [T, H] and scales [T, H/32]
+  const uint8_t* x_sf;
+  uint8_t* pool_x;           // [P, H]
+  uint8_t* pool_x_sf;        // chunks [P/128][H/128][512]
+  const uint8_t* sfw1;       // prepared weight scale chunks (two per tile and k-block)
+  const uint8_t* sfw2;
+  uint8_t* pool2;            // intermediate codes [P, I]
+  uint8_t* pool2_sf;         // intermediate scale chunks [P/128][I/128][512]
+  float* partials;           // [K, T, H]
+  float* dbg;                // raw L1 accumulators [P, 2I] or null
+  int* ctr_gather;           // mode 3: rows gathered per pool block
+  int* ctr_l1;               // mode 3: L1 epilogue warps finished per pool block
   int* status;
   uint64_t timeout_ns;
-  unsigned long long* prof;   // per-CTA wait/busy nanoseconds (debug_flags bit 1) or null
+  unsigned long long* prof;  // per-CTA wait/busy nanoseconds (debug_flags bit 1) or null
 };
 
-struct TokenMaps {
-  CUtensorMap b32, b64, b128;   // pool rows, boxes of 32 / 64 / 128 rows x 128 K
+struct Maps {
+  CUtensorMap w1, w2;                       // weights
+  CUtensorMap x32, x64, x128;               // pooled activations, boxes of 32/64/128 rows
+  CUtensorMap a32, a64, a128;               // intermediate codes
 };
+
+constexpr int kMaxLag = 64;
 
 struct SmemLayout {
   static constexpr int tok = 0;
   static constexpr int wgt = tok + kStages * kTokBytes;
   static constexpr int sft = wgt + kStages * kWgtBytes;
   static constexpr int sfw = sft + kStages * kSFChunk;
-  static constexpr int meta = sfw + kStages * 2 * kSFChunk;           // blk_off[E+1], cnt[E]
-  static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
-  // barriers: full[S], empty[S], tfull, tempty
-  static constexpr int nbars = 2 * kStages + 2;
+  static constexpr int meta = sfw + kStages * 2 * kSFChunk;   // blk_off[E+1], cnt[E], seg[E+lag+1]
+  static constexpr int meta_ints(int E) { return (E + 1) + E + (E + kMaxLag + 1); }
+  static constexpr int bars_after_meta(int E) { return meta + (meta_ints(E) * 4 + 15) / 16 * 16; }
+  static constexpr int nbars = 2 * kStages + 2;  // full[S], empty[S], tfull, tempty
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory budget");
 
-__device__ __forceinline__ void decode_tile(int tile, int nblocks, const int* blk_off, const int* cnt, int E,
-                                            int& e, int& n, int& b, int& valid) {
-  // tiles run expert by expert; inside an expert weight tile n outer, pool block inner
-  int lo = 0, hi = E - 1;                      // largest e with blk_off[e] * nblocks <= tile
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (blk_off[mid] * nblocks <= tile) lo = mid; else hi = mid - 1;
+struct Task {
+  int type;      // 1 = L1, 2 = L2
+  int e, n, b, valid;
+};
+
+struct Sched {
+  const int* blk;   // [E+1] pool-block offsets per expert
+  const int* cnt;   // [E]
+  const int* seg;   // [E+lag+1] mode-3 segment offsets
+  int E, NB1, NB2, mode, lag, total;
+
+  __device__ __forceinline__ int largest_leq(const int* a, int n, int v, int scale) const {
+    int lo = 0, hi = n - 1;                  // largest i < n with a[i] * scale <= v
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a[mid] * scale <= v) lo = mid; else hi = mid - 1;
+    }
+    return lo;
   }
-  e = lo;
-  const int nb = blk_off[e + 1] - blk_off[e];
-  const int local = tile - blk_off[e] * nblocks;
-  n = local / nb;
-  const int bl = local - n * nb;
-  b = blk_off[e] + bl;
-  const int rem = cnt[e] - bl * kBT;
-  valid = rem < kBT ? rem : kBT;
-}
+  // task `local` of expert e's tiles of one kind: weight tile outer, pool block inner
+  __device__ __forceinline__ void fill(Task& t, int type, int e, int local) const {
+    const int nb = blk[e + 1] - blk[e];
+    t.type = type;
+    t.e = e;
+    t.n = local / nb;
+    const int bl = local - t.n * nb;
+    t.b = blk[e] + bl;
+    const int rem = cnt[e] - bl * kBT;
+    t.valid = rem < kBT ? rem : kBT;
+  }
+  __device__ __forceinline__ Task at(int j) const {
+    Task t;
+    if (mode != 3) {
+      const int nbw = mode == 1 ? NB1 : NB2;
+      const int e = largest_leq(blk, E, j, nbw);   // tiles of expert e: [blk[e]*nbw, blk[e+1]*nbw)
+      fill(t, mode, e, j - blk[e] * nbw);
+      return t;
+    }
+    const int u = largest_leq(seg, E + lag, j, 1);
+    const int r = j - seg[u];
+    const int t1 = u < E ? (blk[u + 1] - blk[u]) * NB1 : 0;
+    if (r < t1) fill(t, 1, u, r);
+    else fill(t, 2, u - lag, r - t1);
+    return t;
+  }
+};
 
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: A = e4m3 (0) in
 // bits [9:7], B = e2m1 (5) in [12:10], both K-major, N>>3 in [22:17], UE8M0
@@ -122,14 +178,13 @@ __device__ __forceinline__ uint32_t make_idesc(int sf_id) {
          (static_cast<uint32_t>(sf_id) << 29) | (static_cast<uint32_t>(sf_id) << 4);
 }
 
-template <int PHASE>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_mx_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ TokenMaps tmT, const Args args) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ Maps maps, const Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int E = args.E;
   int* s_blk = reinterpret_cast<int*>(smem + SmemLayout::meta);
   int* s_cnt = s_blk + E + 1;
+  int* s_seg = s_cnt + E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars_after_meta(E));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
@@ -141,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Status st{args.status, args.timeout_ns};
+  const int lag = args.mode == 3 ? args.lag : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -153,10 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp < kProducers && lane == 0) {
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmT.b32);
-    prefetch_tmap(&tmT.b64);
-    prefetch_tmap(&tmT.b128);
+    prefetch_tmap(&maps.w1);
+    prefetch_tmap(&maps.w2);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(s_tmem, kTmemCols);
@@ -164,13 +218,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   for (int i = threadIdx.x; i <= E; i += kThreads) s_blk[i] = args.blk_off[i];
   for (int i = threadIdx.x; i < E; i += kThreads) s_cnt[i] = args.cnt[i];
+  __syncthreads();
+  if (args.mode == 3 && warp == 0) {
+    // segment offsets: segment u = expert u's L1 tiles + expert (u - lag)'s L2 tiles
+    int run = 0;
+    for (int base = 0; base < E + lag; base += 32) {
+      const int u = base + lane;
+      int v = 0;
+      if (u < E + lag) {
+        if (u < E) v += (s_blk[u + 1] - s_blk[u]) * args.NB1;
+        if (u >= lag && u - lag < E) v += (s_blk[u - lag + 1] - s_blk[u - lag]) * args.NB2;
+      }
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int nv = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nv;
+      }
+      if (u < E + lag) s_seg[u] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_seg[E + lag] = run;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  const int total = s_blk[E] * args.nblocks;
-  const int KB = args.kblocks;
+  const int nblk = s_blk[E];
+  Sched sch{s_blk, s_cnt, s_seg, E, args.NB1, args.NB2, args.mode, lag, 0};
+  sch.total = args.mode == 1 ? nblk * args.NB1
+                             : (args.mode == 2 ? nblk * args.NB2 : nblk * (args.NB1 + args.NB2));
 
   if (warp < kProducers) {
     // ------------------------------------------------------------------ TMA producers
@@ -184,15 +262,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* sw = smem + SmemLayout::sfw + p * 2 * kSFChunk;
       uint64_t w_empty = 0;
       int step = 0;                             // global k-block step of this CTA
-      for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
-        int e, n, b, valid;
-        decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
-        const CUtensorMap* tt = valid <= 32 ? &tmT.b32 : (valid <= 64 ? &tmT.b64 : &tmT.b128);
-        const int rows = valid <= 32 ? 32 : (valid <= 64 ? 64 : 128);
+      for (int j = blockIdx.x; j < sch.total && !*s_abort; j += gridDim.x) {
+        const Task t = sch.at(j);
+        const bool l1 = t.type == 1;
+        const int KB = l1 ? args.KB1 : args.KB2;
+        int kb = ((p - step) % kStages + kStages) % kStages;   // first k-block of this task on stage p
+        if (kb < KB && args.mode == 3) {
+          // the block's rows must be in the pool before they are loaded
+          const bool ok = l1 ? wait_counter_geq(args.ctr_gather + t.b, t.valid, st, s_abort, kSiteGathered)
+                             : wait_counter_geq(args.ctr_l1 + t.b, args.NB1 * kEpiWarps, st, s_abort, kSiteL1Done);
+          if (!ok) break;
+          fence_proxy_async_global();
+        }
+        const CUtensorMap* tt = t.valid <= 32 ? (l1 ? &maps.x32 : &maps.a32)
+                                              : (t.valid <= 64 ? (l1 ? &maps.x64 : &maps.a64)
+                                                               : (l1 ? &maps.x128 : &maps.a128));
+        const int rows = t.valid <= 32 ? 32 : (t.valid <= 64 ? 64 : 128);
         const uint32_t bytes = rows * kBK + kWgtTxBytes + 3 * kSFChunk;
-        const uint8_t* sfw = args.sfw + (static_cast<size_t>(e) * args.nblocks + n) * KB * 2 * kSFChunk;
-        const uint8_t* sft = args.sft + static_cast<size_t>(b) * KB * kSFChunk;
-        int kb = ((p - step) % kStages + kStages) % kStages;   // first k-block of this tile on stage p
+        const uint8_t* sfw = (l1 ? args.sfw1 : args.sfw2) +
+                             (static_cast<size_t>(t.e) * (l1 ? args.NB1 : args.NB2) + t.n) * KB * 2 * kSFChunk;
+        const uint8_t* sft = (l1 ? args.pool_x_sf : args.pool2_sf) + static_cast<size_t>(t.b) * KB * kSFChunk;
         for (; kb < KB; kb += kStages) {
           const uint32_t phase = ((step + kb) / kStages) & 1;
           const uint64_t t0 = args.prof ? globaltimer() : 0;
@@ -200,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (args.prof) w_empty += globaltimer() - t0;
           mbar_arrive_expect_tx(&full[p], bytes);
           const int kc = kb * kBK;
-          tma_load_2d(tk, tt, &full[p], kc, b * kBT, pol_t);
-          if (PHASE == 1) tma_load_3d(wg, &tmW, &full[p], kc, e * 2 * args.I + n * 128, 0, pol_w);
-          else tma_load_2d(wg, &tmW, &full[p], kc, e * args.H + n * kBN, pol_w);
+          tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
+          if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pol_w);
+          else tma_load_2d(wg, &maps.w2, &full[p], kc, t.e * args.H + t.n * kBN, pol_w);
           bulk_load(st_, sft + static_cast<size_t>(kb) * kSFChunk, kSFChunk, &full[p]);
           bulk_load(sw, sfw + static_cast<size_t>(kb) * 2 * kSFChunk, 2 * kSFChunk, &full[p]);
         }
@@ -218,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       uint64_t w_full = 0, w_tempty = 0;
       const uint64_t t_start = globaltimer();
-      for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x, ++it) {
+      for (int j = blockIdx.x; j < sch.total && !*s_abort; j += gridDim.x, ++it) {
+        const Task t = sch.at(j);
+        const int KB = t.type == 1 ? args.KB1 : args.KB2;
         const uint64_t t0 = args.prof ? globaltimer() : 0;
         if (!mbar_wait(tempty, (it & 1) ^ 1, st, s_abort, kSiteTmemEmpty)) break;
         if (args.prof) w_tempty += globaltimer() - t0;
@@ -258,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------------ epilogue (8 warps)
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
     const int half = (warp - kEpiWarp0) >> 2;   // which half of the columns
@@ -266,20 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tlane = tmem + (static_cast<uint32_t>(q * 32) << 16);
     int it = 0;
     uint64_t w_tfull = 0, busy = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      int e, n, b, valid;
-      decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
-      const bool live = m < valid;
-      const size_t row = static_cast<size_t>(b) * kBT + m;
+    for (int j = blockIdx.x; j < sch.total; j += gridDim.x, ++it) {
+      const Task t = sch.at(j);
+      const bool live = m < t.valid;
+      const size_t row = static_cast<size_t>(t.b) * kBT + m;
       const int s = live ? __ldg(args.src + row) : 0;
-      const float w = (PHASE == 1 && live) ? __ldg(args.topk_w + s) : 0.f;   // loaded before the wait
+      const float w = (t.type == 1 && live) ? __ldg(args.topk_w + s) : 0.f;   // loaded before the wait
       const uint64_t t0 = args.prof ? globaltimer() : 0;
       if (!mbar_wait(tfull, it & 1, st, s_abort, kSiteTmemFull)) break;
       const uint64_t t1 = args.prof ? globaltimer() : 0;
       tc_fence_after();
-      if (PHASE == 1) {
-        uint8_t* crow = args.out_codes + row * args.I + n * 128;
-        uint8_t* sfrow = args.out_sf + (static_cast<size_t>(b) * (args.I / 128) + n) * kSFChunk +
+      if (t.type == 1) {
+        uint8_t* crow = args.pool2 + row * args.I + t.n * 128;
+        uint8_t* sfrow = args.pool2_sf + (static_cast<size_t>(t.b) * (args.I / 128) + t.n) * kSFChunk +
                          (m & 31) * 16 + (m >> 5) * 4;
 #pragma unroll 1
         for (int c = 2 * half; c < 2 * half + 2; ++c) {
@@ -291,19 +381,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (args.dbg) {
               float* drow = args.dbg + row * 2 * args.I;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                drow[n * 128 + c * 32 + j] = __uint_as_float(g[j]);
-                drow[args.I + n * 128 + c * 32 + j] = __uint_as_float(u[j]);
+              for (int jj = 0; jj < 32; ++jj) {
+                drow[t.n * 128 + c * 32 + jj] = __uint_as_float(g[jj]);
+                drow[args.I + t.n * 128 + c * 32 + jj] = __uint_as_float(u[jj]);
               }
             }
             float a[32];
             float amax = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float gv = __uint_as_float(g[j]);
+            for (int jj = 0; jj < 32; ++jj) {
+              const float gv = __uint_as_float(g[jj]);
               const float sv = gv * __frcp_rn(1.0f + __expf(-gv));   // silu(g) = g * sigmoid(g)
-              a[j] = sv * __uint_as_float(u[j]) * w;
-              amax = fmaxf(amax, fabsf(a[j]));
+              a[jj] = sv * __uint_as_float(u[jj]) * w;
+              amax = fmaxf(amax, fabsf(a[jj]));
             }
             // UE8M0: smallest e with 448 * 2^e >= max(amax, 1e-10)
             const uint32_t bits = __float_as_uint(fmaxf(amax, 1e-10f));
@@ -325,10 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        const int t = s / args.K;
-        const int k = s - t * args.K;
-        float* prow = args.partials + (static_cast<size_t>(k) * args.T + t) * args.H + n * kBN;
-        const int cols = args.H - n * kBN < kBN ? args.H - n * kBN : kBN;
+        const int tt = s / args.K;
+        const int k = s - tt * args.K;
+        float* prow = args.partials + (static_cast<size_t>(k) * args.T + tt) * args.H + t.n * kBN;
+        const int cols = args.H - t.n * kBN < kBN ? args.H - t.n * kBN : kBN;
 #pragma unroll 1
         for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
           uint32_t v[32];
@@ -344,13 +434,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
+      if (t.type == 1 && args.mode == 3) fence_proxy_async_global();   // codes are read by TMA later
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) {
+        mbar_arrive(tempty);
+        if (t.type == 1 && args.mode == 3) red_release_gpu_add(args.ctr_l1 + t.b, 1);
+      }
       if (args.prof) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
     }
     if (args.prof && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
       args.prof[blockIdx.x * 8 + 6] = busy;
+    }
+  } else if (args.mode == 3) {
+    // ------------------------------------------------------------------ gather warps
+    // This CTA gathers pool blocks b = blockIdx.x, + gridDim.x, ... in order;
+    // each warp copies every other row and publishes its row count.
+    const int gw = warp - kGatherWarp0;
+    const int KBx = args.H / 128;
+    for (int b = blockIdx.x; b < nblk && !*s_abort; b += gridDim.x) {
+      const int e = sch.largest_leq(s_blk, E, b, 1);
+      const int rem = s_cnt[e] - (b - s_blk[e]) * kBT;
+      const int valid = rem < kBT ? rem : kBT;
+      int done = 0;
+      for (int r = gw; r < valid; r += kGatherWarps) {
+        const size_t row = static_cast<size_t>(b) * kBT + r;
+        const int64_t tok = __ldg(args.src + row) / args.K;
+        const uint4* srow = reinterpret_cast<const uint4*>(args.x + tok * args.H);
+        uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
+        for (int i = lane; i < args.H / 16; i += 32) drow[i] = __ldg(srow + i);
+        const uint32_t* ssf = reinterpret_cast<const uint32_t*>(args.x_sf + tok * (args.H / 32));
+        for (int kb = lane; kb < KBx; kb += 32)
+          *reinterpret_cast<uint32_t*>(args.pool_x_sf + (static_cast<size_t>(b) * KBx + kb) * kSFChunk +
+                                       (r & 31) * 16 + (r >> 5) * 4) = __ldg(ssf + kb);
+        ++done;
+      }
+      fence_proxy_async_global();
+      __syncwarp();
+      if (lane == 0 && done) red_release_gpu_add(args.ctr_gather + b, done);
     }
   }
 
@@ -366,69 +487,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int PHASE>
-cudaError_t launch_impl(const GemmLaunch& g, cudaStream_t s) {
+}  // namespace
+
+int mx_lag_auto(int E) {
+  // PR #440 picks lag = clamp(round(0.45 x units), 8, 64) with units of up to
+  // 8 pool blocks; here a unit is a whole expert, so a quarter of that rule.
+  int lag = (E * 45 + 200) / 400;
+  if (lag < 8) lag = 8;
+  if (lag > kMaxLag) lag = kMaxLag;
+  return lag;
+}
+
+cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, cudaStream_t s) {
   const Layout& L = *g.L;
   const WsPtrs& W = *g.W;
-  CUtensorMap tmW;
-  TokenMaps tmT;
+  Maps maps;
   Args a{};
   a.T = L.T; a.H = L.H; a.I = L.I; a.E = L.E; a.K = L.K;
+  a.KB1 = L.H / 128; a.KB2 = L.I / 128; a.NB1 = L.I / 128; a.NB2 = (L.H + kBN - 1) / kBN;
+  a.mode = mode;
+  a.lag = lag < 0 ? 0 : (lag > kMaxLag ? kMaxLag : lag);
   a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;
-  a.sfw = g.wsfp; a.status = W.status; a.timeout_ns = g.timeout_ns;
-  a.dbg = PHASE == 1 ? g.dbg : nullptr;
-  a.prof = g.prof ? g.prof + (PHASE - 1) * 8 * 1024 : nullptr;
-  const uint8_t* pool;
-  int kdim;
-  if (PHASE == 1) {
-    a.kblocks = L.H / 128;
-    a.nblocks = L.I / 128;
-    a.sft = W.pool_x_sf;
-    a.out_codes = W.pool2;
-    a.out_sf = W.pool2_sf;
+  a.x = g.x; a.x_sf = static_cast<const uint8_t*>(g.x_sf);
+  a.pool_x = W.pool_x; a.pool_x_sf = W.pool_x_sf;
+  a.sfw1 = g.w1sfp; a.sfw2 = g.w2sfp;
+  a.pool2 = W.pool2; a.pool2_sf = W.pool2_sf;
+  a.partials = W.part; a.dbg = g.dbg;
+  a.ctr_gather = W.ctr; a.ctr_l1 = W.ctr + L.nblk_cap;
+  a.status = W.status; a.timeout_ns = g.timeout_ns;
+  a.prof = g.prof ? g.prof + (mode == 2 ? 8 * 1024 : 0) : nullptr;
+  {
     // W1 as (k, row, half): half 1 is I rows below half 0, so one box of
     // {128 k, 128 rows, 2 halves} is 128 gate rows followed by the matching 128 up rows
     const uint64_t dims[3] = {static_cast<uint64_t>(L.H), static_cast<uint64_t>(L.E) * 2 * L.I - L.I, 2};
     const uint64_t strides[2] = {static_cast<uint64_t>(L.H) / 2, static_cast<uint64_t>(L.I) * L.H / 2};
     const uint32_t box[3] = {128, 128, 2};
-    if (encode_tmap(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, g.w, dims, strides, box,
+    if (encode_tmap(&maps.w1, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, g.w1, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    pool = W.pool_x;
-    kdim = L.H;
-  } else {
-    a.kblocks = L.I / 128;
-    a.nblocks = (L.H + kBN - 1) / kBN;
-    a.sft = W.pool2_sf;
-    a.partials = W.part;
-    if (encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w, L.I, static_cast<uint64_t>(L.E) * L.H,
-                       L.I / 2, 128, kBN, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-    pool = W.pool2;
-    kdim = L.I;
   }
-  CUtensorMap* maps[3] = {&tmT.b32, &tmT.b64, &tmT.b128};
-  for (int i = 0; i < 3; ++i)
-    if (encode_tmap_2d(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, pool, kdim, L.P, kdim, 128, 32u << i,
+  if (encode_tmap_2d(&maps.w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w2, L.I, static_cast<uint64_t>(L.E) * L.H,
+                     L.I / 2, 128, kBN, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  CUtensorMap* xm[3] = {&maps.x32, &maps.x64, &maps.x128};
+  CUtensorMap* am[3] = {&maps.a32, &maps.a64, &maps.a128};
+  for (int i = 0; i < 3; ++i) {
+    if (encode_tmap_2d(xm[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, W.pool_x, L.H, L.P, L.H, 128, 32u << i,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  const int smem = SmemLayout::total(L.E) + 1024;
-  static int configured[2] = {-1, -1};
+    if (encode_tmap_2d(am[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, W.pool2, L.I, L.P, L.I, 128, 32u << i,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static int configured = -1;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured[PHASE - 1] != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SmemLayout::total(kMaxE) + 1024);
     if (e != cudaSuccess) return e;
-    configured[PHASE - 1] = dev;
+    configured = dev;
   }
-  gemm_mx_kernel<PHASE><<<g.grid, kThreads, smem, s>>>(tmW, tmT, a);
-  return cudaGetLastError();
+  if (mode != 3) {
+    gemm_mx_kernel<<<g.grid, kThreads, SmemLayout::total(L.E) + 1024, s>>>(maps, a);
+    return cudaGetLastError();
+  }
+  // the fused stream waits across CTAs: launch cooperatively so that every CTA is resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SmemLayout::total(L.E) + 1024;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_mx_kernel, maps, a);
 }
-
-}  // namespace
-
-cudaError_t launch_gemm_mx_l1(const GemmLaunch& g, cudaStream_t s) { return launch_impl<1>(g, s); }
-cudaError_t launch_gemm_mx_l2(const GemmLaunch& g, cudaStream_t s) { return launch_impl<2>(g, s); }
 
 }  // namespace mm

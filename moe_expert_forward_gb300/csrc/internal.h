@@ -21,7 +21,7 @@ struct Layout {
   int64_t P;                 // pool row capacity (multiple of BT)
   int64_t nblk_cap;          // P / BT
   int KB1, KB2;              // H/128, I/128
-  size_t status, cnt, blk_off, dscr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
+  size_t status, cnt, blk_off, dscr, ctr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
 };
 
 Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0);
@@ -32,6 +32,7 @@ struct WsPtrs {
   int* cnt;
   int* blk_off;
   int* dscr;
+  int* ctr;                  // [2][nblk_cap] per-block arrival counters of the fused stream
   int* slot;
   int* src;
   uint8_t* pool_x;
@@ -68,14 +69,22 @@ cudaError_t launch_read_intermediate(const Layout& L, const WsPtrs& W, int64_t r
 struct GemmLaunch {
   const Layout* L;
   const WsPtrs* W;
-  const uint8_t* w;          // weights (w1 or w2)
-  const uint8_t* wsfp;       // prepared weight scales
+  const uint8_t* w1;         // e2m1 weights and their prepared scale chunks
+  const uint8_t* w1sfp;
+  const uint8_t* w2;
+  const uint8_t* w2sfp;
+  const uint8_t* x;          // activations and scales (in-kernel gather of the fused stream)
+  const void* x_sf;
   const float* topk_w;
   float* dbg;               // L1 raw accumulators (debug_flags bit 0) or null
   unsigned long long* prof; // per-CTA role timings (debug_flags bit 1) or null
   uint64_t timeout_ns;
   int grid;
 };
+// mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
+cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, cudaStream_t s);
+int mx_lag_auto(int E);
+
 struct GemmLaunchF8 {
   const Layout* L;
   const WsPtrs* W;
@@ -87,8 +96,6 @@ struct GemmLaunchF8 {
 };
 cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s);
 cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s);
-cudaError_t launch_gemm_mx_l1(const GemmLaunch& g, cudaStream_t s);
-cudaError_t launch_gemm_mx_l2(const GemmLaunch& g, cudaStream_t s);
 
 // TMA descriptor creation through the driver entry point.
 CUresult encode_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,

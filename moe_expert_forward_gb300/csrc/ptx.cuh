@@ -88,6 +88,45 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// ------------------------------------------------------------------ cross-CTA counters
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Order this thread's generic-proxy global writes before later async-proxy
+// (TMA) accesses, and the other way round.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until *p >= target (acquire).  Returns false after recording
+// MM_MOE_ERR_TIMEOUT at site `where`, or when `abort` is raised.
+__device__ __forceinline__ bool wait_counter_geq(const int* p, int target, const Status& st, volatile int* abort,
+                                                 int where) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+      if (ld_acquire_gpu(p) >= target) return true;
+      __nanosleep(100);
+    }
+    if (*abort) return false;
+    if (globaltimer() - t0 > st.timeout_ns) {
+      if (atomicCAS(st.word, 0, 4 /*MM_MOE_ERR_TIMEOUT*/) == 0) {
+        st.word[1] = where;
+        st.word[2] = ld_acquire_gpu(p);
+        st.word[3] = target;
+      }
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -112,3 +112,32 @@ def test_forward_l1_accumulators_match_oracle(M):
             got = dbg[slot[t, k]]
             errs.append(np.max(np.abs(got - ref)) / (np.max(np.abs(ref)) + 1e-30))
     assert max(errs) < 1e-5, max(errs)
+
+
+@pytest.mark.parametrize("lag", [0, 1, 3, 64, -1])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "manyexp", "k1"])
+def test_fused_stream_bitwise_equals_two_launch_path(M, name, lag):
+    """The lag-ordered single-launch stream computes every tile exactly as the
+    two-launch path does, whatever the lag: outputs and intermediates are equal bit for bit."""
+    cfg = SMALL[name]
+    dev = to_dev(W.make_inputs(cfg, "cpu"))
+    out_a, ws_a, prep, st_a = run_forward(M, cfg, dev, M.options(fused=0))
+    out_a = out_a.clone()
+    out_b, ws_b, _, st_b = run_forward(M, cfg, dev, M.options(fused=1, lag_units=lag), prepared=prep)
+    assert st_a[0] == 0 and st_b[0] == 0, (st_a, st_b)
+    assert torch.equal(out_a, out_b)
+    opt = M.options()
+    pa = M.workspace_view(ws_a, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "pool2")
+    pb = M.workspace_view(ws_b, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "pool2")
+    _, blk, _, src, _ = read_routing(M, cfg, ws_a, opt)
+    live = torch.from_numpy(src[:blk[-1] * 128] >= 0)
+    rows = pa.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()]
+    assert torch.equal(rows, pb.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()])
+
+
+def test_fused_stream_parity_and_masking(M):
+    cfg = SMALL["ragged"].with_(seed=61)
+    inp = W.make_inputs(cfg, "cpu")
+    g = torch.Generator().manual_seed(7)
+    inp["topk_idx"][torch.rand(cfg.T, cfg.K, generator=g) < 0.15] = -1
+    _full_check(M, cfg, inp, M.options(fused=1))

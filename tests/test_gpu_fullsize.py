@@ -25,13 +25,13 @@ def M():
     return M
 
 
-@pytest.mark.parametrize("name", ["flash", "decode", "pro", "f8"])
-def test_fullsize_sampled_rows(M, name):
+@pytest.mark.parametrize("name,fused", [("flash", 0), ("flash", 1), ("decode", 1), ("pro", 1), ("pro", 0), ("f8", 0)])
+def test_fullsize_sampled_rows(M, name, fused):
     cfg = W.CONFIGS[name]
     dev = W.make_inputs(cfg, "cuda")
-    out, ws, prepared, (code, where) = run_forward(M, cfg, dev)
+    opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8, fused=fused)
+    out, ws, prepared, (code, where) = run_forward(M, cfg, dev, opt)
     assert code == 0, f"device status {code} at site {where}"
-    opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
     cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt)
     ref_route = O.route(dev["topk_idx"].cpu().numpy(), cfg.E, bm)
     assert np.array_equal(cnt, ref_route["cnt"]) and np.array_equal(blk, ref_route["blk_off"])
