@@ -94,7 +94,10 @@ typedef struct mm_moe_options {
                                    to the DEBUG workspace region ([P, 2I], pool-row order) and the
                                    call stops after L1; bit 1: the GEMM kernels record per-CTA
                                    wait/busy times of their roles into the PROF workspace region;
-                                   0 for normal use */
+                                   bit 2: in the fused stream every L2 tile waits for one more L1
+                                   completion than will ever arrive, so the call ends with
+                                   MM_MOE_ERR_TIMEOUT after wait_timeout_ms (tests the device-side
+                                   timeout path); 0 for normal use */
   int reserved[7];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between

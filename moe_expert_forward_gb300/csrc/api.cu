@@ -294,13 +294,13 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       if (e == cudaSuccess) e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * 2 * static_cast<size_t>(L.nblk_cap), s);
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
-      if (e == cudaSuccess) e = launch_gemm_mx(g, 3, lag, s);
+      if (e == cudaSuccess) e = launch_gemm_mx(g, 3, lag, (o.debug_flags & 4) ? 1 : 0, s);
       if (e == cudaSuccess) e = mark(3);
     } else {
-      if (e == cudaSuccess) e = launch_gemm_mx(g, 1, 0, s);
+      if (e == cudaSuccess) e = launch_gemm_mx(g, 1, 0, 0, s);
       if (e == cudaSuccess) e = mark(3);
       if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
-      if (e == cudaSuccess) e = launch_gemm_mx(g, 2, 0, s);
+      if (e == cudaSuccess) e = launch_gemm_mx(g, 2, 0, 0, s);
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,

@@ -79,6 +79,7 @@ struct Args {
   int KB1, KB2, NB1, NB2;
   int mode;            // 1, 2 or 3 (see above)
   int lag;             // mode 3: experts by which L2 trails L1
+  int l1_extra;        // mode 3: extra L1 completions an L2 tile waits for (0; 1 = a wait that cannot end)
   const int* cnt;
   const int* blk_off;
   const int* src;
@@ -270,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         if (kb < KB && args.mode == 3) {
           // the block's rows must be in the pool before they are loaded
           const bool ok = l1 ? wait_counter_geq(args.ctr_gather + t.b, t.valid, st, s_abort, kSiteGathered)
-                             : wait_counter_geq(args.ctr_l1 + t.b, args.NB1 * kEpiWarps, st, s_abort, kSiteL1Done);
+                             : wait_counter_geq(args.ctr_l1 + t.b, args.NB1 * kEpiWarps + args.l1_extra, st, s_abort,
+                                              kSiteL1Done);
           if (!ok) break;
           fence_proxy_async_global();
         }
@@ -498,7 +500,7 @@ int mx_lag_auto(int E) {
   return lag;
 }
 
-cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, cudaStream_t s) {
+cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s) {
   const Layout& L = *g.L;
   const WsPtrs& W = *g.W;
   Maps maps;
@@ -507,6 +509,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, cudaStream_t 
   a.KB1 = L.H / 128; a.KB2 = L.I / 128; a.NB1 = L.I / 128; a.NB2 = (L.H + kBN - 1) / kBN;
   a.mode = mode;
   a.lag = lag < 0 ? 0 : (lag > kMaxLag ? kMaxLag : lag);
+  a.l1_extra = l1_extra;
   a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;
   a.x = g.x; a.x_sf = static_cast<const uint8_t*>(g.x_sf);
   a.pool_x = W.pool_x; a.pool_x_sf = W.pool_x_sf;

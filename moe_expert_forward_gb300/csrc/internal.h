@@ -82,7 +82,7 @@ struct GemmLaunch {
   int grid;
 };
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
-cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, cudaStream_t s);
+cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
 int mx_lag_auto(int E);
 
 struct GemmLaunchF8 {
