@@ -26,7 +26,7 @@
 //      SM, grid <= #SMs) and works its tasks in that order, so the stream
 //      cannot deadlock.
 //
-// Warps (480 threads, one CTA per SM):
+// Warps (512 threads in four warpgroups, one CTA per SM):
 //   0..3    TMA producers, warp p owns pipeline stage p.  A TMA-issuing thread
 //           keeps only about four bulk-tensor copies in flight (measured on
 //           GB300), so each stage has its own issuer.  Per stage: one token
@@ -35,10 +35,15 @@
 //           memory; L1 fetches gate and up rows with one 3-D copy) and the
 //           scale chunks.
 //   4..11   epilogue: one token row per thread, the two warps of a TMEM lane
-//           quadrant split the columns.
+//           quadrant split the columns.  Each thread copies its 128
+//           accumulator columns into registers and releases TMEM at once, so
+//           the next tile's MMAs overlap the SwiGLU / requant / stores.
+//           setmaxnreg gives these two warpgroups 176 registers a thread and
+//           the other two 80; the host refuses to launch unless the kernel
+//           starts with exactly the 128 registers a thread the split assumes.
 //   12      TMEM allocator + single-thread MMA issuer (tcgen05.cp of the scales
 //           into TMEM, 4 MMAs of K=32 per stage).
-//   13..14  gather warps (mode 3).
+//   13..14  gather warps (mode 3); warp 15 idles.
 // Every wait is bounded: on a deadline the kernel records MM_MOE_ERR_TIMEOUT
 // and a site code and returns.
 #include <cuda.h>
@@ -56,7 +61,12 @@ constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = kEpiWarp0 + kEpiWarps;
 constexpr int kGatherWarp0 = kMmaWarp + 1;
 constexpr int kGatherWarps = 2;
-constexpr int kThreads = (kGatherWarp0 + kGatherWarps) * 32;
+constexpr int kThreads = 512;          // four warpgroups; warp 15 idles
+static_assert((kGatherWarp0 + kGatherWarps) * 32 <= kThreads, "warp roles");
+constexpr int kLaunchRegs = 128;       // 65536 / 512
+constexpr int kSmallRegs = 80;         // WG0 (producers), WG3 (MMA, gather)
+constexpr int kEpiRegs = 176;          // WG1, WG2 (epilogue)
+static_assert(2 * 128 * kSmallRegs + 2 * 128 * kEpiRegs == kThreads * kLaunchRegs, "register split");
 constexpr int kBN = 256;               // weight rows per tile (MMA N)
 constexpr int kTokBytes = kBT * kBK;   // 128 token rows x 128 K
 constexpr int kWgtBytes = kBN * kBK;   // 256 weight rows x 128 K, 1 byte per element in smem
@@ -179,6 +189,79 @@ __device__ __forceinline__ uint32_t make_idesc(int sf_id) {
          (static_cast<uint32_t>(sf_id) << 29) | (static_cast<uint32_t>(sf_id) << 4);
 }
 
+// SwiGLU x top-k weight and UE8M0 requant of one 32-column block c of an L1
+// tile for one token row: gate g, up u (fp32 bits, overwritten).
+__device__ __forceinline__ void l1_block(uint32_t (&g)[32], const uint32_t (&u)[32], int c, bool live, float w,
+                                         size_t row, int n, const Args& args, uint8_t* crow, uint8_t* sfrow) {
+  if (!live) return;
+  if (args.dbg) {
+    float* drow = args.dbg + row * 2 * args.I;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      drow[n * 128 + c * 32 + jj] = __uint_as_float(g[jj]);
+      drow[args.I + n * 128 + c * 32 + jj] = __uint_as_float(u[jj]);
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) {
+    const float gv = __uint_as_float(g[jj]);
+    const float sv = gv * __frcp_rn(1.0f + __expf(-gv));   // silu(g) = g * sigmoid(g)
+    const float av = sv * __uint_as_float(u[jj]) * w;
+    g[jj] = __float_as_uint(av);
+    amax = fmaxf(amax, fabsf(av));
+  }
+  // UE8M0: smallest e with 448 * 2^e >= max(amax, 1e-10)
+  const uint32_t bits = __float_as_uint(fmaxf(amax, 1e-10f));
+  const int ex = static_cast<int>((bits >> 23) & 0xFF) - 126;
+  int ee = ex - 9 + ((bits & 0x7FFFFF) > 0x600000 ? 1 : 0);
+  ee = ee < -127 ? -127 : (ee > 126 ? 126 : ee);
+  const float scale = __uint_as_float(static_cast<uint32_t>(127 - ee) << 23);
+  uint32_t packed[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t lo = cvt_e4m3x2(__uint_as_float(g[4 * i]) * scale, __uint_as_float(g[4 * i + 1]) * scale);
+    const uint32_t hi = cvt_e4m3x2(__uint_as_float(g[4 * i + 2]) * scale, __uint_as_float(g[4 * i + 3]) * scale);
+    packed[i] = lo | (hi << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(crow + c * 32);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  sfrow[c] = static_cast<uint8_t>(ee + 127);
+}
+
+// Gather warps of the fused stream: this CTA gathers pool blocks b =
+// blockIdx.x, + gridDim.x, ... in order; each warp copies every other row of a
+// block (codes and UE8M0 scales) and publishes its row count (release).
+__device__ __forceinline__ void gather_rows(const Args& args, const int* s_blk, const int* s_cnt, const Sched& sch,
+                                            volatile int* s_abort, int gw, int lane, int nblk) {
+  const int KBx = args.H / 128;
+  for (int b = blockIdx.x; b < nblk && !*s_abort; b += gridDim.x) {
+    const int e = sch.largest_leq(s_blk, args.E, b, 1);
+    const int rem = s_cnt[e] - (b - s_blk[e]) * kBT;
+    const int valid = rem < kBT ? rem : kBT;
+    int done = 0;
+    for (int r = gw; r < valid; r += kGatherWarps) {
+      const size_t row = static_cast<size_t>(b) * kBT + r;
+      const int64_t tok = __ldg(args.src + row) / args.K;
+      const uint4* srow = reinterpret_cast<const uint4*>(args.x + tok * args.H);
+      uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
+      for (int i = lane; i < args.H / 16; i += 32) drow[i] = __ldg(srow + i);
+      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(args.x_sf + tok * (args.H / 32));
+      for (int kb = lane; kb < KBx; kb += 32)
+        *reinterpret_cast<uint32_t*>(args.pool_x_sf + (static_cast<size_t>(b) * KBx + kb) * kSFChunk +
+                                     (r & 31) * 16 + (r >> 5) * 4) = __ldg(ssf + kb);
+      ++done;
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0 && done) red_release_gpu_add(args.ctr_gather + b, done);
+  }
+}
+
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ Maps maps, const Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -251,7 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   sch.total = args.mode == 1 ? nblk * args.NB1
                              : (args.mode == 2 ? nblk * args.NB2 : nblk * (args.NB1 + args.NB2));
 
-  if (warp < kProducers) {
+  const int wg = warp >> 2;
+  // setmaxnreg sits inside each warpgroup's branch: after a join ptxas would
+  // have to compile the code below for the smaller budget
+  if (wg == 0) {
+    regs_dec();
     // ------------------------------------------------------------------ TMA producers
     if (lane == 0) {
       const int p = warp;                       // this warp fills stage p, phases 0,1,0,...
@@ -301,7 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       }
       if (args.prof) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
     }
-  } else if (warp == kMmaWarp) {
+  } else if (wg == 3) {
+    regs_dec();
+    if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0;
@@ -351,7 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       }
     }
     __syncwarp();
-  } else if (warp < kMmaWarp) {
+    } else if (warp < kGatherWarp0 + kGatherWarps && args.mode == 3) {
+      gather_rows(args, s_blk, s_cnt, sch, s_abort, warp - kGatherWarp0, lane, nblk);
+    }
+  } else {
+    regs_inc();
     // ------------------------------------------------------------------ epilogue (8 warps)
     const int q = warp & 3;                // TMEM lane quadrant this warp may access
     const int half = (warp - kEpiWarp0) >> 2;   // which half of the columns
@@ -369,111 +462,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       if (!mbar_wait(tfull, it & 1, st, s_abort, kSiteTmemFull)) break;
       const uint64_t t1 = args.prof ? globaltimer() : 0;
       tc_fence_after();
+      // copy this thread's 128 accumulator columns, then hand TMEM back to the MMA warp
+      // L1: gate [64h, 64h+64) and up [128+64h, 128+64h+64); L2: [128h, 128h+128)
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      {
+        const int c0 = t.type == 1 ? 64 * half : 128 * half;
+        const int c1 = t.type == 1 ? 128 + 64 * half : 128 * half + 64;
+        tmem_ld_32x32b_x32(tlane + c0, r0);
+        tmem_ld_32x32b_x32(tlane + c0 + 32, r1);
+        tmem_ld_32x32b_x32(tlane + c1, r2);
+        tmem_ld_32x32b_x32(tlane + c1 + 32, r3);
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
       if (t.type == 1) {
         uint8_t* crow = args.pool2 + row * args.I + t.n * 128;
         uint8_t* sfrow = args.pool2_sf + (static_cast<size_t>(t.b) * (args.I / 128) + t.n) * kSFChunk +
                          (m & 31) * 16 + (m >> 5) * 4;
-#pragma unroll 1
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(tlane + c * 32, g);
-          tmem_ld_32x32b_x32(tlane + 128 + c * 32, u);
-          tmem_ld_wait();
-          if (live) {
-            if (args.dbg) {
-              float* drow = args.dbg + row * 2 * args.I;
-#pragma unroll
-              for (int jj = 0; jj < 32; ++jj) {
-                drow[t.n * 128 + c * 32 + jj] = __uint_as_float(g[jj]);
-                drow[args.I + t.n * 128 + c * 32 + jj] = __uint_as_float(u[jj]);
-              }
-            }
-            float a[32];
-            float amax = 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const float gv = __uint_as_float(g[jj]);
-              const float sv = gv * __frcp_rn(1.0f + __expf(-gv));   // silu(g) = g * sigmoid(g)
-              a[jj] = sv * __uint_as_float(u[jj]) * w;
-              amax = fmaxf(amax, fabsf(a[jj]));
-            }
-            // UE8M0: smallest e with 448 * 2^e >= max(amax, 1e-10)
-            const uint32_t bits = __float_as_uint(fmaxf(amax, 1e-10f));
-            const int ex = static_cast<int>((bits >> 23) & 0xFF) - 126;
-            int ee = ex - 9 + ((bits & 0x7FFFFF) > 0x600000 ? 1 : 0);
-            ee = ee < -127 ? -127 : (ee > 126 ? 126 : ee);
-            const float scale = __uint_as_float(static_cast<uint32_t>(127 - ee) << 23);
-            uint32_t packed[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t lo = cvt_e4m3x2(a[4 * i] * scale, a[4 * i + 1] * scale);
-              const uint32_t hi = cvt_e4m3x2(a[4 * i + 2] * scale, a[4 * i + 3] * scale);
-              packed[i] = lo | (hi << 16);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(crow + c * 32);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            sfrow[c] = static_cast<uint8_t>(ee + 127);
-          }
+        l1_block(r0, r2, 2 * half, live, w, row, t.n, args, crow, sfrow);
+        l1_block(r1, r3, 2 * half + 1, live, w, row, t.n, args, crow, sfrow);
+        if (args.mode == 3) {
+          fence_proxy_async_global();              // the codes are read by TMA later
+          __syncwarp();
+          if (lane == 0) red_release_gpu_add(args.ctr_l1 + t.b, 1);
         }
       } else {
         const int tt = s / args.K;
         const int k = s - tt * args.K;
-        float* prow = args.partials + (static_cast<size_t>(k) * args.T + tt) * args.H + t.n * kBN;
-        const int cols = args.H - t.n * kBN < kBN ? args.H - t.n * kBN : kBN;
-#pragma unroll 1
-        for (int c = half * (kBN / 64); c < (half + 1) * (kBN / 64); ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tlane + c * 32, v);
-          tmem_ld_wait();
-          if (live && c * 32 < cols) {
-            float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+        const int col0 = t.n * kBN + 128 * half;
+        if (live && col0 < args.H) {
+          float4* dst = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(k) * args.T + tt) * args.H + col0);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          for (int i = 0; i < 8; ++i) {
+            dst[i] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
+                                 __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
+            dst[8 + i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
+                                     __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
+            dst[16 + i] = make_float4(__uint_as_float(r2[4 * i]), __uint_as_float(r2[4 * i + 1]),
+                                      __uint_as_float(r2[4 * i + 2]), __uint_as_float(r2[4 * i + 3]));
+            dst[24 + i] = make_float4(__uint_as_float(r3[4 * i]), __uint_as_float(r3[4 * i + 1]),
+                                      __uint_as_float(r3[4 * i + 2]), __uint_as_float(r3[4 * i + 3]));
           }
         }
-      }
-      tc_fence_before();
-      if (t.type == 1 && args.mode == 3) fence_proxy_async_global();   // codes are read by TMA later
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(tempty);
-        if (t.type == 1 && args.mode == 3) red_release_gpu_add(args.ctr_l1 + t.b, 1);
       }
       if (args.prof) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
     }
     if (args.prof && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
       args.prof[blockIdx.x * 8 + 6] = busy;
-    }
-  } else if (args.mode == 3) {
-    // ------------------------------------------------------------------ gather warps
-    // This CTA gathers pool blocks b = blockIdx.x, + gridDim.x, ... in order;
-    // each warp copies every other row and publishes its row count.
-    const int gw = warp - kGatherWarp0;
-    const int KBx = args.H / 128;
-    for (int b = blockIdx.x; b < nblk && !*s_abort; b += gridDim.x) {
-      const int e = sch.largest_leq(s_blk, E, b, 1);
-      const int rem = s_cnt[e] - (b - s_blk[e]) * kBT;
-      const int valid = rem < kBT ? rem : kBT;
-      int done = 0;
-      for (int r = gw; r < valid; r += kGatherWarps) {
-        const size_t row = static_cast<size_t>(b) * kBT + r;
-        const int64_t tok = __ldg(args.src + row) / args.K;
-        const uint4* srow = reinterpret_cast<const uint4*>(args.x + tok * args.H);
-        uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
-        for (int i = lane; i < args.H / 16; i += 32) drow[i] = __ldg(srow + i);
-        const uint32_t* ssf = reinterpret_cast<const uint32_t*>(args.x_sf + tok * (args.H / 32));
-        for (int kb = lane; kb < KBx; kb += 32)
-          *reinterpret_cast<uint32_t*>(args.pool_x_sf + (static_cast<size_t>(b) * KBx + kb) * kSFChunk +
-                                       (r & 31) * 16 + (r >> 5) * 4) = __ldg(ssf + kb);
-        ++done;
-      }
-      fence_proxy_async_global();
-      __syncwarp();
-      if (lane == 0 && done) red_release_gpu_add(args.ctr_gather + b, done);
     }
   }
 
@@ -546,8 +584,13 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SmemLayout::total(kMaxE) + 1024);
+    // the setmaxnreg split assumes exactly kLaunchRegs registers a thread at launch
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_mx_kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SmemLayout::total(kMaxE) + 1024);
     if (e != cudaSuccess) return e;
     configured = dev;
   }
