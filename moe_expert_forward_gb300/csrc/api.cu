@@ -25,7 +25,7 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.cnt = o; o = align_up(o + sizeof(int) * E, 256);
   L.blk_off = o; o = align_up(o + sizeof(int) * (E + 1), 256);
   L.dscr = o; o = align_up(o + sizeof(int) * static_cast<size_t>(kDispatchMaxCtas) * E, 256);
-  L.ctr = o; o = align_up(o + sizeof(int) * 2 * static_cast<size_t>(L.nblk_cap), 256);
+  L.ctr = o; o = align_up(o + sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), 256);
   L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
   L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
   L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
@@ -290,9 +290,11 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, topk_w, W.dbg, W.prof, timeout_ns, grid};
+    // arrival counters of the fused stream and the tile-group counters of every GEMM launch
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), s);
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
-      if (e == cudaSuccess) e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * 2 * static_cast<size_t>(L.nblk_cap), s);
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
       if (e == cudaSuccess) e = launch_gemm_mx(g, 3, lag, (o.debug_flags & 4) ? 1 : 0, s);
       if (e == cudaSuccess) e = mark(3);

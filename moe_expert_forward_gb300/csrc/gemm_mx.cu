@@ -61,12 +61,16 @@ constexpr int kEpiWarps = 8;
 constexpr int kMmaWarp = kEpiWarp0 + kEpiWarps;
 constexpr int kGatherWarp0 = kMmaWarp + 1;
 constexpr int kGatherWarps = 2;
-constexpr int kThreads = 512;          // four warpgroups; warp 15 idles
-static_assert((kGatherWarp0 + kGatherWarps) * 32 <= kThreads, "warp roles");
+constexpr int kSchedWarp = kGatherWarp0 + kGatherWarps;   // deals tile groups to this CTA's roles
+constexpr int kQueue = 8;                                 // tile groups the scheduler may run ahead
+constexpr int kQueueConsumers = kProducers + 1 + kEpiWarps;   // arrivals that free a queue slot
+constexpr int kThreads = 512;          // four warpgroups
+static_assert((kSchedWarp + 1) * 32 <= kThreads, "warp roles");
 constexpr int kLaunchRegs = 128;       // 65536 / 512
-constexpr int kSmallRegs = 80;         // WG0 (producers), WG3 (MMA, gather)
-constexpr int kEpiRegs = 176;          // WG1, WG2 (epilogue)
-static_assert(2 * 128 * kSmallRegs + 2 * 128 * kEpiRegs == kThreads * kLaunchRegs, "register split");
+constexpr int kSmallRegs = 72;         // WG0 (producers)
+constexpr int kMmaRegs = 104;          // WG3 (MMA issuer with its per-stage descriptors, gather, scheduler)
+constexpr int kEpiRegs = 168;          // WG1, WG2 (epilogue)
+static_assert(128 * kSmallRegs + 128 * kMmaRegs + 2 * 128 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kBN = 256;               // weight rows per tile (MMA N)
 constexpr int kTokBytes = kBT * kBK;   // 128 token rows x 128 K
 constexpr int kWgtBytes = kBN * kBK;   // 256 weight rows x 128 K, 1 byte per element in smem
@@ -81,7 +85,7 @@ constexpr int kSfColsPerStage = 12;    // 4 (tokens) + 8 (weights)
 // wait-site codes reported through the status word
 enum : int {
   kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104,
-  kSiteGathered = 105, kSiteL1Done = 106
+  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueFull = 107, kSiteQueueEmpty = 108
 };
 
 struct Args {
@@ -106,6 +110,7 @@ struct Args {
   float* dbg;                // raw L1 accumulators [P, 2I] or null
   int* ctr_gather;           // mode 3: rows gathered per pool block
   int* ctr_l1;               // mode 3: L1 epilogue warps finished per pool block
+  int* sched;                // tile groups handed out so far (zero at launch)
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;  // per-CTA wait/busy nanoseconds (debug_flags bit 1) or null
@@ -124,10 +129,10 @@ struct SmemLayout {
   static constexpr int wgt = tok + kStages * kTokBytes;
   static constexpr int sft = wgt + kStages * kWgtBytes;
   static constexpr int sfw = sft + kStages * kSFChunk;
-  static constexpr int meta = sfw + kStages * 2 * kSFChunk;   // blk_off[E+1], cnt[E], seg[E+lag+1]
-  static constexpr int meta_ints(int E) { return (E + 1) + E + (E + kMaxLag + 1); }
+  static constexpr int meta = sfw + kStages * 2 * kSFChunk;   // blk_off[E+1], cnt[E], queue[kQueue]
+  static constexpr int meta_ints(int E) { return (E + 1) + E + kQueue; }
   static constexpr int bars_after_meta(int E) { return meta + (meta_ints(E) * 4 + 15) / 16 * 16; }
-  static constexpr int nbars = 2 * kStages + 2;  // full[S], empty[S], tfull, tempty
+  static constexpr int nbars = 2 * kStages + 2 + 2 * kQueue;  // full[S], empty[S], tfull, tempty, qfull, qempty
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -136,13 +141,36 @@ static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "tensor memory b
 struct Task {
   int type;      // 1 = L1, 2 = L2
   int e, n, b, valid;
+  bool last;     // the last pool block of its tile group
+};
+
+// Tasks are dealt to the persistent CTAs in tile groups: one weight tile (e, n)
+// of one GEMM together with every pool block of expert e.  A CTA takes a
+// group's blocks back to back, so the second and later blocks of an expert
+// find the tile's weights still in L2 instead of reading them from HBM again.
+// Group order: modes 1/2, expert-major then tile; mode 3, segment u = expert
+// u's NB1 L1 groups followed by expert (u - lag)'s NB2 L2 groups.  The number
+// of groups per segment does not depend on the routing, so a group index
+// decodes in closed form; groups of experts without tokens are skipped.
+struct Cursor {
+  int i = 0;            // next queue position
+  int bl = 0, nb = 0;   // block within the current group, blocks of its expert
+  Task t;
+};
+
+// Tile groups taken by this CTA, in order: slot i % kQueue holds the i-th
+// (-1 once there are none left).  The scheduler thread fills a slot after
+// every consumer has released it.
+struct Queue {
+  uint64_t* full;       // [kQueue], one arrival: the slot holds a group
+  uint64_t* empty;      // [kQueue], kQueueConsumers arrivals: the slot is free
+  volatile int* g;      // [kQueue]
 };
 
 struct Sched {
   const int* blk;   // [E+1] pool-block offsets per expert
   const int* cnt;   // [E]
-  const int* seg;   // [E+lag+1] mode-3 segment offsets
-  int E, NB1, NB2, mode, lag, total;
+  int E, NB1, NB2, mode, lag;
 
   __device__ __forceinline__ int largest_leq(const int* a, int n, int v, int scale) const {
     int lo = 0, hi = n - 1;                  // largest i < n with a[i] * scale <= v
@@ -152,31 +180,73 @@ struct Sched {
     }
     return lo;
   }
-  // task `local` of expert e's tiles of one kind: weight tile outer, pool block inner
-  __device__ __forceinline__ void fill(Task& t, int type, int e, int local) const {
-    const int nb = blk[e + 1] - blk[e];
-    t.type = type;
-    t.e = e;
-    t.n = local / nb;
-    const int bl = local - t.n * nb;
-    t.b = blk[e] + bl;
-    const int rem = cnt[e] - bl * kBT;
-    t.valid = rem < kBT ? rem : kBT;
+  __device__ __forceinline__ int groups() const {
+    return mode == 1 ? E * NB1 : (mode == 2 ? E * NB2 : E * (NB1 + NB2));
   }
-  __device__ __forceinline__ Task at(int j) const {
-    Task t;
+  // mode 3: groups in the segments before segment u
+  __device__ __forceinline__ int groups_before(int u) const {
+    const int l1 = u < E ? u : E;
+    int l2 = u - lag;
+    l2 = l2 < 0 ? 0 : (l2 > E ? E : l2);
+    return l1 * NB1 + l2 * NB2;
+  }
+  __device__ __forceinline__ void group(int g, Task& t) const {
     if (mode != 3) {
       const int nbw = mode == 1 ? NB1 : NB2;
-      const int e = largest_leq(blk, E, j, nbw);   // tiles of expert e: [blk[e]*nbw, blk[e+1]*nbw)
-      fill(t, mode, e, j - blk[e] * nbw);
-      return t;
+      t.type = mode;
+      t.e = g / nbw;
+      t.n = g - t.e * nbw;
+      return;
     }
-    const int u = largest_leq(seg, E + lag, j, 1);
-    const int r = j - seg[u];
-    const int t1 = u < E ? (blk[u + 1] - blk[u]) * NB1 : 0;
-    if (r < t1) fill(t, 1, u, r);
-    else fill(t, 2, u - lag, r - t1);
-    return t;
+    int lo = 0, hi = E + lag - 1;            // the segment holding group g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (groups_before(mid) <= g) lo = mid; else hi = mid - 1;
+    }
+    const int r = g - groups_before(lo);
+    const int n1 = lo < E ? NB1 : 0;
+    if (r < n1) { t.type = 1; t.e = lo; t.n = r; }
+    else { t.type = 2; t.e = lo - lag; t.n = r - n1; }
+  }
+  __device__ __forceinline__ void block(Cursor& c) const {
+    c.t.b = blk[c.t.e] + c.bl;
+    const int rem = cnt[c.t.e] - c.bl * kBT;
+    c.t.valid = rem < kBT ? rem : kBT;
+    c.t.last = c.bl + 1 == c.nb;
+  }
+  __device__ __forceinline__ int group_blocks(int g) const {
+    Task t;
+    group(g, t);
+    return blk[t.e + 1] - blk[t.e];
+  }
+  // Advance to this CTA's next task; false when there is none (or on abort).
+  // A warp-wide consumer calls this with all 32 lanes converged: lane 0 takes
+  // the queue slot and broadcasts it.
+  __device__ __forceinline__ bool next(Cursor& c, const Queue& q, const Status& st, volatile int* abort,
+                                       bool warp_wide, int lane) const {
+    if (c.bl + 1 < c.nb) {
+      ++c.bl;
+      block(c);
+      return true;
+    }
+    const int slot = c.i % kQueue;
+    const uint32_t parity = (c.i / kQueue) & 1;
+    ++c.i;
+    int g = -1;
+    if (!warp_wide || lane == 0) {
+      if (mbar_wait(&q.full[slot], parity, st, abort, kSiteQueueFull)) {
+        g = q.g[slot];
+        mbar_arrive(&q.empty[slot]);
+      }
+    }
+    if (warp_wide) g = __shfl_sync(0xffffffffu, g, 0);
+    c.nb = 0;
+    if (g < 0) return false;
+    group(g, c.t);
+    c.nb = blk[c.t.e + 1] - blk[c.t.e];
+    c.bl = 0;
+    block(c);
+    return true;
   }
 };
 
@@ -260,6 +330,7 @@ __device__ __forceinline__ void gather_rows(const Args& args, const int* s_blk, 
 }
 
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
+__device__ __forceinline__ void regs_dec_mma() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kMmaRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ Maps maps, const Args args) {
@@ -268,12 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   const int E = args.E;
   int* s_blk = reinterpret_cast<int*>(smem + SmemLayout::meta);
   int* s_cnt = s_blk + E + 1;
-  int* s_seg = s_cnt + E;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars_after_meta(E));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 1;
+  const Queue q{tempty + 1, tempty + 1 + kQueue, s_cnt + E};
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -289,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, kEpiWarps);
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(&q.full[i], 1);
+      mbar_init(&q.empty[i], kQueueConsumers);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -303,36 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   for (int i = threadIdx.x; i <= E; i += kThreads) s_blk[i] = args.blk_off[i];
   for (int i = threadIdx.x; i < E; i += kThreads) s_cnt[i] = args.cnt[i];
   __syncthreads();
-  if (args.mode == 3 && warp == 0) {
-    // segment offsets: segment u = expert u's L1 tiles + expert (u - lag)'s L2 tiles
-    int run = 0;
-    for (int base = 0; base < E + lag; base += 32) {
-      const int u = base + lane;
-      int v = 0;
-      if (u < E + lag) {
-        if (u < E) v += (s_blk[u + 1] - s_blk[u]) * args.NB1;
-        if (u >= lag && u - lag < E) v += (s_blk[u - lag + 1] - s_blk[u - lag]) * args.NB2;
-      }
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int nv = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += nv;
-      }
-      if (u < E + lag) s_seg[u] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_seg[E + lag] = run;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
   const int nblk = s_blk[E];
-  Sched sch{s_blk, s_cnt, s_seg, E, args.NB1, args.NB2, args.mode, lag, 0};
-  sch.total = args.mode == 1 ? nblk * args.NB1
-                             : (args.mode == 2 ? nblk * args.NB2 : nblk * (args.NB1 + args.NB2));
+  const Sched sch{s_blk, s_cnt, E, args.NB1, args.NB2, args.mode, lag};
 
   const int wg = warp >> 2;
   // setmaxnreg sits inside each warpgroup's branch: after a join ptxas would
@@ -342,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     // ------------------------------------------------------------------ TMA producers
     if (lane == 0) {
       const int p = warp;                       // this warp fills stage p, phases 0,1,0,...
-      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_w = policy_evict_first();    // a tile group's last pass over its weights
+      const uint64_t pol_wk = policy_evict_normal();  // earlier passes: the next block reads them again
       const uint64_t pol_t = policy_evict_last();
       uint8_t* tk = smem + SmemLayout::tok + p * kTokBytes;
       uint8_t* wg = smem + SmemLayout::wgt + p * kWgtBytes;
@@ -350,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       uint8_t* sw = smem + SmemLayout::sfw + p * 2 * kSFChunk;
       uint64_t w_empty = 0;
       int step = 0;                             // global k-block step of this CTA
-      for (int j = blockIdx.x; j < sch.total && !*s_abort; j += gridDim.x) {
-        const Task t = sch.at(j);
+      for (Cursor c; !*s_abort && sch.next(c, q, st, s_abort, false, lane);) {
+        const Task& t = c.t;
         const bool l1 = t.type == 1;
         const int KB = l1 ? args.KB1 : args.KB2;
         int kb = ((p - step) % kStages + kStages) % kStages;   // first k-block of this task on stage p
@@ -379,8 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           mbar_arrive_expect_tx(&full[p], bytes);
           const int kc = kb * kBK;
           tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
-          if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pol_w);
-          else tma_load_2d(wg, &maps.w2, &full[p], kc, t.e * args.H + t.n * kBN, pol_w);
+          const uint64_t pw = t.last ? pol_w : pol_wk;
+          if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pw);
+          else tma_load_2d(wg, &maps.w2, &full[p], kc, t.e * args.H + t.n * kBN, pw);
           bulk_load(st_, sft + static_cast<size_t>(kb) * kSFChunk, kSFChunk, &full[p]);
           bulk_load(sw, sfw + static_cast<size_t>(kb) * 2 * kSFChunk, 2 * kSFChunk, &full[p]);
         }
@@ -389,48 +443,65 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       if (args.prof) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
     }
   } else if (wg == 3) {
-    regs_dec();
+    regs_dec_mma();
     if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
+      // The issuing thread, not the tensor pipe, is the limit when every MMA's
+      // descriptors are rebuilt after its stage's wait: walk the CTA's k-block
+      // stream one round of kStages at a time so that each stage's descriptors
+      // and TMEM columns are fixed offsets from values computed once here.
+      const uint64_t dtok = make_smem_desc(smem_u32(smem + SmemLayout::tok), 16, 1024, 2);
+      const uint64_t dwgt = make_smem_desc(smem_u32(smem + SmemLayout::wgt), 16, 1024, 2);
+      const uint64_t dsft = make_smem_desc(smem_u32(smem + SmemLayout::sft), 0, 128, 0);
+      const uint64_t dsfw = make_smem_desc(smem_u32(smem + SmemLayout::sfw), 0, 128, 0);
       uint32_t phase = 0;
-      int it = 0;
+      int it = 0, kb = 0, KB = 0;
+      Cursor cur;
       uint64_t w_full = 0, w_tempty = 0;
       const uint64_t t_start = globaltimer();
-      for (int j = blockIdx.x; j < sch.total && !*s_abort; j += gridDim.x, ++it) {
-        const Task t = sch.at(j);
-        const int KB = t.type == 1 ? args.KB1 : args.KB2;
+      // start_task: the accumulator must have been drained by the epilogue
+      auto start_task = [&]() -> bool {
+        if (*s_abort || !sch.next(cur, q, st, s_abort, false, lane)) return false;
+        KB = cur.t.type == 1 ? args.KB1 : args.KB2;
         const uint64_t t0 = args.prof ? globaltimer() : 0;
-        if (!mbar_wait(tempty, (it & 1) ^ 1, st, s_abort, kSiteTmemEmpty)) break;
+        if (!mbar_wait(tempty, (it & 1) ^ 1, st, s_abort, kSiteTmemEmpty)) return false;
         if (args.prof) w_tempty += globaltimer() - t0;
         tc_fence_after();
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
-          const uint64_t t1 = args.prof ? globaltimer() : 0;
-          if (!mbar_wait(&full[stage], phase, st, s_abort, kSiteFull)) { ok = false; break; }
-          if (args.prof) w_full += globaltimer() - t1;
-          tc_fence_after();
-          const uint32_t sft_col = tmem + kSfCol0 + stage * kSfColsPerStage;
-          const uint32_t sfw_col = sft_col + 4;
-          const uint32_t sf_t = smem_u32(smem + SmemLayout::sft + stage * kSFChunk);
-          const uint32_t sf_w = smem_u32(smem + SmemLayout::sfw + stage * 2 * kSFChunk);
-          tc_cp_32x128b_warpx4(sft_col, make_smem_desc(sf_t, 0, 128, 0));
-          tc_cp_32x128b_warpx4(sfw_col, make_smem_desc(sf_w, 0, 128, 0));
-          tc_cp_32x128b_warpx4(sfw_col + 4, make_smem_desc(sf_w + kSFChunk, 0, 128, 0));
-          const uint32_t a0 = smem_u32(smem + SmemLayout::tok + stage * kTokBytes);
-          const uint32_t b0 = smem_u32(smem + SmemLayout::wgt + stage * kWgtBytes);
+        return true;
+      };
+      bool live = start_task();
+      while (live) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = make_smem_desc(a0 + kk * 32, 16, 1024, 2);
-            const uint64_t bdesc = make_smem_desc(b0 + kk * 32, 16, 1024, 2);
-            tc_mma_mxf8f6f4(tmem, adesc, bdesc, make_idesc(kk), sft_col, sfw_col, (kb | kk) != 0);
+        for (int s = 0; s < kStages; ++s) {
+          if (live) {
+            const uint64_t t1 = args.prof ? globaltimer() : 0;
+            if (!mbar_wait(&full[s], phase, st, s_abort, kSiteFull)) {
+              live = false;
+            } else {
+              if (args.prof) w_full += globaltimer() - t1;
+              tc_fence_after();
+              const uint32_t sft_col = tmem + kSfCol0 + s * kSfColsPerStage;
+              const uint32_t sfw_col = sft_col + 4;
+              tc_cp_32x128b_warpx4(sft_col, dsft + ((s * kSFChunk) >> 4));
+              tc_cp_32x128b_warpx4(sfw_col, dsfw + ((s * 2 * kSFChunk) >> 4));
+              tc_cp_32x128b_warpx4(sfw_col + 4, dsfw + (((s * 2 + 1) * kSFChunk) >> 4));
+              const uint64_t da = dtok + ((s * kTokBytes) >> 4);
+              const uint64_t db = dwgt + ((s * kWgtBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)   // K advances 32 bytes = 2 descriptor units
+                tc_mma_mxf8f6f4(tmem, da + 2 * kk, db + 2 * kk, make_idesc(kk), sft_col, sfw_col, (kb | kk) != 0);
+              tc_commit(&empty[s]);
+              if (++kb == KB) {
+                tc_commit(tfull);
+                kb = 0;
+                ++it;
+                live = start_task();
+              }
+            }
           }
-          tc_commit(&empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
-        tc_commit(tfull);
+        phase ^= 1;
       }
       if (args.prof) {
         args.prof[blockIdx.x * 8 + 1] = w_full;
@@ -442,18 +513,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     __syncwarp();
     } else if (warp < kGatherWarp0 + kGatherWarps && args.mode == 3) {
       gather_rows(args, s_blk, s_cnt, sch, s_abort, warp - kGatherWarp0, lane, nblk);
+    } else if (warp == kSchedWarp && lane == 0) {
+      // ------------------------------------------------------------------ tile-group scheduler
+      // Groups are taken from one counter shared by all CTAs, in increasing
+      // order, so CTAs that are free start the groups next to each other at
+      // about the same time: an expert's token block is read by its tiles
+      // while it is still in L2, and no CTA is left with a longer tail of
+      // static work.  Every dependency of a group (the gather and L1 tiles
+      // of the blocks an L2 group reads) has a smaller index, so the group
+      // with the smallest index not yet finished can always run.
+      const int ng = sch.groups();
+      for (int i = 0;; ++i) {
+        const int slot = i % kQueue;
+        if (!mbar_wait(&q.empty[slot], ((i / kQueue) & 1) ^ 1, st, s_abort, kSiteQueueEmpty)) break;
+        int g = -1;
+        for (;;) {
+          const int x = atomicAdd(args.sched, 1);
+          if (x >= ng) break;
+          if (sch.group_blocks(x) > 0) {   // experts without tokens have nothing to do
+            g = x;
+            break;
+          }
+        }
+        q.g[slot] = g;
+        mbar_arrive(&q.full[slot]);
+        if (g < 0) break;
+      }
     }
   } else {
     regs_inc();
     // ------------------------------------------------------------------ epilogue (8 warps)
-    const int q = warp & 3;                // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;             // TMEM lane quadrant this warp may access
     const int half = (warp - kEpiWarp0) >> 2;   // which half of the columns
-    const int m = q * 32 + lane;           // accumulator row = pool row inside the block
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int m = quad * 32 + lane;           // accumulator row = pool row inside the block
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     int it = 0;
     uint64_t w_tfull = 0, busy = 0;
-    for (int j = blockIdx.x; j < sch.total; j += gridDim.x, ++it) {
-      const Task t = sch.at(j);
+    for (Cursor c; sch.next(c, q, st, s_abort, true, lane); ++it) {
+      const Task& t = c.t;
       const bool live = m < t.valid;
       const size_t row = static_cast<size_t>(t.b) * kBT + m;
       const int s = live ? __ldg(args.src + row) : 0;
@@ -555,6 +652,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.pool2 = W.pool2; a.pool2_sf = W.pool2_sf;
   a.partials = W.part; a.dbg = g.dbg;
   a.ctr_gather = W.ctr; a.ctr_l1 = W.ctr + L.nblk_cap;
+  a.sched = W.ctr + 2 * L.nblk_cap + mode;
   a.status = W.status; a.timeout_ns = g.timeout_ns;
   a.prof = g.prof ? g.prof + (mode == 2 ? 8 * 1024 : 0) : nullptr;
   {

@@ -32,7 +32,8 @@ struct WsPtrs {
   int* cnt;
   int* blk_off;
   int* dscr;
-  int* ctr;                  // [2][nblk_cap] per-block arrival counters of the fused stream
+  int* ctr;                  // [2][nblk_cap] per-block arrival counters of the fused stream, then
+                             // kSchedCounters tile-group counters
   int* slot;
   int* src;
   uint8_t* pool_x;
@@ -56,6 +57,7 @@ const DevInfo& dev_info();
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
                             int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
                             int64_t scratch_ints, cudaStream_t s);
+constexpr int kSchedCounters = 4;        // tile-group counters after the arrival counters, one per GEMM mode
 constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA counts [CTAs][E]
 cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
                           cudaStream_t s);
