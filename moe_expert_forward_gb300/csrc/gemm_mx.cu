@@ -333,6 +333,9 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 __device__ __forceinline__ void regs_dec_mma() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kMmaRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
 
+// kProf: record per-role wait and busy times (debug_flags bit 1).  A separate
+// instantiation, because even untaken timing branches slow the MMA issue loop.
+template <bool kProf>
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ Maps maps, const Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -426,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const uint8_t* sft = (l1 ? args.pool_x_sf : args.pool2_sf) + static_cast<size_t>(t.b) * KB * kSFChunk;
         for (; kb < KB; kb += kStages) {
           const uint32_t phase = ((step + kb) / kStages) & 1;
-          const uint64_t t0 = args.prof ? globaltimer() : 0;
+          const uint64_t t0 = kProf ? globaltimer() : 0;
           if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
-          if (args.prof) w_empty += globaltimer() - t0;
+          if (kProf) w_empty += globaltimer() - t0;
           mbar_arrive_expect_tx(&full[p], bytes);
           const int kc = kb * kBK;
           tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         step += KB;
       }
-      if (args.prof) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
+      if (kProf) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
     }
   } else if (wg == 3) {
     regs_dec_mma();
@@ -458,15 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       uint32_t phase = 0;
       int it = 0, kb = 0, KB = 0;
       Cursor cur;
-      uint64_t w_full = 0, w_tempty = 0;
+      uint64_t w_full = 0, w_tempty = 0;   // SM cycles (clock64) spent in these waits
       const uint64_t t_start = globaltimer();
+      const long long c_start = clock64();
       // start_task: the accumulator must have been drained by the epilogue
       auto start_task = [&]() -> bool {
         if (*s_abort || !sch.next(cur, q, st, s_abort, false, lane)) return false;
         KB = cur.t.type == 1 ? args.KB1 : args.KB2;
-        const uint64_t t0 = args.prof ? globaltimer() : 0;
+        const long long t0 = kProf ? clock64() : 0;
         if (!mbar_wait(tempty, (it & 1) ^ 1, st, s_abort, kSiteTmemEmpty)) return false;
-        if (args.prof) w_tempty += globaltimer() - t0;
+        if (kProf) w_tempty += clock64() - t0;
         tc_fence_after();
         return true;
       };
@@ -475,11 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
 #pragma unroll
         for (int s = 0; s < kStages; ++s) {
           if (live) {
-            const uint64_t t1 = args.prof ? globaltimer() : 0;
+            const long long t1 = kProf ? clock64() : 0;
             if (!mbar_wait(&full[s], phase, st, s_abort, kSiteFull)) {
               live = false;
             } else {
-              if (args.prof) w_full += globaltimer() - t1;
+              if (kProf) w_full += clock64() - t1;
               tc_fence_after();
               const uint32_t sft_col = tmem + kSfCol0 + s * kSfColsPerStage;
               const uint32_t sfw_col = sft_col + 4;
@@ -503,11 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         phase ^= 1;
       }
-      if (args.prof) {
+      if (kProf) {
         args.prof[blockIdx.x * 8 + 1] = w_full;
         args.prof[blockIdx.x * 8 + 2] = w_tempty;
         args.prof[blockIdx.x * 8 + 3] = globaltimer() - t_start;
         args.prof[blockIdx.x * 8 + 4] = it;
+        args.prof[blockIdx.x * 8 + 7] = clock64() - c_start;   // SM cycles over the span
       }
     }
     __syncwarp();
@@ -555,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       const size_t row = static_cast<size_t>(t.b) * kBT + m;
       const int s = live ? __ldg(args.src + row) : 0;
       const float w = (t.type == 1 && live) ? __ldg(args.topk_w + s) : 0.f;   // loaded before the wait
-      const uint64_t t0 = args.prof ? globaltimer() : 0;
+      const uint64_t t0 = kProf ? globaltimer() : 0;
       if (!mbar_wait(tfull, it & 1, st, s_abort, kSiteTmemFull)) break;
-      const uint64_t t1 = args.prof ? globaltimer() : 0;
+      const uint64_t t1 = kProf ? globaltimer() : 0;
       tc_fence_after();
       // copy this thread's 128 accumulator columns, then hand TMEM back to the MMA warp
       // L1: gate [64h, 64h+64) and up [128+64h, 128+64h+64); L2: [128h, 128h+128)
@@ -604,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           }
         }
       }
-      if (args.prof) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
+      if (kProf) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
     }
-    if (args.prof && warp == kEpiWarp0 && lane == 0) {
+    if (kProf && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
       args.prof[blockIdx.x * 8 + 6] = busy;
     }
@@ -678,22 +683,23 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  static int configured = -1;
+  auto kernel = a.prof ? gemm_mx_kernel<true> : gemm_mx_kernel<false>;
+  static int configured[2] = {-1, -1};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (configured != dev) {
+  int& conf = configured[a.prof ? 1 : 0];
+  if (conf != dev) {
     // the setmaxnreg split assumes exactly kLaunchRegs registers a thread at launch
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_mx_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(gemm_mx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemLayout::total(kMaxE) + 1024);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total(kMaxE) + 1024);
     if (e != cudaSuccess) return e;
-    configured = dev;
+    conf = dev;
   }
   if (mode != 3) {
-    gemm_mx_kernel<<<g.grid, kThreads, SmemLayout::total(L.E) + 1024, s>>>(maps, a);
+    kernel<<<g.grid, kThreads, SmemLayout::total(L.E) + 1024, s>>>(maps, a);
     return cudaGetLastError();
   }
   // the fused stream waits across CTAs: launch cooperatively so that every CTA is resident
@@ -707,7 +713,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_mx_kernel, maps, a);
+  return cudaLaunchKernelEx(&cfg, kernel, maps, a);
 }
 
 }  // namespace mm
