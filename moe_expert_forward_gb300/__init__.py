@@ -206,10 +206,34 @@ def options(variant: int = MM_MOE_VARIANT_MX, **kw) -> mm_moe_options:
     return o
 
 
+def _need(t, nbytes: int, name: str, what: str) -> None:
+    """The C ABI takes bare pointers; check here that a tensor is a contiguous
+    CUDA buffer of at least `nbytes` bytes before its address goes down."""
+    if t is None or not t.is_cuda or not t.is_contiguous() or t.numel() * t.element_size() < nbytes:
+        got = "None" if t is None else (f"{tuple(t.shape)} {t.dtype} on {t.device}"
+                                        f"{'' if t.is_contiguous() else ' (not contiguous)'}")
+        raise MMError(MM_MOE_ERR_INVALID_ARG, f"{what}: {name} must be a contiguous CUDA tensor of at least "
+                                              f"{nbytes} bytes, got {got}")
+
+
+def _input_bytes(variant: int, T: int, H: int, I: int, E: int, K: int) -> dict:
+    """Bytes of every caller buffer of one forward, in the layouts of mm_moe.h."""
+    if variant == MM_MOE_VARIANT_MX:
+        return {"x": T * H, "x_sf": T * (H // 32), "w1": E * 2 * I * H // 2, "w1_sf": E * 2 * I * (H // 32),
+                "w2": E * H * I // 2, "w2_sf": E * H * (I // 32), "topk_idx": 4 * T * K, "topk_w": 4 * T * K,
+                "out": 2 * T * H}
+    return {"x": T * H, "x_sf": 4 * T * (H // 128), "w1": E * 2 * I * H, "w1_sf": 4 * E * (2 * I // 128) * (H // 128),
+            "w2": E * H * I, "w2_sf": 4 * E * (H // 128) * (I // 128), "topk_idx": 4 * T * K, "topk_w": 4 * T * K,
+            "out": 2 * T * H}
+
+
 def prepare_weights(w1_sf, w2_sf, H, I, E, opt=None, stream=None):
     """Return (w1_sfp, w2_sfp) device tensors in the kernels' scale layout."""
     import torch
     opt = opt or options()
+    need = _input_bytes(opt.variant, 0, H, I, E, 1)
+    _need(w1_sf, need["w1_sf"], "w1_sf", "prepare_weights")
+    _need(w2_sf, need["w2_sf"], "w2_sf", "prepare_weights")
     n1, n2 = mm_moe_weight_sf_size(opt, H, I, E)
     a = torch.empty(n1, dtype=torch.uint8, device=w1_sf.device)
     b = torch.empty(n2, dtype=torch.uint8, device=w1_sf.device)
@@ -226,9 +250,19 @@ def alloc_workspace(T, H, I, E, K, opt=None, device="cuda"):
 
 def forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, H, I, E, workspace, opt=None, stream=None):
     T, K = topk_idx.shape
+    opt = opt or options()
+    need = _input_bytes(opt.variant, T, H, I, E, K)
+    for name, t in (("x", x), ("x_sf", x_sf), ("topk_idx", topk_idx), ("topk_w", topk_w), ("w1", w1), ("w2", w2),
+                    ("out", out)):
+        if T > 0 or name in ("w1", "w2"):
+            _need(t, need[name], name, "forward")
+    n1, n2 = mm_moe_weight_sf_size(opt, H, I, E)
+    _need(w1_sfp, n1, "w1_sfp", "forward")
+    _need(w2_sfp, n2, "w2_sfp", "forward")
+    _need(workspace, 0, "workspace", "forward")   # its size goes down with it: the library checks that
     _check(mm_moe_forward(_ptr(x), _ptr(x_sf), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w1_sfp), _ptr(w2),
                           _ptr(w2_sfp), _ptr(out), T, H, I, E, K, _ptr(workspace), workspace.numel(),
-                          opt or options(), _stream(stream)), "mm_moe_forward")
+                          opt, _stream(stream)), "mm_moe_forward")
     return out
 
 

@@ -286,13 +286,13 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
   const uint64_t timeout_ns = static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull;
+  // arrival counters of the fused stream and the tile-group counters of every GEMM launch
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), s);
   if (o.variant == MM_MOE_VARIANT_MX) {
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, topk_w, W.dbg, W.prof, timeout_ns, grid};
-    // arrival counters of the fused stream and the tile-group counters of every GEMM launch
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), s);
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);

@@ -66,3 +66,28 @@ def test_weight_sf_sizes(M):
     assert a == 256 * 4096 * 4096 // 32 and b == 256 * 4096 * 2048 // 32
     a, b = M.mm_moe_weight_sf_size(M.options(M.MM_MOE_VARIANT_F8), 4096, 2048, 256)
     assert a == 256 * 32 * 32 * 4 and b == 256 * 32 * 16 * 4
+
+
+def test_binding_rejects_wrong_buffers_before_any_device_work(M):
+    """The C ABI takes bare pointers; the Python binding checks device, contiguity
+    and byte size of every buffer against the layouts of mm_moe.h first, so a
+    host tensor or the other variant's scale array never reaches a kernel."""
+    import torch
+    H, I, E = 256, 128, 8
+    # F8 scale arrays ([E, 2I/128, H/128] fp32) are far smaller than MX's UE8M0 ones ([E, 2I, H/32] bytes)
+    f8_w1_sf = torch.empty(E, 2 * I // 128, H // 128, dtype=torch.float32)
+    f8_w2_sf = torch.empty(E, H // 128, I // 128, dtype=torch.float32)
+    with pytest.raises(M.MMError) as ei:
+        M.prepare_weights(f8_w1_sf, f8_w2_sf, H, I, E, M.options(M.MM_MOE_VARIANT_MX))
+    assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG and "w1_sf" in str(ei.value)
+    # a host tensor of the right size is refused as well
+    mx_w1_sf = torch.empty(E, 2 * I, H // 32, dtype=torch.uint8)
+    with pytest.raises(M.MMError) as ei:
+        M.prepare_weights(mx_w1_sf, mx_w1_sf, H, I, E, M.options(M.MM_MOE_VARIANT_MX))
+    assert "CUDA" in str(ei.value)
+    T, K = 4, 2
+    idx = torch.zeros(T, K, dtype=torch.int32)
+    with pytest.raises(M.MMError) as ei:
+        M.forward(torch.empty(T, H, dtype=torch.uint8), None, idx, None, None, None, None, None, None, H, I, E,
+                  torch.empty(16, dtype=torch.uint8))
+    assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG
