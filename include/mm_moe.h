@@ -98,7 +98,12 @@ typedef struct mm_moe_options {
                                    completion than will ever arrive, so the call ends with
                                    MM_MOE_ERR_TIMEOUT after wait_timeout_ms (tests the device-side
                                    timeout path); 0 for normal use */
-  int reserved[7];
+  int cta_pairs;                /* MX variant: 2 = the GEMM CTAs run as 2-CTA clusters whose two CTAs take
+                                   neighbouring weight tiles of the same pool block and load each token
+                                   tile once for both (TMA multicast); 0 or 1 = one CTA per tile group
+                                   (default: the pair's lockstep costs more than the halved token reads
+                                   save on GB300).  The results are identical either way. */
+  int reserved[6];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

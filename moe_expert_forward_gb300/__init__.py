@@ -37,7 +37,8 @@ EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_
 class mm_moe_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("fused", ctypes.c_int), ("lag_units", ctypes.c_int),
                 ("retain_intermediate", ctypes.c_int), ("wait_timeout_ms", ctypes.c_uint),
-                ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("reserved", ctypes.c_int * 7),
+                ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("cta_pairs", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6),
                 ("timing_events", ctypes.c_void_p)]
 
 

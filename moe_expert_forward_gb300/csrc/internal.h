@@ -82,6 +82,7 @@ struct GemmLaunch {
   unsigned long long* prof; // per-CTA role timings (debug_flags bit 1) or null
   uint64_t timeout_ns;
   int grid;
+  bool pair;                // run as 2-CTA clusters sharing token tiles (when the device allows)
 };
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);

@@ -135,6 +135,27 @@ def test_fused_stream_bitwise_equals_two_launch_path(M, name, lag):
     assert torch.equal(rows, pb.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()])
 
 
+@pytest.mark.parametrize("fused", [0, 1])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "manyexp", "k1"])
+def test_cta_pairs_bitwise_equal_single_ctas(M, name, fused):
+    """2-CTA clusters (each CTA loading half of every token tile into both, one
+    weight tile each; tiny has an odd tile count, so one CTA of the last pair
+    only helps load) compute every tile exactly as single CTAs do."""
+    cfg = SMALL[name]
+    dev = to_dev(W.make_inputs(cfg, "cpu"))
+    out_a, ws_a, prep, st_a = run_forward(M, cfg, dev, M.options(fused=fused, cta_pairs=0))
+    out_a = out_a.clone()
+    out_b, ws_b, _, st_b = run_forward(M, cfg, dev, M.options(fused=fused, cta_pairs=2), prepared=prep)
+    assert st_a[0] == 0 and st_b[0] == 0, (st_a, st_b)
+    assert torch.equal(out_a, out_b)
+    opt = M.options()
+    pa = M.workspace_view(ws_a, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "pool2")
+    pb = M.workspace_view(ws_b, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "pool2")
+    _, blk, _, src, _ = read_routing(M, cfg, ws_a, opt)
+    live = torch.from_numpy(src[:blk[-1] * 128] >= 0)
+    assert torch.equal(pa.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()], pb.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()])
+
+
 def test_fused_stream_parity_and_masking(M):
     cfg = SMALL["ragged"].with_(seed=61)
     inp = W.make_inputs(cfg, "cpu")
