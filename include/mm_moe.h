@@ -31,7 +31,8 @@
  *                      (value 2^(b-127)) per 32 contiguous elements along the
  *                      contraction dimension; tcgen05 kind::mxf8f6f4.
  *   MM_MOE_VARIANT_F8  e4m3 activations with one fp32 scale per 1x128, e4m3
- *                      weights with one fp32 scale per 128x128 block; the
+ *                      weights with one fp32 scale per 128x128 block (H and I
+ *                      at most 8192, else MM_MOE_ERR_UNSUPPORTED); the
  *                      intermediate is requantised per 128 with a raw fp32
  *                      scale amax/448 (DeepGEMM PR #440, "Why the order and not
  *                      the pool size"); tcgen05 kind::f8f6f4.

@@ -265,6 +265,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       !aligned(workspace, 256) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
     return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
+  // the F8 epilogue stages each task's weight scales in shared memory for up to kF8MaxKB k-blocks
+  if (o.variant == MM_MOE_VARIANT_F8 && (H / 128 > kF8MaxKB || I / 128 > kF8MaxKB)) return MM_MOE_ERR_UNSUPPORTED;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
   const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
   const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
@@ -307,7 +309,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,
-                   grid};
+                   grid, W.prof};
     if (e == cudaSuccess) e = launch_gemm_f8_l1(g, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {

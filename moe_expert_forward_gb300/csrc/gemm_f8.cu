@@ -39,6 +39,7 @@ constexpr int kBN = 256;
 constexpr int kTokBytes = kBT * kBK;
 constexpr int kWgtBytes = kBN * kBK;
 constexpr int kTmemCols = 512;
+constexpr int kMaxKB = kF8MaxKB;       // k-blocks of weight scales staged per task (H, I <= 8192)
 
 enum : int { kSiteEmpty = 201, kSiteFull = 202, kSitePEmpty = 203, kSitePFull = 204, kSiteAmax = 205 };
 
@@ -57,6 +58,7 @@ struct Args {
   float* partials;      // L2: [K, T, H]
   int* status;
   uint64_t timeout_ns;
+  unsigned long long* prof;   // per-CTA role cycles (debug_flags bit 1) or null
 };
 
 struct TokenMaps {
@@ -66,11 +68,12 @@ struct TokenMaps {
 struct SmemLayout {
   static constexpr int tok = 0;
   static constexpr int wgt = tok + kStages * kTokBytes;
-  static constexpr int amax = wgt + kStages * kWgtBytes;              // [2][128] fp32
-  static constexpr int meta = amax + 2 * 128 * 4;
+  static constexpr int amax = wgt + kStages * kWgtBytes;              // [2 tasks][2 halves][128] fp32
+  static constexpr int wsc = amax + 2 * 2 * 128 * 4;                   // [2 tasks][2 rows][kMaxKB] fp32
+  static constexpr int meta = wsc + 2 * 2 * kMaxKB * 4;
   static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
-  // full[S], empty[S], pfull[2], pempty[2], epi
-  static constexpr int nbars = 2 * kStages + 5;
+  // full[S], empty[S], pfull[2], pempty[2], epi, wsc
+  static constexpr int nbars = 2 * kStages + 6;
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -101,7 +104,12 @@ __device__ __forceinline__ uint32_t make_idesc() {
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
 
-template <int PHASE>
+// kProf: record per-role SM cycles into args.prof[blockIdx.x * 8 + i]: 0 MMA
+// issuer span, 1 its waits for a free partial buffer, 2 its waits for data, 3
+// epilogue (warp 4) waits for a partial, 4 promotion, 5 per-task SwiGLU /
+// requant / stores, 6 k-blocks, 7 epilogue span; args.prof[4096 + blockIdx.x]:
+// the epilogue's per-task setup.  A separate instantiation.
+template <int PHASE, bool kProf>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ TokenMaps tmT, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -110,12 +118,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_blk = reinterpret_cast<int*>(smem + SmemLayout::meta);
   int* s_cnt = s_blk + E + 1;
   float* s_amax = reinterpret_cast<float*>(smem + SmemLayout::amax);
+  float* s_wsc = reinterpret_cast<float*>(smem + SmemLayout::wsc);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars_after_meta(E));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* pfull = bars + 2 * kStages;
   uint64_t* pempty = pfull + 2;
   uint64_t* epibar = pempty + 2;
+  uint64_t* wscbar = epibar + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -134,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pempty[i], 8);
     }
     mbar_init(epibar, 256);
+    mbar_init(wscbar, 256);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -192,12 +203,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int g = 0;                                 // global k-block counter: partial buffer g & 1
+      const long long c_start = kProf ? clock64() : 0;
+      long long c_pe = 0, c_full = 0;
       for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++g) {
           const int pb = g & 1;
+          const long long tm0 = kProf ? clock64() : 0;
           if (!mbar_wait(&pempty[pb], ((g >> 1) & 1) ^ 1, st, s_abort, kSitePEmpty)) { ok = false; break; }
+          const long long tm1 = kProf ? clock64() : 0;
           if (!mbar_wait(&full[stage], phase, st, s_abort, kSiteFull)) { ok = false; break; }
+          if (kProf) { c_pe += tm1 - tm0; c_full += clock64() - tm1; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(smem + SmemLayout::tok + stage * kTokBytes);
           const uint32_t b0 = smem_u32(smem + SmemLayout::wgt + stage * kWgtBytes);
@@ -210,6 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
+      }
+      if (kProf) {
+        args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
+        args.prof[blockIdx.x * 8 + 1] = c_pe;
+        args.prof[blockIdx.x * 8 + 2] = c_full;
+        args.prof[blockIdx.x * 8 + 6] = g;
       }
     }
     __syncwarp();
@@ -226,6 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c1 = PHASE == 1 ? 128 + 64 * half : 128 * half + 64;
     int g = 0;
     uint32_t ephase = 0;
+    uint32_t wphase = 0;
+    const long long e_start = kProf ? clock64() : 0;
+    long long e_wait = 0, e_promo = 0, e_tail = 0, e_setup = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, n, b, valid;
       decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
@@ -233,28 +258,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t row = static_cast<size_t>(b) * kBT + m;
       const int s = live ? __ldg(args.src + row) : 0;
       const float w = (PHASE == 1 && live) ? __ldg(args.topk_w + s) : 0.f;
-      // weight scale rows (in blocks of 128) of the two column groups
-      int wr0, wr1, wrows;
-      if (PHASE == 1) { wr0 = n; wr1 = (args.I >> 7) + n; wrows = 2 * args.I / 128; }
-      else {
-        wrows = args.H / 128;
-        wr0 = 2 * n + half < wrows ? 2 * n + half : wrows - 1;   // a half past H is never stored
-        wr1 = wr0;
+      const int wrows = PHASE == 1 ? 2 * args.I / 128 : args.H / 128;   // weight scale block rows
+      // the task's weight scales (two block rows x KB) go to shared memory once: the
+      // epilogue threads load them together and meet at a bounded rendezvous; the
+      // buffer alternates between tasks, so a slow reader of the last task is never
+      // overwritten (its next writer passed this task's rendezvous first)
+      const long long ts0 = kProf ? clock64() : 0;
+      const int et = (warp - 4) * 32 + lane;
+      float* wsc = s_wsc + (wphase & 1) * 2 * kMaxKB;
+      {
+        const int ra = PHASE == 1 ? n : (2 * n < wrows ? 2 * n : wrows - 1);
+        const int rb = PHASE == 1 ? (args.I >> 7) + n : (2 * n + 1 < wrows ? 2 * n + 1 : wrows - 1);
+        for (int i = et; i < 2 * KB; i += 256) {
+          const int r = i / KB;
+          wsc[r * kMaxKB + (i - r * KB)] =
+              __ldg(args.sw + (static_cast<size_t>(e) * wrows + (r ? rb : ra)) * KB + (i - r * KB));
+        }
       }
-      const float* swe = args.sw + static_cast<size_t>(e) * wrows * KB;
+      mbar_arrive(wscbar);
+      if (!mbar_wait(wscbar, wphase & 1, st, s_abort, kSiteAmax)) break;
+      ++wphase;
+      // L1: gate scales row 0, up scales row 1; L2: this half's 128 columns use row `half`
+      const float* w0s = wsc + (PHASE == 1 ? 0 : half) * kMaxKB;
+      const float* w1s = wsc + (PHASE == 1 ? 1 : half) * kMaxKB;
       const float* sxr = args.sx + row * KB;
       float acc0[64], acc1[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
       bool ok = true;
-      float sx_next = live ? __ldg(sxr) : 0.f;
+      // the row's activation scale of k-block kb + 2 is loaded while kb's partial is
+      // promoted, so no global-load latency sits between a partial and its promotion
+      float sxa = live ? __ldg(sxr) : 0.f;
+      float sxb = (live && KB > 1) ? __ldg(sxr + 1) : 0.f;
+      if (kProf) e_setup += clock64() - ts0;
       for (int kb = 0; kb < KB; ++kb, ++g) {
-        const float sxk = sx_next;
-        if (kb + 1 < KB) sx_next = live ? __ldg(sxr + kb + 1) : 0.f;
-        const float f0 = sxk * __ldg(swe + static_cast<size_t>(wr0) * KB + kb);
-        const float f1 = sxk * __ldg(swe + static_cast<size_t>(wr1) * KB + kb);
+        const float f0 = sxa * w0s[kb];
+        const float f1 = sxa * w1s[kb];
+        sxa = sxb;
+        if (kb + 2 < KB) sxb = live ? __ldg(sxr + kb + 2) : 0.f;
         const int pb = g & 1;
+        const long long tw0 = kProf ? clock64() : 0;
         if (!mbar_wait(&pfull[pb], (g >> 1) & 1, st, s_abort, kSitePFull)) { ok = false; break; }
+        const long long tw1 = kProf ? clock64() : 0;
         tc_fence_after();
         // one 32-column slice at a time keeps at most 128 sums + 32 loaded values live
         const uint32_t tb = tlane + pb * kBN;
@@ -278,8 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty[pb]);
+        if (kProf) { e_wait += tw1 - tw0; e_promo += clock64() - tw1; }
       }
       if (!ok) break;
+      const long long tw2 = kProf ? clock64() : 0;
       if (PHASE == 1) {
         // a = silu(gate) * up * w over this thread's 64 intermediate columns
         float amax = 0.f;
@@ -290,18 +337,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           amax = fmaxf(amax, fabsf(acc0[j]));
         }
         // the 128-column requant block spans both halves: exchange row amax
-        s_amax[half * 128 + m] = amax;
+        // one rendezvous per task: the exchange buffer alternates between tasks, and a
+        // thread writes it again two tasks later only after everyone passed the next rendezvous
+        float* xa = s_amax + (ephase & 1) * 256;
+        xa[half * 128 + m] = amax;
         mbar_arrive(epibar);
         if (!mbar_wait(epibar, ephase, st, s_abort, kSiteAmax)) break;
         ephase ^= 1;
-        amax = fmaxf(amax, s_amax[(half ^ 1) * 128 + m]);
+        amax = fmaxf(amax, xa[(half ^ 1) * 128 + m]);
         if (live) {
           const float sf = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+          // x * (1/s) instead of x / s: the fp32 quotient moves by at most about an ulp,
+          // which changes an e4m3 code only within ~2^-20 of a rounding boundary
+          const float rsf = __frcp_rn(sf);
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const uint32_t lo = cvt_e4m3x2(__fdiv_rn(acc0[4 * i], sf), __fdiv_rn(acc0[4 * i + 1], sf));
-            const uint32_t hi = cvt_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sf), __fdiv_rn(acc0[4 * i + 3], sf));
+            const uint32_t lo = cvt_e4m3x2(acc0[4 * i] * rsf, acc0[4 * i + 1] * rsf);
+            const uint32_t hi = cvt_e4m3x2(acc0[4 * i + 2] * rsf, acc0[4 * i + 3] * rsf);
             packed[i] = lo | (hi << 16);
           }
           uint4* dst = reinterpret_cast<uint4*>(args.out_codes + row * args.I + n * 128 + 64 * half);
@@ -310,23 +363,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
           if (half == 0) args.out_sf[row * (args.I / 128) + n] = sf;
         }
-        // second rendezvous: s_amax may be overwritten by the next tile only after both halves read it
-        mbar_arrive(epibar);
-        if (!mbar_wait(epibar, ephase, st, s_abort, kSiteAmax)) break;
-        ephase ^= 1;
       } else {
         if (live && n * kBN + 128 * half < args.H) {
           const int t = s / args.K;
           const int k = s - t * args.K;
           float4* dst = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(k) * args.T + t) * args.H +
                                                   n * kBN + 128 * half);
+          // 32-byte stores: half the store instructions of float4
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            dst[i] = make_float4(acc0[4 * i], acc0[4 * i + 1], acc0[4 * i + 2], acc0[4 * i + 3]);
-            dst[16 + i] = make_float4(acc1[4 * i], acc1[4 * i + 1], acc1[4 * i + 2], acc1[4 * i + 3]);
+          for (int i = 0; i < 8; ++i) {
+            st_global_v8(reinterpret_cast<float*>(dst) + 8 * i, acc0 + 8 * i);
+            st_global_v8(reinterpret_cast<float*>(dst) + 64 + 8 * i, acc1 + 8 * i);
           }
         }
       }
+      if (kProf) e_tail += clock64() - tw2;
+    }
+    if (kProf && warp == 4 && lane == 0) {
+      args.prof[blockIdx.x * 8 + 3] = e_wait;
+      args.prof[blockIdx.x * 8 + 4] = e_promo;
+      args.prof[blockIdx.x * 8 + 5] = e_tail;
+      args.prof[blockIdx.x * 8 + 7] = clock64() - e_start;
+      args.prof[4096 + blockIdx.x] = e_setup;   // inside this phase's 8192-entry region
     }
   }
 
@@ -345,17 +403,18 @@ template <int PHASE>
 cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   const Layout& L = *g.L;
   const WsPtrs& W = *g.W;
+  const bool prof = g.prof != nullptr;
+  auto kernel = prof ? gemm_f8_kernel<PHASE, true> : gemm_f8_kernel<PHASE, false>;
   // The register split assumes the kernel starts with exactly kLaunchRegs per thread.
-  static int checked[2] = {0, 0};
-  if (!checked[PHASE - 1]) {
+  static int checked[2][2] = {{0, 0}, {0, 0}};
+  if (!checked[PHASE - 1][prof]) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, gemm_f8_kernel<PHASE>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(gemm_f8_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemLayout::total(kMaxE) + 1024);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total(kMaxE) + 1024);
     if (e != cudaSuccess) return e;
-    checked[PHASE - 1] = 1;
+    checked[PHASE - 1][prof] = 1;
   }
   CUtensorMap tmW;
   TokenMaps tmT;
@@ -363,6 +422,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   a.T = L.T; a.H = L.H; a.I = L.I; a.E = L.E; a.K = L.K;
   a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;
   a.status = W.status; a.timeout_ns = g.timeout_ns;
+  a.prof = g.prof ? g.prof + (PHASE == 2 ? 8 * 1024 : 0) : nullptr;
   a.sw = g.wsf;
   const uint8_t* pool;
   int kdim;
@@ -396,7 +456,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
     if (encode_tmap_2d(maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, pool, kdim, L.P, kdim, 128, 32u << i,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  gemm_f8_kernel<PHASE><<<g.grid, kThreads, SmemLayout::total(L.E) + 1024, s>>>(tmW, tmT, a);
+  kernel<<<g.grid, kThreads, SmemLayout::total(L.E) + 1024, s>>>(tmW, tmT, a);
   return cudaGetLastError();
 }
 

@@ -57,6 +57,7 @@ const DevInfo& dev_info();
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
                             int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
                             int64_t scratch_ints, cudaStream_t s);
+constexpr int kF8MaxKB = 64;             // F8 variant: H and I at most 64 x 128
 constexpr int kSchedCounters = 4;        // tile-group counters after the arrival counters, one per GEMM mode
 constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA counts [CTAs][E]
 cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
@@ -96,6 +97,7 @@ struct GemmLaunchF8 {
   const float* topk_w;
   uint64_t timeout_ns;
   int grid;
+  unsigned long long* prof;  // per-CTA role cycles (debug_flags bit 1) or null
 };
 cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s);
 cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s);
