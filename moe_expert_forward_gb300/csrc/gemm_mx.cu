@@ -488,17 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const int k = s - tt * args.K;
         const int col0 = t.n * kBN + 128 * half;
         if (live && col0 < args.H) {
-          float4* dst = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(k) * args.T + tt) * args.H + col0);
+          float* dst = args.partials + (static_cast<size_t>(k) * args.T + tt) * args.H + col0;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            dst[i] = make_float4(__uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
-                                 __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
-            dst[8 + i] = make_float4(__uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]),
-                                     __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]));
-            dst[16 + i] = make_float4(__uint_as_float(r2[4 * i]), __uint_as_float(r2[4 * i + 1]),
-                                      __uint_as_float(r2[4 * i + 2]), __uint_as_float(r2[4 * i + 3]));
-            dst[24 + i] = make_float4(__uint_as_float(r3[4 * i]), __uint_as_float(r3[4 * i + 1]),
-                                      __uint_as_float(r3[4 * i + 2]), __uint_as_float(r3[4 * i + 3]));
+          for (int i = 0; i < 4; ++i) {   // 32-byte stores of the row's 128 columns
+            st_global_v8(dst + 8 * i, r0 + 8 * i);
+            st_global_v8(dst + 32 + 8 * i, r1 + 8 * i);
+            st_global_v8(dst + 64 + 8 * i, r2 + 8 * i);
+            st_global_v8(dst + 96 + 8 * i, r3 + 8 * i);
           }
         }
       }

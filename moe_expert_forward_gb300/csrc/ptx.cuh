@@ -95,6 +95,13 @@ __device__ __forceinline__ void st_global_v8(float* p, const float* v) {
                : "memory");
 }
 
+// The same for eight 32-bit words (fp32 bit patterns straight from TMEM).
+__device__ __forceinline__ void st_global_v8(float* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
