@@ -360,7 +360,7 @@ def run_reference(args, ws_n, rank):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_inputs(cfg, dev, with_weights=False)
     # only the experts the sampled tokens use are materialised
-    n = args.cpu_tokens
+    n = args.ref_tokens
     rows = list(range(min(n, cfg.T)))
     used = sorted(set(int(e) for e in inp["topk_idx"][rows].cpu().numpy().ravel() if e >= 0))
     inp.update(W.make_weights(cfg, dev, experts=used))
@@ -390,7 +390,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="flash", choices=list(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-tokens", type=int, default=4)
+    ap.add_argument("--cpu-tokens", type=int, default=16,
+                    help="tokens of the workload the oracle baseline times once (about 10 s of host work)")
+    ap.add_argument("--ref-tokens", type=int, default=4,
+                    help="--impl reference: tokens of the workload the oracle processes per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,
                     help="1: gather + L1 + L2 as one lag-ordered persistent launch; default: the library's")
