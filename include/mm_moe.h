@@ -54,7 +54,7 @@
  *            mm_moe_prepare_weights (sizes from mm_moe_weight_sf_size)
  *   out      bf16 [T, H]
  * Shape limits: H % 128 == 0, I % 128 == 0, 1 <= K <= 16, K <= E <= 1024,
- * T >= 0 (T = 0 is a no-op).  w1/w2 must be 32-byte aligned, x/workspace
+ * T >= 0 (T = 0 computes nothing and only clears the workspace's status word).  w1/w2 must be 32-byte aligned, x/workspace
  * 256-byte aligned.
  */
 #ifndef MM_MOE_H_

@@ -258,7 +258,13 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
-  if (T == 0) return MM_MOE_OK;
+  if (T == 0) {
+    // nothing to compute; leave a clean status word for mm_moe_sync_status
+    if (workspace && workspace_bytes >= 16 && aligned(workspace, 256))
+      return cudaMemsetAsync(workspace, 0, 16, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MM_MOE_OK
+                                                                                              : MM_MOE_ERR_CUDA;
+    return MM_MOE_OK;
+  }
   if (!x || !x_sf || !topk_idx || !topk_w || !w1 || !w1_sfp || !w2 || !w2_sfp || !out || !workspace)
     return MM_MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(x_sf, 4) || !aligned(w1, 32) || !aligned(w2, 32) || !aligned(out, 16) ||
