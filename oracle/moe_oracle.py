@@ -247,13 +247,18 @@ def forward_pair(x_hat: np.ndarray, w: float, W1: np.ndarray, W2: np.ndarray, I:
 
 def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.ndarray,
             topk_w: np.ndarray, experts: ExpertFn, H: int, I: int, E: int, variant: str,
-            keep_intermediate: bool = False):
+            keep_intermediate: bool = False, partials_bf16: bool = False):
     """Output rows out[t, :] (bf16 values as fp64) for the tokens in `rows`.
 
     Each (token, slot) pair is computed independently (forward_pair); the pairs
     are visited expert by expert only so that each expert is decoded once, which
     does not change any value.  Returns (out [len(rows), H], inter) where inter
-    maps (t, k) -> (codes, sf) of the requantised intermediate when asked."""
+    maps (t, k) -> (codes, sf) of the requantised intermediate when asked.
+
+    partials_bf16: the combine of the pages' own design ("MEGAMOE_SM90_DESIGN.md"
+    §11, L2 BF16 epilogue + combine): every per-slot output y_k is cast to bf16
+    (round to nearest even) before the top-k sum, which then runs in fixed k order
+    and is cast to bf16 once more.  Read here as bf16_rne of the fp64 y_k."""
     rows = [int(t) for t in rows]
     K = topk_idx.shape[1]
     pairs: Dict[int, list] = {}
@@ -279,6 +284,6 @@ def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.n
         acc = np.zeros(H, dtype=np.float64)
         for k in range(K):                           # fixed k order
             if (t, k) in y:
-                acc = acc + y[(t, k)]
+                acc = acc + (bf16_rne(y[(t, k)]) if partials_bf16 else y[(t, k)])
         out[i] = bf16_rne(acc)
     return out, inter

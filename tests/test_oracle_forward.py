@@ -52,7 +52,7 @@ def _requant_torch(a32: torch.Tensor, variant: str) -> torch.Tensor:
     return (q.double() * s.double()[..., None]).reshape(a32.shape)
 
 
-def brute_force(cfg, inp):
+def brute_force(cfg, inp, partials_bf16=False):
     x, W1, W2 = _deq_all(cfg, inp)
     idx, w = inp["topk_idx"].long(), inp["topk_w"].double()
     T, I = cfg.T, cfg.I
@@ -65,16 +65,18 @@ def brute_force(cfg, inp):
         a = torch.nn.functional.silu(g) * u * w[:, k:k + 1]
         ah = _requant_torch(a.float(), cfg.variant)
         y = torch.einsum("thi,ti->th", W2[e], ah)
+        if partials_bf16:                  # library cast, round to nearest even
+            y = y.to(torch.bfloat16).double()
         out += torch.where(valid[:, None], y, torch.zeros_like(y))
     return out
 
 
-def run_oracle(cfg, inp, rows=None):
+def run_oracle(cfg, inp, rows=None, partials_bf16=False):
     npi = W.to_numpy(inp)
     rows = np.arange(cfg.T) if rows is None else rows
     out, inter = O.forward(rows, npi["x"], npi["x_sf"], npi["topk_idx"], npi["topk_w"],
                            O.expert_from_arrays(npi["w1"], npi["w1_sf"], npi["w2"], npi["w2_sf"]),
-                           cfg.H, cfg.I, cfg.E, cfg.variant, keep_intermediate=True)
+                           cfg.H, cfg.I, cfg.E, cfg.variant, keep_intermediate=True, partials_bf16=partials_bf16)
     return out, inter
 
 
@@ -87,6 +89,28 @@ def test_oracle_matches_dense_brute_force(cfg):
     exact = np.mean(out == ref)
     assert exact > 0.999, exact
     assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
+
+
+@pytest.mark.parametrize("cfg", [TINY_MX.with_(seed=5, K=3), TINY_F8], ids=["mx_k3", "f8"])
+def test_oracle_bf16_partials_match_dense_brute_force(cfg):
+    """The bf16-partials combine (each slot's output cast to bf16 before the sum)
+    against the independent brute force with torch's bf16 cast."""
+    inp = W.make_inputs(cfg, "cpu")
+    out, _ = run_oracle(cfg, inp, partials_bf16=True)
+    ref = O.bf16_rne(brute_force(cfg, inp, partials_bf16=True).numpy())
+    assert np.mean(out == ref) > 0.999
+    assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
+    full, _ = run_oracle(cfg, inp)
+    assert not np.array_equal(out, full)     # the extra rounding is visible with K > 1
+
+
+def test_oracle_bf16_partials_single_slot_equal_fp32_partials():
+    """With one slot per token the sum has one term: bf16(bf16(y)) = bf16(y)."""
+    cfg = TINY_MX.with_(K=1, seed=9)
+    inp = W.make_inputs(cfg, "cpu")
+    a, _ = run_oracle(cfg, inp, partials_bf16=True)
+    b, _ = run_oracle(cfg, inp)
+    assert np.array_equal(a, b)
 
 
 def test_oracle_identity_weights_closed_form():
