@@ -132,8 +132,9 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ accounting
-def workload_accounting(cfg, idx: np.ndarray):
-    """Algorithmic bytes / FLOPs of one step and of the two GEMM kernels."""
+def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4):
+    """Algorithmic bytes / FLOPs of one step and of the two GEMM kernels
+    (part_elem: bytes of one L2 partial, 4 for fp32, 2 for bf16)."""
     T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
     valid = (idx >= 0) & (idx < E)
     touched = int(np.unique(idx[valid]).size)
@@ -151,7 +152,7 @@ def workload_accounting(cfg, idx: np.ndarray):
     step_bytes = touched * (w1_b + w2_b) + T * x_b + T * K * 8 + T * H * 2
     flops = 6.0 * pairs * H * I
     l1_bytes = touched * w1_b + pairs * x_b + pairs * a_b
-    l2_bytes = touched * w2_b + pairs * a_b + pairs * H * 4
+    l2_bytes = touched * w2_b + pairs * a_b + pairs * H * part_elem
     gather_bytes = pairs * x_b * 2           # read the token's row, write its pool row
     return {"touched_experts": touched, "pairs": pairs, "step_bytes": step_bytes, "flops": flops,
             "gather_bytes": gather_bytes,
@@ -188,6 +189,7 @@ def run_ours(args, ws_n, rank, local):
     opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
     if args.fused is not None:
         opt.fused = args.fused
+    opt.partials_bf16 = 1 if args.partials == "bf16" else 0
     fused = bool(opt.fused) and cfg.variant == "mx"
     w1p, w2p = M.prepare_weights(inp["w1_sf"], inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
     ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt, dev)
@@ -222,7 +224,7 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
-        o = M.options(opt.variant, fused=opt.fused)
+        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16)
         o.timing_events = ctypes.cast(arrays[i], ctypes.c_void_p)
         fwd(o)
     torch.cuda.synchronize()
@@ -260,7 +262,7 @@ def run_ours(args, ws_n, rank, local):
     clk = clocks.stop()
 
     idx_np = inp["topk_idx"].cpu().numpy()
-    acc = workload_accounting(cfg, idx_np)
+    acc = workload_accounting(cfg, idx_np, 2 if opt.partials_bf16 else 4)
     pk, pk_src = peaks()
     hbm = float(pk["hbm_gbs"])
     fp8 = float(pk["bf16_tflops"]) * FP8_OVER_BF16
@@ -298,7 +300,7 @@ def run_ours(args, ws_n, rank, local):
                    "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K, "seed": cfg.seed,
                    "l2_policy": "L2 flushed (512 MiB write) before every timed step; weights 3+ GB >> L2",
                    "parallelism": f"replicas x{ws_n} (no data-path collective)",
-                   "fused_stream": fused},
+                   "fused_stream": fused, "partials": args.partials},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
         "path_roofline": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (step_ms * 1e-3),
                           "bytes": acc["step_bytes"], "flops": acc["flops"],
@@ -311,7 +313,7 @@ def run_ours(args, ws_n, rank, local):
         "roofline": {"kernel": ("gemm_mx_kernel (fused gather + L1 + L2 stream)" if fused else
                                 f"gemm_{'mx' if cfg.variant == 'mx' else 'f8'}_kernel ({dom.upper()} grouped GEMM)"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": kernel_traffic(dom, cfg.name),
+                     "frac": achieved / hbm, "traffic": kernel_traffic(dom, cfg.name if args.partials == "fp32" else f"{cfg.name}:bf16-partials"),
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "peak_source": f"{pk_src} hbm_gbs (STREAM-style copy)"},
         "e2e": {"value": ws_n * cfg.T / (e2e_step_ms * 1e-3), "unit": "tokens/s",
@@ -390,6 +392,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="flash", choices=list(W.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
+                    help="L2 partials: fp32 (default) or cast to bf16 before the combine")
     ap.add_argument("--cpu-tokens", type=int, default=16,
                     help="tokens of the workload the oracle baseline times once (about 10 s of host work)")
     ap.add_argument("--ref-tokens", type=int, default=4,

@@ -104,7 +104,11 @@ typedef struct mm_moe_options {
                                    tile once for both (TMA multicast); 0 or 1 = one CTA per tile group
                                    (default: the pair's lockstep costs more than the halved token reads
                                    save on GB300).  The results are identical either way. */
-  int reserved[6];
+  int partials_bf16;            /* 0 (default): the L2 epilogue writes fp32 partials [K, T, H] and the
+                                   combine sums them in fixed k order; 1: the partials are cast to
+                                   bf16 (round to nearest even) first, halving their traffic (the
+                                   L2 BF16 epilogue + combine of the pages' SM90 design) */
+  int reserved[5];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

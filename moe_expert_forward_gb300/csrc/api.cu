@@ -11,7 +11,7 @@ namespace mm {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags) {
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags, int partials_bf16) {
   Layout L{};
   L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = kBT;
   const int64_t pairs = static_cast<int64_t>(T) * K;
@@ -36,7 +36,8 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.pool2_sf = o;
   o = align_up(o + (variant == MM_MOE_VARIANT_MX ? static_cast<size_t>(L.P) * I / 32
                                                  : static_cast<size_t>(L.P) * (I / 128) * sizeof(float)), 1024);
-  L.part = o; o = align_up(o + static_cast<size_t>(pairs) * H * sizeof(float), 1024);
+  L.part_elem = partials_bf16 ? 2 : 4;
+  L.part = o; o = align_up(o + static_cast<size_t>(pairs) * H * L.part_elem, 1024);
   L.dbg = o;
   L.dbg_bytes = (debug_flags & 1) ? static_cast<size_t>(L.P) * 2 * I * sizeof(float) : 0;
   o = align_up(o + L.dbg_bytes, 1024);
@@ -189,7 +190,7 @@ int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E,
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
-  *bytes = make_layout(T, H, I, E, K, o.variant, o.debug_flags).total;
+  *bytes = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16).total;
   return MM_MOE_OK;
 }
 
@@ -275,7 +276,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (o.variant == MM_MOE_VARIANT_F8 && (H / 128 > kF8MaxKB || I / 128 > kF8MaxKB)) return MM_MOE_ERR_UNSUPPORTED;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
   const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
   if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
   const WsPtrs W = ws_ptrs(workspace, L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -339,7 +340,7 @@ int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T,
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!workspace) return MM_MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
   const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -358,7 +359,7 @@ int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, i
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!workspace || !codes || !sf || rows < 0) return MM_MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
   if (rows > L.P) return MM_MOE_ERR_INVALID_ARG;
   if (rows == 0) return MM_MOE_OK;
   const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
@@ -371,7 +372,7 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!ptr || !bytes) return MM_MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags);
+  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
   const size_t offs[13] = {L.status, L.cnt, L.blk_off, L.slot, L.src, L.pool_x, L.pool_x_sf, L.pool2, L.pool2_sf,
                            L.part, L.dbg, L.prof, L.total};
   if (region < 0 || region > 11) return MM_MOE_ERR_INVALID_ARG;
@@ -383,7 +384,7 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
   else if (region == 2) n = sizeof(int) * (E + 1);
   else if (region == 3) n = sizeof(int) * static_cast<size_t>(T) * K;
   else if (region == 4) n = sizeof(int) * static_cast<size_t>(L.P);
-  else if (region == 9) n = sizeof(float) * static_cast<size_t>(T) * K * H;
+  else if (region == 9) n = static_cast<size_t>(L.part_elem) * T * K * H;
   else n = offs[region + 1] - offs[region];
   *ptr = static_cast<uint8_t*>(const_cast<void*>(workspace)) + offs[region];
   *bytes = n;

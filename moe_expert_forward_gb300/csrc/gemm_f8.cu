@@ -55,7 +55,8 @@ struct Args {
   const float* sx;      // token scales [P, kdim/128]
   uint8_t* out_codes;   // L1: intermediate codes [P, I]
   float* out_sf;        // L1: intermediate scales [P, I/128]
-  float* partials;      // L2: [K, T, H]
+  float* partials;      // L2: [K, T, H] fp32, or bf16 when pbf16
+  int pbf16;
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;   // per-CTA role cycles (debug_flags bit 1) or null
@@ -367,13 +368,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (live && n * kBN + 128 * half < args.H) {
           const int t = s / args.K;
           const int k = s - t * args.K;
-          float4* dst = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(k) * args.T + t) * args.H +
-                                                  n * kBN + 128 * half);
-          // 32-byte stores: half the store instructions of float4
+          const size_t off = (static_cast<size_t>(k) * args.T + t) * args.H + n * kBN + 128 * half;
+          if (args.pbf16) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.partials) + off;
+            st_bf16x32(dst, acc0);
+            st_bf16x32(dst + 32, acc0 + 32);
+            st_bf16x32(dst + 64, acc1);
+            st_bf16x32(dst + 96, acc1 + 32);
+          } else {
+            float* dst = args.partials + off;
+            // 32-byte stores: half the store instructions of float4
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            st_global_v8(reinterpret_cast<float*>(dst) + 8 * i, acc0 + 8 * i);
-            st_global_v8(reinterpret_cast<float*>(dst) + 64 + 8 * i, acc1 + 8 * i);
+            for (int i = 0; i < 8; ++i) {
+              st_global_v8(dst + 8 * i, acc0 + 8 * i);
+              st_global_v8(dst + 64 + 8 * i, acc1 + 8 * i);
+            }
           }
         }
       }
@@ -445,6 +454,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
     a.nblocks = (L.H + kBN - 1) / kBN;
     a.sx = reinterpret_cast<const float*>(W.pool2_sf);
     a.partials = W.part;
+    a.pbf16 = L.part_elem == 2;
     if (encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.w, L.I, static_cast<uint64_t>(L.E) * L.H, L.I, 128,
                        kBN, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;

@@ -106,7 +106,8 @@ struct Args {
   const uint8_t* sfw2;
   uint8_t* pool2;            // intermediate codes [P, I]
   uint8_t* pool2_sf;         // intermediate scale chunks [P/128][I/128][512]
-  float* partials;           // [K, T, H]
+  float* partials;           // [K, T, H] fp32, or bf16 when pbf16
+  int pbf16;                 // partials cast to bf16 (round to nearest even)
   float* dbg;                // raw L1 accumulators [P, 2I] or null
   int* ctr_gather;           // mode 3: rows gathered per pool block
   int* ctr_l1;               // mode 3: L1 epilogue warps finished per pool block
@@ -488,13 +489,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const int k = s - tt * args.K;
         const int col0 = t.n * kBN + 128 * half;
         if (live && col0 < args.H) {
-          float* dst = args.partials + (static_cast<size_t>(k) * args.T + tt) * args.H + col0;
+          const size_t off = (static_cast<size_t>(k) * args.T + tt) * args.H + col0;
+          if (args.pbf16) {
+            __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(args.partials) + off;
+            st_bf16x32(dst, r0);
+            st_bf16x32(dst + 32, r1);
+            st_bf16x32(dst + 64, r2);
+            st_bf16x32(dst + 96, r3);
+          } else {
+            float* dst = args.partials + off;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {   // 32-byte stores of the row's 128 columns
-            st_global_v8(dst + 8 * i, r0 + 8 * i);
-            st_global_v8(dst + 32 + 8 * i, r1 + 8 * i);
-            st_global_v8(dst + 64 + 8 * i, r2 + 8 * i);
-            st_global_v8(dst + 96 + 8 * i, r3 + 8 * i);
+            for (int i = 0; i < 4; ++i) {   // 32-byte stores of the row's 128 columns
+              st_global_v8(dst + 8 * i, r0 + 8 * i);
+              st_global_v8(dst + 32 + 8 * i, r1 + 8 * i);
+              st_global_v8(dst + 64 + 8 * i, r2 + 8 * i);
+              st_global_v8(dst + 96 + 8 * i, r3 + 8 * i);
+            }
           }
         }
       }
@@ -546,6 +556,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.sfw1 = g.w1sfp; a.sfw2 = g.w2sfp;
   a.pool2 = W.pool2; a.pool2_sf = W.pool2_sf;
   a.partials = W.part; a.dbg = g.dbg;
+  a.pbf16 = L.part_elem == 2;
   a.ctr_gather = W.ctr; a.ctr_l1 = W.ctr + L.nblk_cap;
   a.sched = W.ctr + 2 * L.nblk_cap + mode;
   a.status = W.status; a.timeout_ns = g.timeout_ns;

@@ -21,10 +21,11 @@ struct Layout {
   int64_t P;                 // pool row capacity (multiple of BT)
   int64_t nblk_cap;          // P / BT
   int KB1, KB2;              // H/128, I/128
+  int part_elem;             // bytes of one partial: 4 (fp32) or 2 (bf16)
   size_t status, cnt, blk_off, dscr, ctr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
 };
 
-Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0);
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0, int partials_bf16 = 0);
 
 // Device pointers resolved from a workspace.
 struct WsPtrs {

@@ -262,8 +262,13 @@ cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, co
 
 // ----------------------------------------------------------------------------- combine
 // out[t, h] = bf16_rn( sum_{k=0..K-1, slot valid} part[k][t][h] ), summed in k order in fp32.
+// out[t, h] = bf16(sum over k = 0..K-1 of part[k][t][h]), the sum in fp32 in
+// fixed k order; slots with a masked or out-of-range expert are skipped.  Each
+// thread takes 8 consecutive columns of one token.  PartT: float, or bf16 when
+// the L2 epilogue cast its partials.
+template <typename PartT>
 __global__ void __launch_bounds__(256)
-    combine_kernel(const float* __restrict__ part, const int32_t* __restrict__ idx, int T, int K, int E, int H,
+    combine_kernel(const PartT* __restrict__ part, const int32_t* __restrict__ idx, int T, int K, int E, int H,
                    __nv_bfloat16* __restrict__ out) {
   const int64_t groups = static_cast<int64_t>(T) * (H / 8);
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
@@ -274,10 +279,20 @@ __global__ void __launch_bounds__(256)
     for (int k = 0; k < K; ++k) {
       const int e = __ldg(idx + t * K + k);
       if (e < 0 || e >= E) continue;
-      const float4* p = reinterpret_cast<const float4*>(part + ((static_cast<int64_t>(k) * T + t) * H + h));
-      const float4 a = __ldcs(p), b = __ldcs(p + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      const PartT* p = part + ((static_cast<int64_t>(k) * T + t) * H + h);
+      if constexpr (sizeof(PartT) == 4) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(p)), b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      } else {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // bf16 -> fp32 is exact: the bits move up 16 places
+          acc[2 * i] += __uint_as_float(w[i] << 16);
+          acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
+        }
+      }
     }
     uint4 o;
     __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[0], acc[1]);
@@ -299,8 +314,12 @@ cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk
   const int64_t cap = static_cast<int64_t>(dev_info().sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  combine_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(W.part, topk_idx, L.T, L.K, L.E, L.H,
-                                                          static_cast<__nv_bfloat16*>(out));
+  if (L.part_elem == 2)
+    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16*>(W.part), topk_idx, L.T, L.K, L.E, L.H, static_cast<__nv_bfloat16*>(out));
+  else
+    combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(W.part, topk_idx, L.T, L.K, L.E, L.H,
+                                                                   static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 namespace mm {
 
@@ -100,6 +101,31 @@ __device__ __forceinline__ void st_global_v8(float* p, const uint32_t* v) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
                "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
+}
+
+// fp32 bit patterns -> bf16 pairs (round to nearest even), low half = first value
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// 32 fp32 values (bit patterns) -> 32 bf16 at a 32-byte aligned address, two 32-byte stores
+__device__ __forceinline__ void st_bf16x32(__nv_bfloat16* p, const uint32_t* v) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  st_global_v8(reinterpret_cast<float*>(p), w);
+  st_global_v8(reinterpret_cast<float*>(p) + 8, w + 8);
+}
+
+__device__ __forceinline__ void st_bf16x32(__nv_bfloat16* p, const float* v) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  st_global_v8(reinterpret_cast<float*>(p), w);
+  st_global_v8(reinterpret_cast<float*>(p) + 8, w + 8);
 }
 
 // ------------------------------------------------------------------ thread-block clusters
