@@ -230,10 +230,17 @@ def expert_from_arrays(w1, w1_sf, w2, w2_sf) -> ExpertFn:
 
 
 def forward_pair(x_hat: np.ndarray, w: float, W1: np.ndarray, W2: np.ndarray, I: int,
-                 variant: str):
-    """Steps 3-6 for one (token, expert) pair.  Returns (y fp64 [H], codes, sf, a fp64)."""
+                 variant: str, clamp: Optional[float] = None):
+    """Steps 3-6 for one (token, expert) pair.  Returns (y fp64 [H], codes, sf, a fp64).
+
+    clamp: the optional activation clamp of "MEGAMOE_SM90_DESIGN.md" §10 (L1
+    epilogue: SwiGLU + FP8 quantization): gate and up are each limited to
+    [-clamp, clamp] before the SwiGLU."""
     g = W1[:I] @ x_hat
     u = W1[I:] @ x_hat
+    if clamp is not None:
+        g = np.clip(g, -clamp, clamp)
+        u = np.clip(u, -clamp, clamp)
     with np.errstate(over="ignore"):
         a = g / (1.0 + np.exp(-g)) * u * float(np.float32(w))
     a32 = a.astype(np.float32)
@@ -247,7 +254,7 @@ def forward_pair(x_hat: np.ndarray, w: float, W1: np.ndarray, W2: np.ndarray, I:
 
 def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.ndarray,
             topk_w: np.ndarray, experts: ExpertFn, H: int, I: int, E: int, variant: str,
-            keep_intermediate: bool = False, partials_bf16: bool = False):
+            keep_intermediate: bool = False, partials_bf16: bool = False, clamp: Optional[float] = None):
     """Output rows out[t, :] (bf16 values as fp64) for the tokens in `rows`.
 
     Each (token, slot) pair is computed independently (forward_pair); the pairs
@@ -275,7 +282,7 @@ def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.n
         W1 = dequant_weight(w1, w1_sf, variant)
         W2 = dequant_weight(w2, w2_sf, variant)
         for (t, k) in pairs[e]:
-            yk, codes, sf, _ = forward_pair(x_hat[t], topk_w[t, k], W1, W2, I, variant)
+            yk, codes, sf, _ = forward_pair(x_hat[t], topk_w[t, k], W1, W2, I, variant, clamp)
             y[(t, k)] = yk
             if keep_intermediate:
                 inter[(t, k)] = (codes, sf)

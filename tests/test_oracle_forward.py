@@ -52,7 +52,7 @@ def _requant_torch(a32: torch.Tensor, variant: str) -> torch.Tensor:
     return (q.double() * s.double()[..., None]).reshape(a32.shape)
 
 
-def brute_force(cfg, inp, partials_bf16=False):
+def brute_force(cfg, inp, partials_bf16=False, clamp=None):
     x, W1, W2 = _deq_all(cfg, inp)
     idx, w = inp["topk_idx"].long(), inp["topk_w"].double()
     T, I = cfg.T, cfg.I
@@ -62,6 +62,8 @@ def brute_force(cfg, inp, partials_bf16=False):
         e = idx[:, k].clamp(0, cfg.E - 1)
         h = torch.einsum("tnh,th->tn", W1[e], x)
         g, u = h[:, :I], h[:, I:]
+        if clamp is not None:
+            g, u = g.clamp(-clamp, clamp), u.clamp(-clamp, clamp)
         a = torch.nn.functional.silu(g) * u * w[:, k:k + 1]
         ah = _requant_torch(a.float(), cfg.variant)
         y = torch.einsum("thi,ti->th", W2[e], ah)
@@ -71,12 +73,13 @@ def brute_force(cfg, inp, partials_bf16=False):
     return out
 
 
-def run_oracle(cfg, inp, rows=None, partials_bf16=False):
+def run_oracle(cfg, inp, rows=None, partials_bf16=False, clamp=None):
     npi = W.to_numpy(inp)
     rows = np.arange(cfg.T) if rows is None else rows
     out, inter = O.forward(rows, npi["x"], npi["x_sf"], npi["topk_idx"], npi["topk_w"],
                            O.expert_from_arrays(npi["w1"], npi["w1_sf"], npi["w2"], npi["w2_sf"]),
-                           cfg.H, cfg.I, cfg.E, cfg.variant, keep_intermediate=True, partials_bf16=partials_bf16)
+                           cfg.H, cfg.I, cfg.E, cfg.variant, keep_intermediate=True, partials_bf16=partials_bf16,
+                           clamp=clamp)
     return out, inter
 
 
@@ -102,6 +105,21 @@ def test_oracle_bf16_partials_match_dense_brute_force(cfg):
     assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
     full, _ = run_oracle(cfg, inp)
     assert not np.array_equal(out, full)     # the extra rounding is visible with K > 1
+
+
+@pytest.mark.parametrize("cfg", [TINY_MX.with_(seed=6, K=3), TINY_F8], ids=["mx_k3", "f8"])
+def test_oracle_activation_clamp_matches_dense_brute_force(cfg):
+    """Gate and up clamped to [-c, c] before the SwiGLU, with c small enough
+    that most pre-activations are clamped; a huge c changes nothing."""
+    inp = W.make_inputs(cfg, "cpu")
+    out, _ = run_oracle(cfg, inp, clamp=0.05)
+    ref = O.bf16_rne(brute_force(cfg, inp, clamp=0.05).numpy())
+    assert np.mean(out == ref) > 0.999
+    assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
+    free, _ = run_oracle(cfg, inp)
+    assert not np.array_equal(out, free)
+    loose, _ = run_oracle(cfg, inp, clamp=1e30)
+    assert np.array_equal(loose, free)
 
 
 def test_oracle_bf16_partials_single_slot_equal_fp32_partials():
