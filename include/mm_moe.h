@@ -108,7 +108,9 @@ typedef struct mm_moe_options {
                                    combine sums them in fixed k order; 1: the partials are cast to
                                    bf16 (round to nearest even) first, halving their traffic (the
                                    L2 BF16 epilogue + combine of the pages' SM90 design) */
-  int reserved[5];
+  float activation_clamp;       /* > 0: gate and up are each clamped to [-c, c] before the SwiGLU (the
+                                   pages' optional activation clamp); <= 0 (default): no clamp */
+  int reserved[4];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

@@ -38,7 +38,8 @@ class mm_moe_options(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("fused", ctypes.c_int), ("lag_units", ctypes.c_int),
                 ("retain_intermediate", ctypes.c_int), ("wait_timeout_ms", ctypes.c_uint),
                 ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("cta_pairs", ctypes.c_int),
-                ("partials_bf16", ctypes.c_int), ("reserved", ctypes.c_int * 5),
+                ("partials_bf16", ctypes.c_int), ("activation_clamp", ctypes.c_float),
+                ("reserved", ctypes.c_int * 4),
                 ("timing_events", ctypes.c_void_p)]
 
 

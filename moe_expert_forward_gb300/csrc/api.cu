@@ -295,6 +295,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
   const uint64_t timeout_ns = static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull;
+  const float clamp = o.activation_clamp > 0.f ? o.activation_clamp : INFINITY;
   // arrival counters of the fused stream and the tile-group counters of every GEMM launch
   if (e == cudaSuccess)
     e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), s);
@@ -302,7 +303,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 o.cta_pairs == 2};
+                 o.cta_pairs == 2, clamp};
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
@@ -316,7 +317,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,
-                   grid, W.prof};
+                   grid, W.prof, clamp};
     if (e == cudaSuccess) e = launch_gemm_f8_l1(g, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {

@@ -32,9 +32,10 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kThreads = 512;
 constexpr int kLaunchRegs = 128;       // 65536 / 512
-constexpr int kSmallRegs = 56;         // producers, MMA warpgroup
+constexpr int kSmallRegs = 56;         // producers
+constexpr int kMmaRegs = 56;           // MMA warpgroup
 constexpr int kEpiRegs = 200;          // epilogue warpgroups
-static_assert(2 * 128 * kSmallRegs + 2 * 128 * kEpiRegs == kThreads * kLaunchRegs, "register split");
+static_assert(128 * kSmallRegs + 128 * kMmaRegs + 2 * 128 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kBN = 256;
 constexpr int kTokBytes = kBT * kBK;
 constexpr int kWgtBytes = kBN * kBK;
@@ -57,6 +58,7 @@ struct Args {
   float* out_sf;        // L1: intermediate scales [P, I/128]
   float* partials;      // L2: [K, T, H] fp32, or bf16 when pbf16
   int pbf16;
+  float clamp;          // gate and up clamped to [-clamp, clamp] before the SwiGLU (+inf: none)
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;   // per-CTA role cycles (debug_flags bit 1) or null
@@ -103,6 +105,7 @@ __device__ __forceinline__ uint32_t make_idesc() {
 }
 
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
+__device__ __forceinline__ void regs_dec_mma() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kMmaRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
 
 // kProf: record per-role SM cycles into args.prof[blockIdx.x * 8 + i]: 0 MMA
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (wg == 3) {
-    regs_dec();
+    regs_dec_mma();
     // ------------------------------------------------------------------ MMA issuer
     if (warp == 12 && lane == 0) {
       int stage = 0;
@@ -330,6 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long tw2 = kProf ? clock64() : 0;
       if (PHASE == 1) {
         // a = silu(gate) * up * w over this thread's 64 intermediate columns
+        if (args.clamp < INFINITY) {   // the optional activation clamp, a pass of its own
+          const float c = args.clamp;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            acc0[j] = fminf(fmaxf(acc0[j], -c), c);
+            acc1[j] = fminf(fmaxf(acc1[j], -c), c);
+          }
+        }
         float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
@@ -433,6 +444,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   a.status = W.status; a.timeout_ns = g.timeout_ns;
   a.prof = g.prof ? g.prof + (PHASE == 2 ? 8 * 1024 : 0) : nullptr;
   a.sw = g.wsf;
+  a.clamp = g.clamp;   // both phases: L1 applies it, L2 ignores it
   const uint8_t* pool;
   int kdim;
   if (PHASE == 1) {

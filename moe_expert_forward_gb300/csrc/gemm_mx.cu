@@ -108,6 +108,7 @@ struct Args {
   uint8_t* pool2_sf;         // intermediate scale chunks [P/128][I/128][512]
   float* partials;           // [K, T, H] fp32, or bf16 when pbf16
   int pbf16;                 // partials cast to bf16 (round to nearest even)
+  float clamp;               // gate and up clamped to [-clamp, clamp] before the SwiGLU (+inf: none)
   float* dbg;                // raw L1 accumulators [P, 2I] or null
   int* ctr_gather;           // mode 3: rows gathered per pool block
   int* ctr_l1;               // mode 3: L1 epilogue warps finished per pool block
@@ -149,8 +150,8 @@ __device__ __forceinline__ uint32_t make_idesc(int sf_id) {
 }
 
 // SwiGLU x top-k weight and UE8M0 requant of one 32-column block c of an L1
-// tile for one token row: gate g, up u (fp32 bits, overwritten).
-__device__ __forceinline__ void l1_block(uint32_t (&g)[32], const uint32_t (&u)[32], int c, bool live, float w,
+// tile for one token row: gate g, up u (fp32 bits, both overwritten).
+__device__ __forceinline__ void l1_block(uint32_t (&g)[32], uint32_t (&u)[32], int c, bool live, float w,
                                          size_t row, int n, const Args& args, uint8_t* crow, uint8_t* sfrow) {
   if (!live) return;
   if (args.dbg) {
@@ -161,12 +162,21 @@ __device__ __forceinline__ void l1_block(uint32_t (&g)[32], const uint32_t (&u)[
       drow[args.I + n * 128 + c * 32 + jj] = __uint_as_float(u[jj]);
     }
   }
+  if (args.clamp < INFINITY) {   // the optional activation clamp, a pass of its own
+    const float cl = args.clamp;
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      g[jj] = __float_as_uint(fminf(fmaxf(__uint_as_float(g[jj]), -cl), cl));
+      u[jj] = __float_as_uint(fminf(fmaxf(__uint_as_float(u[jj]), -cl), cl));
+    }
+  }
   float amax = 0.f;
 #pragma unroll
   for (int jj = 0; jj < 32; ++jj) {
     const float gv = __uint_as_float(g[jj]);
+    const float uv = __uint_as_float(u[jj]);
     const float sv = gv * __frcp_rn(1.0f + __expf(-gv));   // silu(g) = g * sigmoid(g)
-    const float av = sv * __uint_as_float(u[jj]) * w;
+    const float av = sv * uv * w;
     g[jj] = __float_as_uint(av);
     amax = fmaxf(amax, fabsf(av));
   }
@@ -557,6 +567,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.pool2 = W.pool2; a.pool2_sf = W.pool2_sf;
   a.partials = W.part; a.dbg = g.dbg;
   a.pbf16 = L.part_elem == 2;
+  a.clamp = g.clamp;
   a.ctr_gather = W.ctr; a.ctr_l1 = W.ctr + L.nblk_cap;
   a.sched = W.ctr + 2 * L.nblk_cap + mode;
   a.status = W.status; a.timeout_ns = g.timeout_ns;

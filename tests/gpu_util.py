@@ -64,13 +64,13 @@ def host_experts(dev_inp: dict):
     return get
 
 
-def oracle_rows(cfg, dev_inp: dict, rows, keep_intermediate=True, partials_bf16=False):
+def oracle_rows(cfg, dev_inp: dict, rows, keep_intermediate=True, partials_bf16=False, clamp=None):
     x = dev_inp["x"].cpu().numpy()
     x_sf = dev_inp["x_sf"].cpu().numpy()
     idx = dev_inp["topk_idx"].cpu().numpy()
     w = dev_inp["topk_w"].cpu().numpy()
     return O.forward(rows, x, x_sf, idx, w, host_experts(dev_inp), cfg.H, cfg.I, cfg.E, cfg.variant,
-                     keep_intermediate=keep_intermediate, partials_bf16=partials_bf16)
+                     keep_intermediate=keep_intermediate, partials_bf16=partials_bf16, clamp=clamp)
 
 
 def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict) -> float:
