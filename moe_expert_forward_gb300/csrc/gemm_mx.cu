@@ -341,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
           if (kProf) w_empty += globaltimer() - t0;
           mbar_arrive_expect_tx(&full[p], bytes);
-          const int kc = kb * kBK;
+          const int kbe = t.rev ? KB - 1 - kb : kb;   // the k-block this stage carries
+          const int kc = kbe * kBK;
           if (!kPair) {
             tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
           } else if (rows >= 64) {
@@ -351,12 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           } else if (rank == 0) {
             tma_load_2d_mc(tk, tt, &full[p], kc, t.b * kBT, 0x3, pol_t);
           }
-          bulk_load(st_, sft + static_cast<size_t>(kb) * kSFChunk, kSFChunk, &full[p]);
+          bulk_load(st_, sft + static_cast<size_t>(kbe) * kSFChunk, kSFChunk, &full[p]);
           if (!t.ghost) {
             const uint64_t pw = t.last ? pol_w : pol_wk;
             if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pw);
             else tma_load_2d(wg, &maps.w2, &full[p], kc, t.e * args.H + t.n * kBN, pw);
-            bulk_load(sw, sfw + static_cast<size_t>(kb) * 2 * kSFChunk, 2 * kSFChunk, &full[p]);
+            bulk_load(sw, sfw + static_cast<size_t>(kbe) * 2 * kSFChunk, 2 * kSFChunk, &full[p]);
           }
         }
         step += KB;

@@ -14,12 +14,16 @@ struct Task {
   int e, n, b, valid;
   bool last;     // the last pool block of its tile group
   bool ghost;    // CTA pairs: tile n does not exist (odd tile count); the CTA only helps load tokens
+  bool rev;      // walk the contraction from its last k-block down (odd blocks of a group)
 };
 
 // Tasks are dealt to the persistent CTAs in tile groups: one weight tile (e, n)
 // of one GEMM together with every pool block of expert e.  A CTA takes a
 // group's blocks back to back, so the second and later blocks of an expert
 // find the tile's weights still in L2 instead of reading them from HBM again.
+// Every other block walks the contraction backwards: it starts with the
+// k-blocks its predecessor loaded last, the ones most likely still in L2 when
+// the 152 CTAs' tiles together are larger than L2.
 // Group order: modes 1/2, expert-major then tile; mode 3, segment u = expert
 // u's NB1 L1 groups followed by expert (u - lag)'s NB2 L2 groups.  The number
 // of groups per segment does not depend on the routing, so a group index
@@ -97,6 +101,7 @@ struct Sched {
     const int rem = cnt[c.t.e] - c.bl * kBT;
     c.t.valid = rem < kBT ? rem : kBT;
     c.t.last = c.bl + 1 == c.nb;
+    c.t.rev = (c.bl & 1) != 0;
   }
   __device__ __forceinline__ int group_blocks(int g) const {
     Task t;
