@@ -110,7 +110,9 @@ typedef struct mm_moe_options {
                                    L2 BF16 epilogue + combine of the pages' SM90 design) */
   float activation_clamp;       /* > 0: gate and up are each clamped to [-c, c] before the SwiGLU (the
                                    pages' optional activation clamp); <= 0 (default): no clamp */
-  int reserved[4];
+  int precise_swiglu;           /* 0 (default): silu(g) = g * rcp.approx(1 + __expf(-g)), the pages'
+                                   fast-math SwiGLU; 1: g / (1 + expf(-g)) with the IEEE division */
+  int reserved[3];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

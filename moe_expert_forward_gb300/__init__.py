@@ -39,7 +39,7 @@ class mm_moe_options(ctypes.Structure):
                 ("retain_intermediate", ctypes.c_int), ("wait_timeout_ms", ctypes.c_uint),
                 ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("cta_pairs", ctypes.c_int),
                 ("partials_bf16", ctypes.c_int), ("activation_clamp", ctypes.c_float),
-                ("reserved", ctypes.c_int * 4),
+                ("precise_swiglu", ctypes.c_int), ("reserved", ctypes.c_int * 3),
                 ("timing_events", ctypes.c_void_p)]
 
 

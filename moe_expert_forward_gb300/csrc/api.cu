@@ -303,7 +303,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 o.cta_pairs == 2, clamp};
+                 o.cta_pairs == 2, clamp, o.precise_swiglu != 0};
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
@@ -317,7 +317,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,
-                   grid, W.prof, clamp};
+                   grid, W.prof, clamp, o.precise_swiglu != 0};
     if (e == cudaSuccess) e = launch_gemm_f8_l1(g, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {

@@ -59,6 +59,7 @@ struct Args {
   float* partials;      // L2: [K, T, H] fp32, or bf16 when pbf16
   int pbf16;
   float clamp;          // gate and up clamped to [-clamp, clamp] before the SwiGLU (+inf: none)
+  int precise;          // SwiGLU with expf and the IEEE division (else the fast-math form)
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;   // per-CTA role cycles (debug_flags bit 1) or null
@@ -112,7 +113,8 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 // issuer span, 1 its waits for a free partial buffer, 2 its waits for data, 3
 // epilogue (warp 4) waits for a partial, 4 promotion, 5 per-task SwiGLU /
 // requant / stores, 6 k-blocks, 7 epilogue span; args.prof[4096 + blockIdx.x]:
-// the epilogue's per-task setup.  A separate instantiation.
+// the epilogue's per-task setup, [5120 + blockIdx.x] the L1 tail's SwiGLU and
+// amax, [6144 + blockIdx.x] its amax rendezvous.  A separate instantiation.
 template <int PHASE, bool kProf>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ TokenMaps tmT, const Args args) {
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ephase = 0;
     uint32_t wphase = 0;
     const long long e_start = kProf ? clock64() : 0;
-    long long e_wait = 0, e_promo = 0, e_tail = 0, e_setup = 0;
+    long long e_wait = 0, e_promo = 0, e_tail = 0, e_setup = 0, e_math = 0, e_rdv = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, n, b, valid;
       decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
@@ -342,20 +344,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         float amax = 0.f;
+        if (args.precise) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float gv = acc0[j];
-          acc0[j] = gv * __frcp_rn(1.0f + __expf(-gv)) * acc1[j] * w;
-          amax = fmaxf(amax, fabsf(acc0[j]));
+          for (int j = 0; j < 64; ++j) {
+            acc0[j] = silu_precise(acc0[j]) * acc1[j] * w;
+            amax = fmaxf(amax, fabsf(acc0[j]));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            acc0[j] = silu_fast(acc0[j]) * acc1[j] * w;
+            amax = fmaxf(amax, fabsf(acc0[j]));
+          }
         }
         // the 128-column requant block spans both halves: exchange row amax
         // one rendezvous per task: the exchange buffer alternates between tasks, and a
         // thread writes it again two tasks later only after everyone passed the next rendezvous
+        const long long tr0 = kProf ? clock64() : 0;
         float* xa = s_amax + (ephase & 1) * 256;
         xa[half * 128 + m] = amax;
         mbar_arrive(epibar);
         if (!mbar_wait(epibar, ephase, st, s_abort, kSiteAmax)) break;
         ephase ^= 1;
+        if (kProf) { e_math += tr0 - tw2; e_rdv += clock64() - tr0; }
         amax = fmaxf(amax, xa[(half ^ 1) * 128 + m]);
         if (live) {
           const float sf = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
@@ -405,6 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       args.prof[blockIdx.x * 8 + 5] = e_tail;
       args.prof[blockIdx.x * 8 + 7] = clock64() - e_start;
       args.prof[4096 + blockIdx.x] = e_setup;   // inside this phase's 8192-entry region
+      args.prof[4096 + 1024 + blockIdx.x] = e_math;
+      args.prof[4096 + 2048 + blockIdx.x] = e_rdv;
     }
   }
 
@@ -445,6 +458,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   a.prof = g.prof ? g.prof + (PHASE == 2 ? 8 * 1024 : 0) : nullptr;
   a.sw = g.wsf;
   a.clamp = g.clamp;   // both phases: L1 applies it, L2 ignores it
+  a.precise = g.precise;
   const uint8_t* pool;
   int kdim;
   if (PHASE == 1) {

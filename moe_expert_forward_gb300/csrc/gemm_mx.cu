@@ -109,6 +109,7 @@ struct Args {
   float* partials;           // [K, T, H] fp32, or bf16 when pbf16
   int pbf16;                 // partials cast to bf16 (round to nearest even)
   float clamp;               // gate and up clamped to [-clamp, clamp] before the SwiGLU (+inf: none)
+  int precise;               // SwiGLU with expf and the IEEE division (else the fast-math form)
   float* dbg;                // raw L1 accumulators [P, 2I] or null
   int* ctr_gather;           // mode 3: rows gathered per pool block
   int* ctr_l1;               // mode 3: L1 epilogue warps finished per pool block
@@ -171,14 +172,20 @@ __device__ __forceinline__ void l1_block(uint32_t (&g)[32], uint32_t (&u)[32], i
     }
   }
   float amax = 0.f;
+  if (args.precise) {
 #pragma unroll
-  for (int jj = 0; jj < 32; ++jj) {
-    const float gv = __uint_as_float(g[jj]);
-    const float uv = __uint_as_float(u[jj]);
-    const float sv = gv * __frcp_rn(1.0f + __expf(-gv));   // silu(g) = g * sigmoid(g)
-    const float av = sv * uv * w;
-    g[jj] = __float_as_uint(av);
-    amax = fmaxf(amax, fabsf(av));
+    for (int jj = 0; jj < 32; ++jj) {
+      const float av = silu_precise(__uint_as_float(g[jj])) * __uint_as_float(u[jj]) * w;
+      g[jj] = __float_as_uint(av);
+      amax = fmaxf(amax, fabsf(av));
+    }
+  } else {
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const float av = silu_fast(__uint_as_float(g[jj])) * __uint_as_float(u[jj]) * w;
+      g[jj] = __float_as_uint(av);
+      amax = fmaxf(amax, fabsf(av));
+    }
   }
   // UE8M0: smallest e with 448 * 2^e >= max(amax, 1e-10)
   const uint32_t bits = __float_as_uint(fmaxf(amax, 1e-10f));
@@ -569,6 +576,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.partials = W.part; a.dbg = g.dbg;
   a.pbf16 = L.part_elem == 2;
   a.clamp = g.clamp;
+  a.precise = g.precise;
   a.ctr_gather = W.ctr; a.ctr_l1 = W.ctr + L.nblk_cap;
   a.sched = W.ctr + 2 * L.nblk_cap + mode;
   a.status = W.status; a.timeout_ns = g.timeout_ns;

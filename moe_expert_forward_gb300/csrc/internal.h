@@ -86,6 +86,7 @@ struct GemmLaunch {
   int grid;
   bool pair;                // run as 2-CTA clusters sharing token tiles (when the device allows)
   float clamp;              // activation clamp of gate and up (+inf: none)
+  int precise;              // SwiGLU with expf and the IEEE division instead of the fast-math form
 };
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
@@ -101,6 +102,7 @@ struct GemmLaunchF8 {
   int grid;
   unsigned long long* prof;  // per-CTA role cycles (debug_flags bit 1) or null
   float clamp;               // activation clamp of gate and up (+inf: none)
+  int precise;               // SwiGLU with expf and the IEEE division instead of the fast-math form
 };
 cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s);
 cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s);

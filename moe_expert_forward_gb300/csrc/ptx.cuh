@@ -374,6 +374,19 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo,
 }
 
 // fp32 pair -> two e4m3 codes, round to nearest even, saturating; lo goes to the low byte.
+// Approximate reciprocal (rcp.approx.ftz.f32, within about one ulp): the fast
+// reciprocal of the fast-math SwiGLU.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// silu(g) = g * sigmoid(g): the fast-math form (__expf and the approximate
+// reciprocal) or, when `precise`, expf and the IEEE division.
+__device__ __forceinline__ float silu_fast(float g) { return g * rcp_approx(1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_precise(float g) { return __fdiv_rn(g, 1.0f + expf(-g)); }
+
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));

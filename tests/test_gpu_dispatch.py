@@ -95,3 +95,31 @@ def test_dispatch_skewed_all_one_expert(M):
     cnt, blk, slot, src, st = _dispatch(M, idx, E, 128)
     ref = O.route(idx, E, 128)
     assert np.array_equal(slot, ref["slot"]) and list(cnt) == [0, 0, T]
+
+
+@pytest.mark.parametrize("T", [512, 513])
+def test_dispatch_single_cta_boundary(M, T):
+    """4096 and 4104 pairs: the last full CTA chunk and one more CTA with a
+    ragged 8-pair chunk; both give the oracle's routing."""
+    rng = np.random.default_rng(7 + T)
+    E, K = 96, 8
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[rng.random(idx.shape) < 0.03] = -1
+    cnt, blk, slot, src, st = _dispatch(M, idx, E, 128)
+    ref = O.route(idx, E, 128)
+    assert st == 0
+    assert np.array_equal(cnt, ref["cnt"]) and np.array_equal(blk, ref["blk_off"])
+    assert np.array_equal(slot, ref["slot"])
+    assert np.array_equal(src[:len(ref["src"])], ref["src"])
+
+
+def test_dispatch_flags_out_of_range_experts_many_ctas(M):
+    """An out-of-range index in the middle CTA of a 12-CTA dispatch is flagged."""
+    rng = np.random.default_rng(11)
+    T, K, E = 3000, 2, 50
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[1234, 1] = E + 3
+    cnt, blk, slot, src, st = _dispatch(M, idx, E, 64)
+    ref = O.route(idx, E, 64)
+    assert st == M.MM_MOE_ERR_BAD_ROUTING
+    assert np.array_equal(slot, ref["slot"]) and np.array_equal(cnt, ref["cnt"])
