@@ -132,9 +132,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ accounting
-def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4):
+def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4, x_bf16: bool = False):
     """Algorithmic bytes / FLOPs of one step and of the two GEMM kernels
-    (part_elem: bytes of one L2 partial, 4 for fp32, 2 for bf16)."""
+    (part_elem: bytes of one L2 partial, 4 for fp32, 2 for bf16; x_bf16: the
+    caller's x is bf16 and the gather quantises it)."""
     T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
     valid = (idx >= 0) & (idx < E)
     touched = int(np.unique(idx[valid]).size)
@@ -149,11 +150,12 @@ def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4):
         w2_b = H * I + (H // 128) * (I // 128) * 4
         x_b = H + (H // 128) * 4
         a_b = I + (I // 128) * 4
-    step_bytes = touched * (w1_b + w2_b) + T * x_b + T * K * 8 + T * H * 2
+    x_in = 2 * H if x_bf16 else x_b          # the caller's row of x
+    step_bytes = touched * (w1_b + w2_b) + T * x_in + T * K * 8 + T * H * 2
     flops = 6.0 * pairs * H * I
     l1_bytes = touched * w1_b + pairs * x_b + pairs * a_b
     l2_bytes = touched * w2_b + pairs * a_b + pairs * H * part_elem
-    gather_bytes = pairs * x_b * 2           # read the token's row, write its pool row
+    gather_bytes = pairs * (x_in + x_b)      # read the token's row, write its pool row
     return {"touched_experts": touched, "pairs": pairs, "step_bytes": step_bytes, "flops": flops,
             "gather_bytes": gather_bytes,
             "l1_bytes": l1_bytes, "l2_bytes": l2_bytes, "l1_flops": 4.0 * pairs * H * I,
@@ -190,6 +192,10 @@ def run_ours(args, ws_n, rank, local):
     if args.fused is not None:
         opt.fused = args.fused
     opt.partials_bf16 = 1 if args.partials == "bf16" else 0
+    if args.x == "bf16":
+        # bf16 activations: the gather quantises each row (x_sf is not read)
+        inp["x"], inp["x_sf"] = W.make_x_bf16(cfg, dev), None
+        opt.x_bf16 = 1
     fused = bool(opt.fused) and cfg.variant == "mx"
     w1p, w2p = M.prepare_weights(inp["w1_sf"], inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
     ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt, dev)
@@ -224,7 +230,7 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
-        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16)
+        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16, x_bf16=opt.x_bf16)
         o.timing_events = ctypes.cast(arrays[i], ctypes.c_void_p)
         fwd(o)
     torch.cuda.synchronize()
@@ -237,7 +243,7 @@ def run_ours(args, ws_n, rank, local):
     step_ms = max_over_ranks(step_ms_local, ws_n)
 
     # end to end: pinned host inputs -> device, forward, output -> pinned host, every step
-    host = {k: inp[k].cpu().pin_memory() for k in ("x", "x_sf", "topk_idx", "topk_w")}
+    host = {k: inp[k].cpu().pin_memory() for k in ("x", "x_sf", "topk_idx", "topk_w") if inp[k] is not None}
     dbuf = {k: torch.empty_like(inp[k]) for k in host}
     hout = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -249,7 +255,7 @@ def run_ours(args, ws_n, rank, local):
         a.record()
         for k in host:
             dbuf[k].copy_(host[k], non_blocking=True)
-        fwd(opt, dbuf["x"], dbuf["x_sf"], dbuf["topk_idx"], dbuf["topk_w"])
+        fwd(opt, dbuf["x"], dbuf.get("x_sf"), dbuf["topk_idx"], dbuf["topk_w"])
         hout.copy_(out, non_blocking=True)
         b.record()
         b.synchronize()
@@ -262,7 +268,7 @@ def run_ours(args, ws_n, rank, local):
     clk = clocks.stop()
 
     idx_np = inp["topk_idx"].cpu().numpy()
-    acc = workload_accounting(cfg, idx_np, 2 if opt.partials_bf16 else 4)
+    acc = workload_accounting(cfg, idx_np, 2 if opt.partials_bf16 else 4, bool(opt.x_bf16))
     pk, pk_src = peaks()
     hbm = float(pk["hbm_gbs"])
     fp8 = float(pk["bf16_tflops"]) * FP8_OVER_BF16
@@ -300,7 +306,7 @@ def run_ours(args, ws_n, rank, local):
                    "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K, "seed": cfg.seed,
                    "l2_policy": "L2 flushed (512 MiB write) before every timed step; weights 3+ GB >> L2",
                    "parallelism": f"replicas x{ws_n} (no data-path collective)",
-                   "fused_stream": fused, "partials": args.partials},
+                   "fused_stream": fused, "partials": args.partials, "x": args.x},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
         "path_roofline": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (step_ms * 1e-3),
                           "bytes": acc["step_bytes"], "flops": acc["flops"],
@@ -329,8 +335,9 @@ def run_ours(args, ws_n, rank, local):
 # ------------------------------------------------------------------ oracle (CPU) runs
 def oracle_tokens(cfg, inp, rows):
     import oracle as O
-    x = inp["x"][rows].cpu().numpy()
-    x_sf = inp["x_sf"][rows].cpu().numpy()
+    bf16_x = inp["x_sf"] is None             # the layer quantises bf16 rows first: the oracle does too
+    x = inp["x"][rows].float().cpu().numpy() if bf16_x else inp["x"][rows].cpu().numpy()
+    x_sf = None if bf16_x else inp["x_sf"][rows].cpu().numpy()
     idx = inp["topk_idx"][rows].cpu().numpy()
     w = inp["topk_w"][rows].cpu().numpy()
     cache = {}
@@ -343,6 +350,8 @@ def oracle_tokens(cfg, inp, rows):
     for e in np.unique(idx[idx >= 0]):
         experts(int(e))
     t0 = time.perf_counter()
+    if bf16_x:
+        x, x_sf = O.quantise_x(x, cfg.variant)
     O.forward(range(len(rows)), x, x_sf, idx, w, experts, cfg.H, cfg.I, cfg.E, cfg.variant)
     return time.perf_counter() - t0
 
@@ -361,6 +370,8 @@ def run_reference(args, ws_n, rank):
         return None
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_inputs(cfg, dev, with_weights=False)
+    if args.x == "bf16":
+        inp["x"], inp["x_sf"] = W.make_x_bf16(cfg, dev), None
     # only the experts the sampled tokens use are materialised
     n = args.ref_tokens
     rows = list(range(min(n, cfg.T)))
@@ -379,7 +390,7 @@ def run_reference(args, ws_n, rank):
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded workload generator)",
             "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.K}",
-                       "sample_tokens": len(rows)},
+                       "sample_tokens": len(rows), "x": args.x},
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"first {len(rows)} tokens per step ({len(rows) * cfg.K} pairs)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -394,6 +405,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
                     help="L2 partials: fp32 (default) or cast to bf16 before the combine")
+    ap.add_argument("--x", default="fp8", choices=["fp8", "bf16"],
+                    help="activations: fp8 codes + scales (default) or bf16, quantised inside the gather")
     ap.add_argument("--cpu-tokens", type=int, default=16,
                     help="tokens of the workload the oracle baseline times once (about 10 s of host work)")
     ap.add_argument("--ref-tokens", type=int, default=4,

@@ -112,7 +112,13 @@ typedef struct mm_moe_options {
                                    pages' optional activation clamp); <= 0 (default): no clamp */
   int precise_swiglu;           /* 0 (default): silu(g) = g * rcp.approx(1 + __expf(-g)), the pages'
                                    fast-math SwiGLU; 1: g / (1 + expf(-g)) with the IEEE division */
-  int reserved[3];
+  int x_bf16;                   /* 0 (default): x holds e4m3 codes and x_sf their scales; 1: x is bf16
+                                   [T, H] (row-major, 16-byte aligned), x_sf is ignored (may be NULL),
+                                   and the gather quantises each row on its way into the pool with
+                                   the variant's rule (MX: UE8M0 per 32, 448 * 2^e >= amax; F8: fp32
+                                   max(amax, 1e-10) / 448 per 128).  Non-finite inputs give
+                                   unspecified codes. */
+  int reserved[2];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

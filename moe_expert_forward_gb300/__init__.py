@@ -39,7 +39,7 @@ class mm_moe_options(ctypes.Structure):
                 ("retain_intermediate", ctypes.c_int), ("wait_timeout_ms", ctypes.c_uint),
                 ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("cta_pairs", ctypes.c_int),
                 ("partials_bf16", ctypes.c_int), ("activation_clamp", ctypes.c_float),
-                ("precise_swiglu", ctypes.c_int), ("reserved", ctypes.c_int * 3),
+                ("precise_swiglu", ctypes.c_int), ("x_bf16", ctypes.c_int), ("reserved", ctypes.c_int * 2),
                 ("timing_events", ctypes.c_void_p)]
 
 
@@ -254,8 +254,12 @@ def forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, H, I, E, wor
     T, K = topk_idx.shape
     opt = opt or options()
     need = _input_bytes(opt.variant, T, H, I, E, K)
+    if opt.x_bf16:
+        need["x"] = 2 * T * H          # bf16 rows; the gather quantises them, x_sf is not read
     for name, t in (("x", x), ("x_sf", x_sf), ("topk_idx", topk_idx), ("topk_w", topk_w), ("w1", w1), ("w2", w2),
                     ("out", out)):
+        if name == "x_sf" and opt.x_bf16:
+            continue
         if T > 0 or name in ("w1", "w2"):
             _need(t, need[name], name, "forward")
     n1, n2 = mm_moe_weight_sf_size(opt, H, I, E)

@@ -266,9 +266,9 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
                                                                                               : MM_MOE_ERR_CUDA;
     return MM_MOE_OK;
   }
-  if (!x || !x_sf || !topk_idx || !topk_w || !w1 || !w1_sfp || !w2 || !w2_sfp || !out || !workspace)
+  if (!x || (!x_sf && !o.x_bf16) || !topk_idx || !topk_w || !w1 || !w1_sfp || !w2 || !w2_sfp || !out || !workspace)
     return MM_MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(x_sf, 4) || !aligned(w1, 32) || !aligned(w2, 32) || !aligned(out, 16) ||
+  if (!aligned(x, 16) || (!o.x_bf16 && !aligned(x_sf, 4)) || !aligned(w1, 32) || !aligned(w2, 32) || !aligned(out, 16) ||
       !aligned(workspace, 256) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
     return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
@@ -291,7 +291,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, W.dscr,
                         static_cast<int64_t>(kDispatchMaxCtas) * E, s);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess && !fused) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, s);
+  if (e == cudaSuccess && !fused) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
   const uint64_t timeout_ns = static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull;
@@ -302,7 +302,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (o.variant == MM_MOE_VARIANT_MX) {
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
-                 static_cast<const uint8_t*>(x), x_sf, topk_w, W.dbg, W.prof, timeout_ns, grid,
+                 static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
                  o.cta_pairs == 2, clamp, o.precise_swiglu != 0};
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch

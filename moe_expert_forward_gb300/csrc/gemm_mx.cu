@@ -50,6 +50,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "sched.cuh"
 
 namespace mm {
@@ -98,8 +99,9 @@ struct Args {
   const int* blk_off;
   const int* src;
   const float* topk_w;
-  const uint8_t* x;          // mode 3 gather: activations [T, H] and scales [T, H/32]
+  const uint8_t* x;          // mode 3 gather: activations [T, H] and scales [T, H/32], or bf16 [T, H]
   const uint8_t* x_sf;
+  int x_bf16;                // the gather quantises bf16 rows (x_sf unused)
   uint8_t* pool_x;           // [P, H]
   uint8_t* pool_x_sf;        // chunks [P/128][H/128][512]
   const uint8_t* sfw1;       // prepared weight scale chunks (two per tile and k-block)
@@ -187,12 +189,8 @@ __device__ __forceinline__ void l1_block(uint32_t (&g)[32], uint32_t (&u)[32], i
       amax = fmaxf(amax, fabsf(av));
     }
   }
-  // UE8M0: smallest e with 448 * 2^e >= max(amax, 1e-10)
-  const uint32_t bits = __float_as_uint(fmaxf(amax, 1e-10f));
-  const int ex = static_cast<int>((bits >> 23) & 0xFF) - 126;
-  int ee = ex - 9 + ((bits & 0x7FFFFF) > 0x600000 ? 1 : 0);
-  ee = ee < -127 ? -127 : (ee > 126 ? 126 : ee);
-  const float scale = __uint_as_float(static_cast<uint32_t>(127 - ee) << 23);
+  const int ee = ue8m0_exponent_e4m3(amax);   // smallest e with 448 * 2^e >= max(amax, 1e-10)
+  const float scale = exp2_neg(ee);
   uint32_t packed[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -220,6 +218,18 @@ __device__ __forceinline__ void gather_rows(const Args& args, const int* s_blk, 
     for (int r = gw; r < valid; r += kGatherWarps) {
       const size_t row = static_cast<size_t>(b) * kBT + r;
       const int64_t tok = __ldg(args.src + row) / args.K;
+      if (args.x_bf16) {
+        const __nv_bfloat16* brow = reinterpret_cast<const __nv_bfloat16*>(args.x) + tok * args.H;
+        uint8_t* chunk0 = args.pool_x_sf + static_cast<size_t>(b) * KBx * kSFChunk + (r & 31) * 16 + (r >> 5) * 4;
+        uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
+        quant_row_mx_bf16(brow, args.H, lane, [&](int j, const uint4 (&c)[2], uint8_t sfb, bool) {
+          drow[2 * j] = c[0];
+          drow[2 * j + 1] = c[1];
+          chunk0[(j >> 2) * kSFChunk + (j & 3)] = sfb;
+        });
+        ++done;
+        continue;
+      }
       const uint4* srow = reinterpret_cast<const uint4*>(args.x + tok * args.H);
       uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
       for (int i = lane; i < args.H / 16; i += 32) drow[i] = __ldg(srow + i);
@@ -569,7 +579,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.lag = lag < 0 ? 0 : (lag > kMaxLag ? kMaxLag : lag);
   a.l1_extra = l1_extra;
   a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;
-  a.x = g.x; a.x_sf = static_cast<const uint8_t*>(g.x_sf);
+  a.x = g.x; a.x_sf = static_cast<const uint8_t*>(g.x_sf); a.x_bf16 = g.x_bf16 ? 1 : 0;
   a.pool_x = W.pool_x; a.pool_x_sf = W.pool_x_sf;
   a.sfw1 = g.w1sfp; a.sfw2 = g.w2sfp;
   a.pool2 = W.pool2; a.pool2_sf = W.pool2_sf;

@@ -61,7 +61,8 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int bl
 constexpr int kF8MaxKB = 64;             // F8 variant: H and I at most 64 x 128
 constexpr int kSchedCounters = 4;        // tile-group counters after the arrival counters, one per GEMM mode
 constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA counts [CTAs][E]
-cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
+// x_bf16: x is bf16 [T, H] and each row is quantised on its way into the pool
+cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf, bool x_bf16,
                           cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out,
                            cudaStream_t s);
@@ -79,6 +80,7 @@ struct GemmLaunch {
   const uint8_t* w2sfp;
   const uint8_t* x;          // activations and scales (in-kernel gather of the fused stream)
   const void* x_sf;
+  bool x_bf16;               // x is bf16 [T, H]: the gather quantises (x_sf unused)
   const float* topk_w;
   float* dbg;               // L1 raw accumulators (debug_flags bit 0) or null
   unsigned long long* prof; // per-CTA role timings (debug_flags bit 1) or null

@@ -4,6 +4,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace mm {
 
@@ -218,45 +219,115 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int bl
 }
 
 // ----------------------------------------------------------------------------- gather
-// One warp per pool row: copies the token's H code bytes and its scales.  MX
-// scales go to the 512-byte chunk layout the MMA consumes; F8 scales to a plain
-// [P, H/128] fp32 array.
+// Token-major: one warp per token reads the token's row once and writes it to
+// each of its pool rows slot[t*K + k] (masked slots are skipped; padding rows
+// are never written, the GEMM epilogues ignore them).  MX scales go to the
+// 512-byte chunk layout the MMA consumes; F8 scales to a plain [P, H/128] fp32
+// array.  Every lane holds the token's K pool rows; the shuffles that spread
+// them run with the warp converged.
+__device__ __forceinline__ void token_rows(const int32_t* __restrict__ slot, int64_t t, int K, int lane,
+                                           int (&rows)[kMaxK]) {
+  const int myrow = lane < K ? __ldg(slot + t * K + lane) : -1;
+#pragma unroll
+  for (int k = 0; k < kMaxK; ++k) rows[k] = __shfl_sync(0xffffffffu, myrow, k);
+}
+
+// x holds e4m3 codes [T, H] and their scales (MX: UE8M0 bytes [T, H/32]; F8: fp32 [T, H/128]).
 __global__ void __launch_bounds__(256)
-    gather_kernel(const int32_t* __restrict__ blk_off_end, const int32_t* __restrict__ src, int K, int H,
-                  int BT, int variant, const uint8_t* __restrict__ x, const void* __restrict__ x_sf,
-                  uint8_t* __restrict__ pool_x, uint8_t* __restrict__ pool_x_sf) {
-  const int64_t rows = static_cast<int64_t>(*blk_off_end) * BT;
+    gather_kernel(const int32_t* __restrict__ slot, int T, int K, int H, int BT, int variant,
+                  const uint8_t* __restrict__ x, const void* __restrict__ x_sf, uint8_t* __restrict__ pool_x,
+                  uint8_t* __restrict__ pool_x_sf) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int KB = H / 128;
-  for (int64_t r = warp0; r < rows; r += nwarps) {
-    const int s = __ldg(src + r);
-    if (s < 0) continue;
-    const int64_t t = s / K;
+  for (int64_t t = warp0; t < T; t += nwarps) {
+    int rows[kMaxK];
+    token_rows(slot, t, K, lane, rows);
     const uint4* srow = reinterpret_cast<const uint4*>(x + t * H);
-    uint4* drow = reinterpret_cast<uint4*>(pool_x + r * H);
-    for (int i = lane; i < H / 16; i += 32) drow[i] = __ldg(srow + i);
-    if (variant == MM_MOE_VARIANT_MX) {
-      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(x_sf) + t * (H / 32));
-      const int rr = static_cast<int>(r % BT);
-      const int64_t blk = r / BT;
-      for (int kb = lane; kb < KB; kb += 32)
-        *reinterpret_cast<uint32_t*>(pool_x_sf + (blk * KB + kb) * kSFChunk + sf_chunk_offset(rr, 0)) =
-            __ldg(ssf + kb);
-    } else {
-      const float* ssf = static_cast<const float*>(x_sf) + t * KB;
-      float* dsf = reinterpret_cast<float*>(pool_x_sf) + r * KB;
-      for (int kb = lane; kb < KB; kb += 32) dsf[kb] = __ldg(ssf + kb);
+#pragma unroll 4
+    for (int i = lane; i < H / 16; i += 32) {
+      const uint4 v = __ldg(srow + i);
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        const int r = k < K ? rows[k] : -1;
+        if (r >= 0) reinterpret_cast<uint4*>(pool_x + static_cast<int64_t>(r) * H)[i] = v;
+      }
+    }
+    for (int kb = lane; kb < KB; kb += 32) {
+      if (variant == MM_MOE_VARIANT_MX) {
+        // the four UE8M0 bytes of one 128-element block, one 32-bit word in either layout
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(x_sf) + t * (H / 32)) + kb);
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+          const int r = k < K ? rows[k] : -1;
+          if (r >= 0)
+            *reinterpret_cast<uint32_t*>(pool_x_sf + (static_cast<int64_t>(r / BT) * KB + kb) * kSFChunk +
+                                         sf_chunk_offset(r % BT, 0)) = w;
+        }
+      } else {
+        const float sc = __ldg(static_cast<const float*>(x_sf) + t * KB + kb);
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+          const int r = k < K ? rows[k] : -1;
+          if (r >= 0) reinterpret_cast<float*>(pool_x_sf)[static_cast<int64_t>(r) * KB + kb] = sc;
+        }
+      }
     }
   }
 }
 
-cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf,
+// x holds bf16 activations [T, H]: each token's row is quantised once
+// (quant.cuh) and every chunk written to each of the token's pool rows, so the
+// division-heavy F8 rule runs once per token rather than once per slot.
+__global__ void __launch_bounds__(256)
+    gather_quant_kernel(const int32_t* __restrict__ slot, int T, int K, int H, int BT, int variant,
+                        const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ pool_x,
+                        uint8_t* __restrict__ pool_x_sf) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = warp0; t < T; t += nwarps) {
+    int rows[kMaxK];
+    token_rows(slot, t, K, lane, rows);
+    const __nv_bfloat16* brow = x + t * H;
+    if (variant == MM_MOE_VARIANT_MX) {
+      quant_row_mx_bf16(brow, H, lane, [&](int j, const uint4 (&c)[2], uint8_t sfb, bool) {
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+          const int r = k < K ? rows[k] : -1;
+          if (r < 0) continue;
+          uint4* d = reinterpret_cast<uint4*>(pool_x + static_cast<int64_t>(r) * H) + 2 * j;
+          d[0] = c[0];
+          d[1] = c[1];
+          pool_x_sf[(static_cast<int64_t>(r / BT) * (H / 128) + (j >> 2)) * kSFChunk + sf_chunk_offset(r % BT, j & 3)] =
+              sfb;
+        }
+      });
+    } else {
+      quant_row_f8_bf16(brow, H, lane, [&](int c, const uint4 (&cd)[2], float sc, bool lead) {
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+          const int r = k < K ? rows[k] : -1;
+          if (r < 0) continue;
+          uint4* d = reinterpret_cast<uint4*>(pool_x + static_cast<int64_t>(r) * H) + 2 * c;
+          d[0] = cd[0];
+          d[1] = cd[1];
+          if (lead) reinterpret_cast<float*>(pool_x_sf)[static_cast<int64_t>(r) * (H / 128) + (c >> 2)] = sc;
+        }
+      });
+    }
+  }
+}
+
+cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf, bool x_bf16,
                           cudaStream_t s) {
   const int grid = dev_info().sms * 4;
-  gather_kernel<<<grid, 256, 0, s>>>(W.blk_off + L.E, W.src, L.K, L.H, L.BT, L.variant, x, x_sf, W.pool_x,
-                                     W.pool_x_sf);
+  if (x_bf16)
+    gather_quant_kernel<<<grid, 256, 0, s>>>(W.slot, L.T, L.K, L.H, L.BT, L.variant,
+                                             reinterpret_cast<const __nv_bfloat16*>(x), W.pool_x, W.pool_x_sf);
+  else
+    gather_kernel<<<grid, 256, 0, s>>>(W.slot, L.T, L.K, L.H, L.BT, L.variant, x, x_sf, W.pool_x, W.pool_x_sf);
   return cudaGetLastError();
 }
 

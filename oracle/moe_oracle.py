@@ -159,6 +159,24 @@ def requant_f8(a32: np.ndarray, block: int = 128) -> Tuple[np.ndarray, np.ndarra
     return codes.reshape(n), s, deq.reshape(n)
 
 
+def quantise_x(x: np.ndarray, variant: str) -> Tuple[np.ndarray, np.ndarray]:
+    """bf16 activations (given as their exact fp32 / fp64 values) [T, H] -> the
+    layer's FP8 input: (e4m3 codes u8 [T, H], scales).  The pages feed the
+    layer x already quantised ("07 · MegaMoE" §3: the buffer's input region
+    holds x and x_sf) in the formats of step 5 above, so a bf16 row is
+    quantised here with the same block rule: UE8M0 per 32 (requant_mx) for
+    mx, fp32 amax/448 per 128 (requant_f8) for f8.  mx scales: UE8M0 bytes
+    [T, H/32]; f8 scales: fp32 [T, H/128].  Blocks never straddle rows (H is
+    a multiple of the block), so the whole matrix is one call."""
+    x = np.asarray(x, dtype=np.float32)
+    T, H = x.shape
+    if variant == "mx":
+        codes, sf, _ = requant_mx(x.reshape(T * H), 32)
+        return codes.reshape(T, H), sf.reshape(T, H // 32)
+    codes, sf, _ = requant_f8(x.reshape(T * H), 128)
+    return codes.reshape(T, H), sf.reshape(T, H // 128)
+
+
 # ----------------------------------------------------------------------------- dequantisation
 
 

@@ -129,3 +129,33 @@ def test_requant_mx_error_bound():
     blocks = np.abs(a).reshape(-1, 32).max(1)
     assert np.all(blocks <= 448 * 2.0 ** (s.astype(np.int64) - 127))
     assert np.all(blocks > 224 * 2.0 ** (s.astype(np.int64) - 127))   # smallest such e
+
+
+@pytest.mark.parametrize("variant", ["mx", "f8"])
+def test_quantise_x_matches_workload_quantiser(variant):
+    """Two independent quantisers of the layer's FP8 input (the oracle's numpy
+    requant and the input generator's torch one) agree bit for bit on bf16 rows."""
+    import workload as W
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn(37, 512, generator=g) * torch.logspace(-3, 3, 37)[:, None]).to(torch.bfloat16)
+    codes, sf = O.quantise_x(x.float().numpy(), variant)
+    if variant == "mx":
+        rc, rs = W.quant_e4m3_ue8m0(x.float(), 32)
+    else:
+        rc, rs = W.quant_e4m3_f32_rows(x.float(), 128)
+    assert np.array_equal(codes, rc.numpy())
+    assert np.array_equal(np.asarray(sf), rs.numpy())
+
+
+def test_quantise_x_closed_forms():
+    """A row of ones: UE8M0 e = -8 (448 * 2^-8 = 1.75 >= 1 > 0.875), byte 119,
+    every code 1 * 2^8 = 256 = 0x78; F8 s = fp32(1/448), code RNE(1/s) = 448 = 0x7E.
+    A zero row: the 1e-10 floor, e = -42 (448 * 2^-42 >= 1e-10 > 448 * 2^-43), codes 0."""
+    ones = np.ones((2, 256), dtype=np.float32)
+    c, s = O.quantise_x(ones, "mx")
+    assert np.all(s == 119) and np.all(c == 0x78)
+    c, s = O.quantise_x(ones, "f8")
+    assert np.all(s == np.float32(1.0) / np.float32(448.0)) and np.all(c == 0x7E)
+    zero = np.zeros((1, 128), dtype=np.float32)
+    c, s = O.quantise_x(zero, "mx")
+    assert np.all(s == 127 - 42) and np.all(c == 0)

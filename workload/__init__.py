@@ -156,6 +156,12 @@ def make_x(cfg: Config, device="cpu"):
     return quant_e4m3_f32_rows(x, 128)
 
 
+def make_x_bf16(cfg: Config, device="cpu"):
+    """bf16 activations [T, H] ~ N(0, 1) for the bf16-input path (its own stream)."""
+    g = _gen(cfg.seed, 4, device)
+    return torch.randn(cfg.T, cfg.H, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
 def make_expert(cfg: Config, e: int, device="cpu"):
     """(w1 [2I,...], w1_sf, w2 [H,...], w2_sf) for one expert."""
     g = _gen(cfg.seed, 1000 + e, device)
