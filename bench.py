@@ -156,8 +156,9 @@ def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4, x_bf16: bool =
     l1_bytes = touched * w1_b + pairs * x_b + pairs * a_b
     l2_bytes = touched * w2_b + pairs * a_b + pairs * H * part_elem
     gather_bytes = pairs * (x_in + x_b)      # read the token's row, write its pool row
+    combine_bytes = pairs * H * part_elem + T * H * 2   # read the partials, write the output
     return {"touched_experts": touched, "pairs": pairs, "step_bytes": step_bytes, "flops": flops,
-            "gather_bytes": gather_bytes,
+            "gather_bytes": gather_bytes, "combine_bytes": combine_bytes,
             "l1_bytes": l1_bytes, "l2_bytes": l2_bytes, "l1_flops": 4.0 * pairs * H * I,
             "l2_flops": 2.0 * pairs * H * I}
 
@@ -192,6 +193,8 @@ def run_ours(args, ws_n, rank, local):
     if args.fused is not None:
         opt.fused = args.fused
     opt.partials_bf16 = 1 if args.partials == "bf16" else 0
+    if args.early_combine is not None:
+        opt.early_combine = args.early_combine
     if args.x == "bf16":
         # bf16 activations: the gather quantises each row (x_sf is not read)
         inp["x"], inp["x_sf"] = W.make_x_bf16(cfg, dev), None
@@ -230,7 +233,8 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
-        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16, x_bf16=opt.x_bf16)
+        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16, x_bf16=opt.x_bf16,
+                      early_combine=opt.early_combine)
         o.timing_events = ctypes.cast(arrays[i], ctypes.c_void_p)
         fwd(o)
     torch.cuda.synchronize()
@@ -274,10 +278,11 @@ def run_ours(args, ws_n, rank, local):
     fp8 = float(pk["bf16_tflops"]) * FP8_OVER_BF16
     stage_mean = stage_ms.mean(0)
     l1_ms, l2_ms = float(stage_mean[2]), float(stage_mean[3])
+    early = fused and bool(opt.early_combine)
     if fused:
-        # one launch runs gather, L1 and L2: its bytes are all three
+        # one launch runs gather, L1 and L2 (and the combine, when early): its bytes are all of them
         dom, dom_ms = "fused", l1_ms + l2_ms
-        dom_bytes = acc["l1_bytes"] + acc["l2_bytes"] + acc["gather_bytes"]
+        dom_bytes = acc["l1_bytes"] + acc["l2_bytes"] + acc["gather_bytes"] + (acc["combine_bytes"] if early else 0)
     else:
         # dominant kernel: the one with the largest share of the step
         dom = "l1" if l1_ms >= l2_ms else "l2"
@@ -306,7 +311,7 @@ def run_ours(args, ws_n, rank, local):
                    "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "K": cfg.K, "seed": cfg.seed,
                    "l2_policy": "L2 flushed (512 MiB write) before every timed step; weights 3+ GB >> L2",
                    "parallelism": f"replicas x{ws_n} (no data-path collective)",
-                   "fused_stream": fused, "partials": args.partials, "x": args.x},
+                   "fused_stream": fused, "early_combine": early, "partials": args.partials, "x": args.x},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
         "path_roofline": {"t_roofline_us": t_roof * 1e6, "frac": t_roof / (step_ms * 1e-3),
                           "bytes": acc["step_bytes"], "flops": acc["flops"],
@@ -316,7 +321,7 @@ def run_ours(args, ws_n, rank, local):
         "stages_ms": ({"dispatch": float(stage_mean[0]), "fused_gather_l1_l2": float(stage_mean[2] + stage_mean[3]),
                        "combine": float(stage_mean[4])} if fused else
                       {s: float(v) for s, v in zip(M.STAGES, stage_mean)}),
-        "roofline": {"kernel": ("gemm_mx_kernel (fused gather + L1 + L2 stream)" if fused else
+        "roofline": {"kernel": (f"gemm_mx_kernel (fused gather + L1 + L2{' + combine' if early else ''} stream)" if fused else
                                 f"gemm_{'mx' if cfg.variant == 'mx' else 'f8'}_kernel ({dom.upper()} grouped GEMM)"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": kernel_traffic(dom, cfg.name if args.partials == "fp32" else f"{cfg.name}:bf16-partials"),
@@ -324,7 +329,7 @@ def run_ours(args, ws_n, rank, local):
                      "peak_source": f"{pk_src} hbm_gbs (STREAM-style copy)"},
         "e2e": {"value": ws_n * cfg.T / (e2e_step_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
-        "gpu_launches": (4 if fused else 6) * K,   # dispatch x2, [gather], GEMM(s), combine
+        "gpu_launches": (3 if early else (4 if fused else 6)) * K,   # dispatch x2, [gather], GEMM(s), [combine]
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -405,6 +410,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
                     help="L2 partials: fp32 (default) or cast to bf16 before the combine")
+    ap.add_argument("--early-combine", type=int, choices=[0, 1], default=None,
+                    help="fused stream: combine in the GEMM's epilogue warps (library default 1) or in a kernel after it")
     ap.add_argument("--x", default="fp8", choices=["fp8", "bf16"],
                     help="activations: fp8 codes + scales (default) or bf16, quantised inside the gather")
     ap.add_argument("--cpu-tokens", type=int, default=16,

@@ -118,7 +118,12 @@ typedef struct mm_moe_options {
                                    the variant's rule (MX: UE8M0 per 32, 448 * 2^e >= amax; F8: fp32
                                    max(amax, 1e-10) / 448 per 128).  Non-finite inputs give
                                    unspecified codes. */
-  int reserved[2];
+  int early_combine;            /* fused stream (MX): 1 = once a CTA has no GEMM work left, its epilogue
+                                   warps combine every token whose experts have finished L2 (the pages'
+                                   early combine) and no combine kernel runs; 0 (default) = a combine
+                                   kernel after the GEMM, which measures as fast or faster on one
+                                   GB300.  Bit-identical either way. */
+  int reserved[1];
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

@@ -25,7 +25,7 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.cnt = o; o = align_up(o + sizeof(int) * E, 256);
   L.blk_off = o; o = align_up(o + sizeof(int) * (E + 1), 256);
   L.dscr = o; o = align_up(o + sizeof(int) * static_cast<size_t>(kDispatchMaxCtas) * E, 256);
-  L.ctr = o; o = align_up(o + sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), 256);
+  L.ctr = o; o = align_up(o + sizeof(int) * ctr_ints(L), 256);
   L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
   L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
   L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
@@ -183,6 +183,7 @@ void mm_moe_default_options(mm_moe_options* opt) {
   opt->retain_intermediate = 0;
   opt->wait_timeout_ms = 2000;
   opt->num_sms = 0;
+  opt->early_combine = 0;
 }
 
 int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E, int K, size_t* bytes) {
@@ -278,6 +279,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
   const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
   if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
+  // early combine in the fused stream
+  const bool early = fused && o.early_combine;
   const WsPtrs W = ws_ptrs(workspace, L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
@@ -298,12 +301,12 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   const float clamp = o.activation_clamp > 0.f ? o.activation_clamp : INFINITY;
   // arrival counters of the fused stream and the tile-group counters of every GEMM launch
   if (e == cudaSuccess)
-    e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * (2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters), s);
+    e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * ctr_ints(L), s);
   if (o.variant == MM_MOE_VARIANT_MX) {
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 o.cta_pairs == 2, clamp, o.precise_swiglu != 0};
+                 o.cta_pairs == 2, clamp, o.precise_swiglu != 0, early, topk_idx, out};
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
@@ -327,7 +330,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     }
   }
   if (e == cudaSuccess) e = mark(4);
-  if (e == cudaSuccess) e = launch_combine(L, W, topk_idx, out, s);
+  // the fused stream's early combine has written `out` already
+  if (e == cudaSuccess && !early) e = launch_combine(L, W, topk_idx, out, s);
   if (e == cudaSuccess) e = mark(5);
   if (e != cudaSuccess) {
     if (getenv("MM_MOE_DEBUG")) fprintf(stderr, "mm_moe_forward: %s\n", cudaGetErrorString(e));

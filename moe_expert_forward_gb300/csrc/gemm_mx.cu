@@ -48,6 +48,7 @@
 // and a site code and returns.
 #include <cuda.h>
 
+#include "combine.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -86,7 +87,7 @@ constexpr int kSfColsPerStage = 12;    // 4 (tokens) + 8 (weights)
 // wait-site codes reported through the status word
 enum : int {
   kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104,
-  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108
+  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108, kSiteCombine = 109, kSiteDeferred = 110
 };
 
 struct Args {
@@ -116,6 +117,12 @@ struct Args {
   int* ctr_gather;           // mode 3: rows gathered per pool block
   int* ctr_l1;               // mode 3: L1 epilogue warps finished per pool block
   int* sched;                // tile groups handed out so far (zero at launch)
+  int early_combine;         // mode 3: the epilogue warps combine tokens after their last task
+  const int32_t* topk_idx;   // early combine: routing [T, K] and the bf16 output [T, H]
+  __nv_bfloat16* out;
+  int* cmb;                  // early combine counters: tokens taken, deferred, classified, deferred taken
+  int* ctr_l2;               // [E] L2 epilogue warps finished per expert (early combine)
+  int* deferred;             // [T] tokens pass 1 could not combine yet, as t + 1 (0: not written)
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;  // per-CTA wait/busy nanoseconds (debug_flags bit 1) or null
@@ -242,6 +249,93 @@ __device__ __forceinline__ void gather_rows(const Args& args, const int* s_blk, 
     fence_proxy_async_global();
     __syncwarp();
     if (lane == 0 && done) red_release_gpu_add(args.ctr_gather + b, done);
+  }
+}
+
+// Early combine (DeepGEMM PR #440, "Also in the diff": math warps reduce the
+// tokens whose selected experts have all published).  An epilogue warp comes
+// here once its CTA has no tile group left, and by then every group of the
+// stream has been dealt, so each L2 tile a token waits for belongs to a CTA
+// that finishes it without any help from this warp: no wait below can close a
+// cycle.  Pass 1 takes tokens in order: a token whose valid slots' experts
+// have all finished L2 (per-expert counts of epilogue warps, read with
+// acquire) is combined at once by the warp, any other is appended to a
+// deferred list.  Pass 2 takes the deferred tokens and waits, bounded, for
+// their experts.  The arithmetic is the combine kernel's (combine.cuh).  Every
+// branch below is warp-uniform.
+template <typename PartT>
+__device__ __forceinline__ void early_combine(const Args& args, const int* s_blk, const Status& st,
+                                              volatile int* s_abort, int lane) {
+  const int T = args.T, K = args.K, E = args.E;
+  const PartT* part = reinterpret_cast<const PartT*>(args.partials);
+  int* take = args.cmb;             // pass 1: tokens taken
+  int* ndef = args.cmb + 1;         // deferred so far
+  int* classified = args.cmb + 2;   // pass-1 tokens combined or deferred
+  int* take2 = args.cmb + 3;        // pass 2: deferred entries taken
+  auto stop = [&]() { return __shfl_sync(0xffffffffu, *s_abort ? 1 : 0, 0) != 0; };
+  auto next = [&](int* ctr) {
+    int c = 0;
+    if (lane == 0) c = atomicAdd(ctr, 1);
+    return __shfl_sync(0xffffffffu, c, 0);
+  };
+  // lane k < K checks slot k; vmask gets the valid slots
+  auto ready = [&](int t, uint32_t& vmask) -> bool {
+    bool ok = true, v = false;
+    if (lane < K) {
+      const int e = __ldg(args.topk_idx + static_cast<int64_t>(t) * K + lane);
+      v = e >= 0 && e < E;
+      if (v) ok = ld_acquire_gpu(args.ctr_l2 + e) >= kEpiWarps * args.NB2 * (s_blk[e + 1] - s_blk[e]);
+    }
+    vmask = __ballot_sync(0xffffffffu, v);
+    const bool all = __all_sync(0xffffffffu, ok);
+    __syncwarp();   // the checking lanes' acquires before every lane's partial loads
+    return all;
+  };
+  while (!stop()) {
+    const int t = next(take);
+    if (t >= T) break;
+    uint32_t vm;
+    if (ready(t, vm)) combine_token_warp<PartT, 4>(part, t, T, args.H, K, vm, args.out, lane);
+    else if (lane == 0) st_release_gpu(args.deferred + atomicAdd(ndef, 1), t + 1);
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(classified, 1);
+  }
+  while (!stop()) {
+    const int c = next(take2);
+    if (c >= T) break;
+    int t = -1;   // stays -1 when entry c will never be written (every token classified, fewer deferred)
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer();
+      while (true) {
+        const int v = ld_acquire_gpu(args.deferred + c);
+        if (v > 0) { t = v - 1; break; }
+        if (ld_acquire_gpu(classified) >= T && ld_acquire_gpu(ndef) <= c) break;
+        if (*s_abort) break;
+        if (globaltimer() - t0 > st.timeout_ns) {
+          report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, kSiteDeferred);
+          *s_abort = 1;
+          break;
+        }
+      }
+    }
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t < 0) break;
+    uint32_t vm;
+    const uint64_t t0 = globaltimer();
+    bool ok = true;
+    while (!ready(t, vm)) {
+      int late = 0;
+      if (lane == 0) late = (*s_abort || globaltimer() - t0 > st.timeout_ns) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, late, 0)) { ok = false; break; }
+    }
+    if (!ok) {   // the first error recorded wins, so an abort raised elsewhere keeps its own
+      if (lane == 0) {
+        report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, kSiteCombine);
+        *s_abort = 1;
+      }
+      break;
+    }
+    combine_token_warp<PartT, 4>(part, t, T, args.H, K, vm, args.out, lane);
   }
 }
 
@@ -535,8 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             }
           }
         }
+        if (args.early_combine && !t.ghost) {
+          __syncwarp();   // the warp's partial stores before its release
+          if (lane == 0) red_release_gpu_add(args.ctr_l2 + t.e, 1);
+        }
       }
       if (kProf) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
+    }
+    if (args.early_combine) {
+      if (args.pbf16) early_combine<__nv_bfloat16>(args, s_blk, st, s_abort, lane);
+      else early_combine<float>(args, s_blk, st, s_abort, lane);
     }
     if (kProf && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
@@ -589,6 +691,12 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.precise = g.precise;
   a.ctr_gather = W.ctr; a.ctr_l1 = W.ctr + L.nblk_cap;
   a.sched = W.ctr + 2 * L.nblk_cap + mode;
+  a.early_combine = (mode == 3 && g.early_combine) ? 1 : 0;
+  a.topk_idx = g.topk_idx;
+  a.out = static_cast<__nv_bfloat16*>(g.out);
+  a.cmb = W.ctr + 2 * L.nblk_cap + kSchedCounters;
+  a.ctr_l2 = a.cmb + kCombineCounters;
+  a.deferred = a.ctr_l2 + L.E;
   a.status = W.status; a.timeout_ns = g.timeout_ns;
   a.prof = g.prof ? g.prof + (mode == 2 ? 8 * 1024 : 0) : nullptr;
   {

@@ -14,6 +14,8 @@ constexpr int kBK = 128;        // contraction elements per pipeline stage
 constexpr int kSFChunk = 512;   // bytes of one 128-row x 128-K scale chunk (MX)
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 16;
+constexpr int kSchedCounters = 4;        // tile-group counters after the arrival counters, one per GEMM mode
+constexpr int kCombineCounters = 4;      // early combine: tokens taken, deferred, classified, deferred taken
 
 // Byte offsets of every buffer inside the caller's workspace.
 struct Layout {
@@ -27,14 +29,20 @@ struct Layout {
 
 Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0, int partials_bf16 = 0);
 
+// Ints of the counter region, zeroed before every forward: [2][nblk_cap]
+// per-block arrival counters, kSchedCounters, kCombineCounters, [E] L2
+// completions per expert, [T] deferred tokens of the early combine (t + 1).
+inline size_t ctr_ints(const Layout& L) {
+  return 2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters + kCombineCounters + L.E + L.T;
+}
+
 // Device pointers resolved from a workspace.
 struct WsPtrs {
   int* status;
   int* cnt;
   int* blk_off;
   int* dscr;
-  int* ctr;                  // [2][nblk_cap] per-block arrival counters of the fused stream, then
-                             // kSchedCounters tile-group counters
+  int* ctr;                  // the counter region (ctr_ints): arrival, tile-group and early-combine counters
   int* slot;
   int* src;
   uint8_t* pool_x;
@@ -59,7 +67,6 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int bl
                             int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
                             int64_t scratch_ints, cudaStream_t s);
 constexpr int kF8MaxKB = 64;             // F8 variant: H and I at most 64 x 128
-constexpr int kSchedCounters = 4;        // tile-group counters after the arrival counters, one per GEMM mode
 constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA counts [CTAs][E]
 // x_bf16: x is bf16 [T, H] and each row is quantised on its way into the pool
 cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf, bool x_bf16,
@@ -89,6 +96,9 @@ struct GemmLaunch {
   bool pair;                // run as 2-CTA clusters sharing token tiles (when the device allows)
   float clamp;              // activation clamp of gate and up (+inf: none)
   int precise;              // SwiGLU with expf and the IEEE division instead of the fast-math form
+  bool early_combine;       // fused stream: the epilogue warps combine tokens once their experts are done
+  const int32_t* topk_idx;  // early combine: the routing and the bf16 output [T, H]
+  void* out;
 };
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);

@@ -2,6 +2,7 @@
 // pool, fixed-order combine, weight-scale relayout and intermediate read-back.
 #include <cuda_bf16.h>
 
+#include "combine.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -332,11 +333,9 @@ cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, co
 }
 
 // ----------------------------------------------------------------------------- combine
-// out[t, h] = bf16_rn( sum_{k=0..K-1, slot valid} part[k][t][h] ), summed in k order in fp32.
 // out[t, h] = bf16(sum over k = 0..K-1 of part[k][t][h]), the sum in fp32 in
 // fixed k order; slots with a masked or out-of-range expert are skipped.  Each
-// thread takes 8 consecutive columns of one token.  PartT: float, or bf16 when
-// the L2 epilogue cast its partials.
+// thread takes 8 consecutive columns of one token (combine.cuh).
 template <typename PartT>
 __global__ void __launch_bounds__(256)
     combine_kernel(const PartT* __restrict__ part, const int32_t* __restrict__ idx, int T, int K, int E, int H,
@@ -346,35 +345,12 @@ __global__ void __launch_bounds__(256)
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t t = g / (H / 8);
     const int h = static_cast<int>(g % (H / 8)) * 8;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < K; ++k) {
-      const int e = __ldg(idx + t * K + k);
-      if (e < 0 || e >= E) continue;
-      const PartT* p = part + ((static_cast<int64_t>(k) * T + t) * H + h);
-      if constexpr (sizeof(PartT) == 4) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(p)), b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-      } else {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {   // bf16 -> fp32 is exact: the bits move up 16 places
-          acc[2 * i] += __uint_as_float(w[i] << 16);
-          acc[2 * i + 1] += __uint_as_float(w[i] & 0xffff0000u);
-        }
-      }
-    }
-    uint4 o;
-    __nv_bfloat162 v0 = __floats2bfloat162_rn(acc[0], acc[1]);
-    __nv_bfloat162 v1 = __floats2bfloat162_rn(acc[2], acc[3]);
-    __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[4], acc[5]);
-    __nv_bfloat162 v3 = __floats2bfloat162_rn(acc[6], acc[7]);
-    o.x = *reinterpret_cast<uint32_t*>(&v0);
-    o.y = *reinterpret_cast<uint32_t*>(&v1);
-    o.z = *reinterpret_cast<uint32_t*>(&v2);
-    o.w = *reinterpret_cast<uint32_t*>(&v3);
-    *reinterpret_cast<uint4*>(out + t * H + h) = o;
+    combine8(part, t, h, T, H, K,
+             [&](int k) {
+               const int e = __ldg(idx + t * K + k);
+               return e >= 0 && e < E;
+             },
+             out);
   }
 }
 
