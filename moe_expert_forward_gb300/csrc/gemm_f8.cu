@@ -292,19 +292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 64; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
       bool ok = true;
-      // the row's activation scale of k-block kb + 2 is loaded while kb's partial is
-      // promoted, so no global-load latency sits between a partial and its promotion
-      float sxa = live ? __ldg(sxr) : 0.f;
-      float sxb = (live && KB > 1) ? __ldg(sxr + 1) : 0.f;
+      // the row's activation scale of k-block kb + 2 is loaded right after kb's is
+      // used; L1 runs two k-blocks a turn with one scale register each, so a load
+      // has two promotions to land and no register move waits on it
+      float sx0 = live ? __ldg(sxr) : 0.f;
+      float sx1 = (live && KB > 1) ? __ldg(sxr + 1) : 0.f;
       if (kProf) e_setup += clock64() - ts0;
-      for (int kb = 0; kb < KB; ++kb, ++g) {
-        const float f0 = sxa * w0s[kb];
-        const float f1 = sxa * w1s[kb];
-        sxa = sxb;
-        if (kb + 2 < KB) sxb = live ? __ldg(sxr + kb + 2) : 0.f;
+      auto promote = [&](int kb, float sx) -> bool {
+        const float f0 = sx * w0s[kb];
+        const float f1 = sx * w1s[kb];
         const int pb = g & 1;
         const long long tw0 = kProf ? clock64() : 0;
-        if (!mbar_wait(&pfull[pb], (g >> 1) & 1, st, s_abort, kSitePFull)) { ok = false; break; }
+        if (!mbar_wait(&pfull[pb], (g >> 1) & 1, st, s_abort, kSitePFull)) return false;
         const long long tw1 = kProf ? clock64() : 0;
         tc_fence_after();
         // one 32-column slice at a time keeps at most 128 sums + 32 loaded values live
@@ -330,6 +329,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty[pb]);
         if (kProf) { e_wait += tw1 - tw0; e_promo += clock64() - tw1; }
+        ++g;
+        return true;
+      };
+      if constexpr (PHASE == 1) {
+        for (int kb = 0; kb < KB; kb += 2) {
+          if (!promote(kb, sx0)) { ok = false; break; }
+          if (kb + 2 < KB) sx0 = live ? __ldg(sxr + kb + 2) : 0.f;
+          if (kb + 1 < KB) {
+            if (!promote(kb + 1, sx1)) { ok = false; break; }
+            if (kb + 3 < KB) sx1 = live ? __ldg(sxr + kb + 3) : 0.f;
+          }
+        }
+      } else {   // one k-block a turn: the two-a-turn body spills here (measured slower)
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!promote(kb, sx0)) { ok = false; break; }
+          sx0 = sx1;
+          if (kb + 2 < KB) sx1 = live ? __ldg(sxr + kb + 2) : 0.f;
+        }
       }
       if (!ok) break;
       const long long tw2 = kProf ? clock64() : 0;
