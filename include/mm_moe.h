@@ -127,7 +127,11 @@ typedef struct mm_moe_options {
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather
-                                   done, [3] L1 done, [4] L2 done, [5] combine done; NULL = none */
+                                   done, [3] L1 done, [4] L2 done, [5] combine done; NULL = none, and a
+                                   NULL entry is skipped.  The GEMM of the fused stream and the combine
+                                   are launched programmatically (they start their setup while the
+                                   kernel before them finishes) unless an event is recorded between
+                                   them and that kernel ([1]/[2], resp. [3]/[4]). */
 } mm_moe_options;
 
 #define MM_MOE_NUM_TIMING_EVENTS 6

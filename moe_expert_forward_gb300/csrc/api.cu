@@ -286,27 +286,30 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
 
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(o.timing_events);
-  auto mark = [&](int i) -> cudaError_t { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+  auto mark = [&](int i) -> cudaError_t { return ev && ev[i] ? cudaEventRecord(ev[i], s) : cudaSuccess; };
+  // kernels follow one another with programmatic launches only where no event sits between them
+  const bool pdl_gemm = fused && !(ev && (ev[1] || ev[2]));
+  const bool pdl_combine = !(ev && (ev[3] || ev[4]));
 
   cudaError_t e = mark(0);
   if (e == cudaSuccess) e = cudaMemsetAsync(W.status, 0, 16, s);
+  // the arrival counters of the fused stream and the tile-group counters of every GEMM launch,
+  // cleared before the routing kernels so that those and the GEMM are adjacent on the stream
+  if (e == cudaSuccess) e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * ctr_ints(L), s);
+  if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
   if (e == cudaSuccess)
     e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, W.dscr,
                         static_cast<int64_t>(kDispatchMaxCtas) * E, s);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess && !fused) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, s);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
   const uint64_t timeout_ns = static_cast<uint64_t>(o.wait_timeout_ms) * 1000000ull;
   const float clamp = o.activation_clamp > 0.f ? o.activation_clamp : INFINITY;
-  // arrival counters of the fused stream and the tile-group counters of every GEMM launch
-  if (e == cudaSuccess)
-    e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * ctr_ints(L), s);
   if (o.variant == MM_MOE_VARIANT_MX) {
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 o.cta_pairs == 2, clamp, o.precise_swiglu != 0, early, topk_idx, out};
+                 o.cta_pairs == 2, clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm};
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
@@ -331,7 +334,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   }
   if (e == cudaSuccess) e = mark(4);
   // the fused stream's early combine has written `out` already
-  if (e == cudaSuccess && !early) e = launch_combine(L, W, topk_idx, out, s);
+  if (e == cudaSuccess && !early) e = launch_combine(L, W, topk_idx, out, pdl_combine, s);
   if (e == cudaSuccess) e = mark(5);
   if (e != cudaSuccess) {
     if (getenv("MM_MOE_DEBUG")) fprintf(stderr, "mm_moe_forward: %s\n", cudaGetErrorString(e));

@@ -394,6 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     tmem_alloc(s_tmem, kTmemCols);
     tmem_relinquish();
   }
+  // with a programmatic launch the setup above overlaps the routing kernel; everything
+  // below reads what that kernel (or earlier work on the stream) wrote
+  pdl_wait();
   for (int i = threadIdx.x; i <= E; i += kThreads) s_blk[i] = args.blk_off[i];
   for (int i = threadIdx.x; i < E; i += kThreads) s_cnt[i] = args.cnt[i];
   __syncthreads();
@@ -775,12 +778,18 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
   if (mode == 3) {
     // the fused stream waits across CTAs: launch cooperatively so that every CTA is resident
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na].val.cooperative = 1;
+    ++na;
+  }
+  if (g.pdl) {
+    // start during the routing kernel: the setup before pdl_wait() overlaps its tail
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
   if (pair) {

@@ -71,7 +71,8 @@ constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA co
 // x_bf16: x is bf16 [T, H] and each row is quantised on its way into the pool
 cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf, bool x_bf16,
                           cudaStream_t s);
-cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out,
+// pdl: programmatic launch after the GEMM (the combine waits for it in-kernel)
+cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out, bool pdl,
                            cudaStream_t s);
 cudaError_t launch_prepare_sf_mx(const uint8_t* w1_sf, const uint8_t* w2_sf, int H, int I, int E,
                                  uint8_t* w1_sfp, uint8_t* w2_sfp, cudaStream_t s);
@@ -99,6 +100,7 @@ struct GemmLaunch {
   bool early_combine;       // fused stream: the epilogue warps combine tokens once their experts are done
   const int32_t* topk_idx;  // early combine: the routing and the bf16 output [T, H]
   void* out;
+  bool pdl;                 // programmatic launch after the routing kernel
 };
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
                            const int32_t* __restrict__ cc, int32_t* __restrict__ cnt, int32_t* __restrict__ blk_off,
                            int32_t* __restrict__ slot, int32_t* __restrict__ src) {
   extern __shared__ int sm[];
+  pdl_trigger();                             // the GEMM may start its setup meanwhile
   int* wc = sm;                              // [8][E] per-warp counts, then offsets
   int* s_base = wc + kDispatchWarps * E;     // [E] rank of this CTA's first pair inside each expert
   int* s_cnt = s_base + E;                   // [E]
@@ -340,6 +341,7 @@ template <typename PartT>
 __global__ void __launch_bounds__(256)
     combine_kernel(const PartT* __restrict__ part, const int32_t* __restrict__ idx, int T, int K, int E, int H,
                    __nv_bfloat16* __restrict__ out) {
+  pdl_wait();                                // the partials of the GEMM before this launch
   const int64_t groups = static_cast<int64_t>(T) * (H / 8);
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
        g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -354,20 +356,28 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out,
+cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk_idx, void* out, bool pdl,
                            cudaStream_t s) {
   const int64_t groups = static_cast<int64_t>(L.T) * (L.H / 8);
   int64_t blocks = (groups + 255) / 256;
   const int64_t cap = static_cast<int64_t>(dev_info().sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   if (L.part_elem == 2)
-    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16*>(W.part), topk_idx, L.T, L.K, L.E, L.H, static_cast<__nv_bfloat16*>(out));
-  else
-    combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(W.part, topk_idx, L.T, L.K, L.E, L.H,
-                                                                   static_cast<__nv_bfloat16*>(out));
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16>, reinterpret_cast<const __nv_bfloat16*>(W.part),
+                              topk_idx, L.T, L.K, L.E, L.H, o);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<float>, static_cast<const float*>(W.part), topk_idx, L.T, L.K, L.E,
+                            L.H, o);
 }
 
 // ----------------------------------------------------------------------------- weight scales (MX)

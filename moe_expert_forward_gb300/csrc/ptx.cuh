@@ -192,6 +192,14 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, 
 }
 
 // ------------------------------------------------------------------ cross-CTA counters
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream still runs;
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible (it returns at once for a kernel launched without the attribute).
+// pdl_trigger() lets the next kernel's CTAs be scheduled before this CTA exits.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void st_release_gpu(int* p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
