@@ -86,7 +86,8 @@ typedef struct mm_moe_options {
                                    debug dump always use separate launches); 0: separate gather /
                                    L1 / L2 launches.  Both give bit-identical results. */
   int lag_units;                /* fused stream: how many experts the L2 tiles trail the L1 tiles
-                                   (0..64); -1 = auto */
+                                   (0..E, larger values act as E); -1 = auto (E: every L1 tile
+                                   before any L2 tile, the fastest order measured on one GPU) */
   int retain_intermediate;      /* keep the whole requantised intermediate readable after the call
                                    (mm_moe_read_intermediate) */
   unsigned wait_timeout_ms;     /* deadline of every device-side wait; 0 = default (2000 ms) */

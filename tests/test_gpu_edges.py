@@ -67,7 +67,7 @@ def test_topk_equals_experts(M, kw):
 @pytest.mark.parametrize("kw", MODES, ids=["fused", "two-launch", "pairs"])
 def test_largest_expert_count(M, kw):
     """E = 1024 (the largest the library takes): most experts get no token, the
-    shared-memory tables are at their largest, and the lag default is reached."""
+    shared-memory tables are at their largest, and the default lag (E) is the largest."""
     cfg = W.Config("e1024", T=96, H=256, I=128, E=1024, K=4, seed=34)
     _check_all_rows(M, cfg, W.make_inputs(cfg, "cpu"), _opt(M, cfg, **kw))
 
