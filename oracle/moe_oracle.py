@@ -30,8 +30,8 @@ fp32 first.  Everything else is fp64.
 Routing (step a1) is the plain definition of the contiguous per-expert pool
 ("07 · MegaMoE" §4; nxmr.cn walkthrough §二.2.4): experts in index order, each
 segment padded to a multiple of the block size, and inside a segment the
-(token, slot) pairs in ascending order (the deterministic order this build
-fixes in place of the pages' round-robin over source ranks).
+(token, slot) pairs in ascending order (a deterministic order, fixed here in
+place of the pages' round-robin over source ranks).
 """
 from __future__ import annotations
 
