@@ -223,7 +223,16 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
 /* Synchronise `stream`, then read the device status word of `workspace`.
  * Returns MM_MOE_OK, MM_MOE_ERR_TIMEOUT, MM_MOE_ERR_BAD_ROUTING or
  * MM_MOE_ERR_CUDA; *where (if non-NULL) receives the code of the check that
- * fired.  The word is cleared by the next forward. */
+ * fired.  The word is cleared by the next forward.
+ * Wait sites of MM_MOE_ERR_TIMEOUT:
+ *   MX GEMM   101 a free pipeline stage, 102 a stage's data, 103 the free
+ *             accumulator, 104 the finished accumulator, 105 a pool block's
+ *             gathered rows, 106 a pool block's L1 tiles, 107 / 108 the
+ *             tile-group queue, 109 an early-combine token's experts, 110 an
+ *             early-combine deferred entry;
+ *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 203 a free
+ *             partial buffer, 204 a finished partial, 205 the epilogue's
+ *             rendezvous (amax exchange, staged weight scales). */
 int mm_moe_sync_status(const void* workspace, void* stream, int* where);
 
 /* Human-readable name of a return code. */
