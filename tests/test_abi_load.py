@@ -91,3 +91,35 @@ def test_binding_rejects_wrong_buffers_before_any_device_work(M):
         M.forward(torch.empty(T, H, dtype=torch.uint8), None, idx, None, None, None, None, None, None, H, I, E,
                   torch.empty(16, dtype=torch.uint8))
     assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG
+
+
+def test_options_struct_layout_matches_the_header(M, tmp_path):
+    """Every field of the ctypes mm_moe_options sits at the offset the C header
+    gives it, and the struct has the header's size (compiled with the host C
+    compiler), so a field added in one place only is caught on the CPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    names = [f[0] for f in M.mm_moe_options._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "mm_moe.h"', 'int main(void) {',
+             '  printf("%zu\\n", sizeof(mm_moe_options));']
+    lines += [f'  printf("%zu\\n", offsetof(mm_moe_options, {n}));' for n in names]
+    lines += ['  return 0;', '}']
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([cc, "-I", inc, str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(M.mm_moe_options)
+    for n, off in zip(names, got[1:]):
+        assert getattr(M.mm_moe_options, n).offset == off, n
+
+
+def test_default_options(M):
+    o = M.mm_moe_default_options()
+    assert (o.variant, o.fused, o.lag_units, o.wait_timeout_ms) == (M.MM_MOE_VARIANT_MX, 1, -1, 2000)
+    assert (o.cta_pairs, o.partials_bf16, o.precise_swiglu, o.x_bf16, o.early_combine) == (0, 0, 0, 0, 0)
+    assert o.activation_clamp == 0.0 and not o.timing_events
