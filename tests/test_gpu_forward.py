@@ -162,3 +162,31 @@ def test_fused_stream_parity_and_masking(M):
     g = torch.Generator().manual_seed(7)
     inp["topk_idx"][torch.rand(cfg.T, cfg.K, generator=g) < 0.15] = -1
     _full_check(M, cfg, inp, M.options(fused=1))
+
+
+@pytest.mark.parametrize("variant", ["mx", "f8"])
+def test_timing_events_do_not_change_the_result(M, variant):
+    """With events between its kernels the library launches them plainly, without
+    them programmatically (the GEMM and the combine start early and wait
+    in-kernel); NULL entries are skipped.  All three give the same bits."""
+    import ctypes
+    cfg = W.Config("ev", T=200, H=512, I=256, E=6, K=3, variant=variant, seed=61)
+    dev = to_dev(W.make_inputs(cfg, "cpu"))
+    var = M.MM_MOE_VARIANT_MX if variant == "mx" else M.MM_MOE_VARIANT_F8
+    a, _, prep, sa = run_forward(M, cfg, dev, M.options(var))
+    a = a.clone()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(M.MM_MOE_NUM_TIMING_EVENTS)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    outs = []
+    for handles in ([e.cuda_event for e in evs], [evs[0].cuda_event] + [None] * 4 + [evs[-1].cuda_event]):
+        arr = (ctypes.c_void_p * M.MM_MOE_NUM_TIMING_EVENTS)(*handles)
+        o = M.options(var)
+        o.timing_events = ctypes.cast(arr, ctypes.c_void_p)
+        b, _, _, sb = run_forward(M, cfg, dev, o, prepared=prep)
+        torch.cuda.synchronize()
+        assert sb[0] == 0, sb
+        outs.append(b.clone())
+    assert sa[0] == 0
+    assert all(torch.equal(a, b) for b in outs)
