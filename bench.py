@@ -1,6 +1,6 @@
 """Benchmark of the MoE-layer forward on GB300 (one JSON line on rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config flash] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config pro] [--impl ours|reference]
 
 A step is one forward of one MoE layer (dispatch, gather, L1 GEMM + SwiGLU +
 requant, L2 GEMM, combine) over one batch of T tokens of the named workload,
@@ -133,9 +133,13 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ accounting
 def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4, x_bf16: bool = False):
-    """Algorithmic bytes / FLOPs of one step and of the two GEMM kernels
-    (part_elem: bytes of one L2 partial, 4 for fp32, 2 for bf16; x_bf16: the
-    caller's x is bf16 and the gather quantises it)."""
+    """Bytes / FLOPs of one step.  step_bytes is the method's algorithmic traffic:
+    the weights + scales of every expert that receives a token, x + its scales,
+    topk_idx + topk_w and the bf16 output.  The *_impl_bytes figures add this
+    implementation's own traffic (pool rows, intermediate, partials) and are
+    reported beside it, never in place of it (part_elem: bytes of one L2
+    partial, 4 for fp32, 2 for bf16; x_bf16: the caller's x is bf16 and the
+    gather quantises it)."""
     T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
     valid = (idx >= 0) & (idx < E)
     touched = int(np.unique(idx[valid]).size)
@@ -153,14 +157,15 @@ def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4, x_bf16: bool =
     x_in = 2 * H if x_bf16 else x_b          # the caller's row of x
     step_bytes = touched * (w1_b + w2_b) + T * x_in + T * K * 8 + T * H * 2
     flops = 6.0 * pairs * H * I
-    l1_bytes = touched * w1_b + pairs * x_b + pairs * a_b
-    l2_bytes = touched * w2_b + pairs * a_b + pairs * H * part_elem
-    gather_bytes = pairs * (x_in + x_b)      # read the token's row, write its pool row
-    combine_bytes = pairs * H * part_elem + T * H * 2   # read the partials, write the output
+    # algorithmic bytes of the separate GEMM launches: their weight streams (+ x for L1)
+    l1_bytes = touched * w1_b + T * x_in + T * K * 8
+    l2_bytes = touched * w2_b
+    # this implementation's own traffic on top of the algorithmic bytes
+    impl = {"pool_rows_write_read": 2 * pairs * x_b, "intermediate_write_read": 2 * pairs * a_b,
+            "partials_write_read": 2 * pairs * H * part_elem}
     return {"touched_experts": touched, "pairs": pairs, "step_bytes": step_bytes, "flops": flops,
-            "gather_bytes": gather_bytes, "combine_bytes": combine_bytes,
-            "l1_bytes": l1_bytes, "l2_bytes": l2_bytes, "l1_flops": 4.0 * pairs * H * I,
-            "l2_flops": 2.0 * pairs * H * I}
+            "l1_bytes": l1_bytes, "l2_bytes": l2_bytes, "impl_bytes": impl,
+            "l1_flops": 4.0 * pairs * H * I, "l2_flops": 2.0 * pairs * H * I}
 
 
 def kernel_traffic(kernel: str, cfg_name: str):
@@ -330,14 +335,17 @@ def run_ours(args, ws_n, rank, local):
     l1_ms, l2_ms = float(stage_mean[2]), float(stage_mean[3])
     early = fused and bool(opt.early_combine)
     if fused:
-        # one launch runs gather, L1 and L2 (and the combine, when early): its bytes are all of them
+        # one launch runs gather, L1 and L2: the layer's algorithmic bytes all pass through it
+        # (the bf16 output is counted too, although the combine kernel after it writes that)
         dom, dom_ms = "fused", l1_ms + l2_ms
-        dom_bytes = acc["l1_bytes"] + acc["l2_bytes"] + acc["gather_bytes"] + (acc["combine_bytes"] if early else 0)
+        dom_bytes = acc["step_bytes"]
+        dom_flops = acc["flops"]
     else:
         # dominant kernel: the one with the largest share of the step
         dom = "l1" if l1_ms >= l2_ms else "l2"
         dom_ms = l1_ms if dom == "l1" else l2_ms
         dom_bytes = acc["l1_bytes"] if dom == "l1" else acc["l2_bytes"]
+        dom_flops = acc["l1_flops"] if dom == "l1" else acc["l2_flops"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     t_roof = max(acc["flops"] / (fp8 * 1e12), acc["step_bytes"] / (hbm * 1e9))
     tokens_per_s = ws_n * cfg.T / (step_ms * 1e-3)
@@ -378,18 +386,31 @@ def run_ours(args, ws_n, rank, local):
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": kernel_traffic(dom, cfg.name if args.partials == "fp32" else f"{cfg.name}:bf16-partials"),
                      "algorithmic_bytes_per_launch": dom_bytes,
-                     "peak_source": f"{pk_src} hbm_gbs (STREAM-style copy)"},
+                     "algorithmic_bytes_def": ("weights + scales of the touched experts, x + x_sf, topk_idx + topk_w, "
+                                               "bf16 out" if fused else
+                                               ("W1 + scales of the touched experts, x + x_sf, topk" if dom == "l1"
+                                                else "W2 + scales of the touched experts")),
+                     "launch_ms": dom_ms,
+                     "implementation_bytes_per_launch": (
+                         {k: v for k, v in acc["impl_bytes"].items()} if fused else None),
+                     "tensor_frac": dom_flops / (dom_ms * 1e-3) / (fp8 * 1e12),
+                     "peak_source": f"{pk_src} hbm_gbs (STREAM-style copy); tensor_frac against "
+                                    f"2 x {pk_src} bf16_tflops (nominal fp8/bf16 ratio)"},
         "e2e": {"value": ws_n * cfg.T / (e2e_step_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step_ms},
         "gpu_launches": (3 if early else (4 if fused else 6)) * K,   # dispatch x2, [gather], GEMM(s), [combine]
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_tokens)
+        result["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_tokens or CPU_TOKENS[cfg.name])
     return result
 
 
 # ------------------------------------------------------------------ oracle (CPU) runs
+# tokens the oracle baseline times once per workload: about 10-30 s of host work each
+CPU_TOKENS = {"tiny": 64, "flash": 16, "pro": 4, "decode": 16, "f8": 8}
+
+
 def oracle_tokens(cfg, inp, rows):
     import oracle as O
     bf16_x = inp["x_sf"] is None             # the layer quantises bf16 rows first: the oracle does too
@@ -407,18 +428,34 @@ def oracle_tokens(cfg, inp, rows):
     for e in np.unique(idx[idx >= 0]):
         experts(int(e))
     t0 = time.perf_counter()
+    c0 = time.process_time()
     if bf16_x:
         x, x_sf = O.quantise_x(x, cfg.variant)
     O.forward(range(len(rows)), x, x_sf, idx, w, experts, cfg.H, cfg.I, cfg.E, cfg.variant)
-    return time.perf_counter() - t0
+    dt = time.perf_counter() - t0
+    return dt, (time.process_time() - c0) / dt
+
+
+def blas_threads() -> str:
+    """numpy's BLAS thread setting as the environment fixes it (unset: the library's default)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return f"{var}={os.environ[var]}"
+    return "unset (numpy's BLAS default)"
 
 
 def cpu_baseline(cfg, inp, n_tokens):
     rows = list(range(min(n_tokens, cfg.T)))
-    dt = oracle_tokens(cfg, inp, rows)
-    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+    dt, busy = oracle_tokens(cfg, inp, rows)
+    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": round(busy, 2),
+            "cores_available": len(os.sched_getaffinity(0)), "blas_threads": blas_threads(),
+            "cores_def": "CPU seconds / wall seconds of the timed oracle call (the average number of "
+                         "busy host threads)",
             "kind": "oracle", "sample": f"first {len(rows)} tokens of the {cfg.name} workload "
-                                        f"({len(rows) * cfg.K} routed pairs), fp64 numpy, {dt:.1f} s"}
+                                        f"({len(rows) * cfg.K} routed pairs), fp64 numpy, {dt:.1f} s",
+            "full_T_extrapolated": {"seconds": dt * cfg.T / len(rows), "tokens_per_s": len(rows) / dt,
+                                    "how": f"linear in tokens: {dt:.2f} s x {cfg.T} / {len(rows)} "
+                                           f"(an extrapolation, not a measurement)"}}
 
 
 def run_reference(args, ws_n, rank):
@@ -434,21 +471,24 @@ def run_reference(args, ws_n, rank):
     rows = list(range(min(n, cfg.T)))
     used = sorted(set(int(e) for e in inp["topk_idx"][rows].cpu().numpy().ravel() if e >= 0))
     inp.update(W.make_weights(cfg, dev, experts=used))
-    times = []
+    times, busy = [], []
     for i in range(max(args.warmup, 0) + args.steps):
-        dt = oracle_tokens(cfg, inp, rows)
+        dt, b = oracle_tokens(cfg, inp, rows)
         if i >= args.warmup:
             times.append(dt)
+            busy.append(b)
     step_s = float(np.mean(times))
     v = len(rows) / step_s
-    cores = len(os.sched_getaffinity(0))
+    cores = round(float(np.mean(busy)), 2)
     return {"impl": "reference", "metric": "MoE-layer tokens/s (one MoE layer forward, 1 GPU per replica)",
             "value": v, "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded workload generator)",
             "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.K}",
                        "sample_tokens": len(rows), "x": args.x},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores,
+                             "cores_available": len(os.sched_getaffinity(0)), "blas_threads": blas_threads(),
+                             "kind": "oracle",
                              "sample": f"first {len(rows)} tokens per step ({len(rows) * cfg.K} pairs)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -458,7 +498,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="flash", choices=list(W.CONFIGS))
+    ap.add_argument("--config", default="pro", choices=list(W.CONFIGS),
+                    help="workload (default pro: the largest single-GPU configuration)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partials", default="fp32", choices=["fp32", "bf16"],
                     help="L2 partials: fp32 (default) or cast to bf16 before the combine")
@@ -466,9 +507,10 @@ def main():
                     help="fused stream: combine in the GEMM's epilogue warps (library default 1) or in a kernel after it")
     ap.add_argument("--x", default="fp8", choices=["fp8", "bf16"],
                     help="activations: fp8 codes + scales (default) or bf16, quantised inside the gather")
-    ap.add_argument("--cpu-tokens", type=int, default=16,
-                    help="tokens of the workload the oracle baseline times once (about 10 s of host work)")
-    ap.add_argument("--ref-tokens", type=int, default=4,
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="tokens of the workload the oracle baseline times once (0: a per-workload count "
+                         "sized for about 10-30 s of host work)")
+    ap.add_argument("--ref-tokens", type=int, default=2,
                     help="--impl reference: tokens of the workload the oracle processes per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,

@@ -40,8 +40,8 @@
  * Layouts (T tokens, H hidden, I intermediate, E experts, K top-k):
  *   x        u8  [T, H]          e4m3 codes
  *   x_sf     MX: u8 [T, H/32]    F8: f32 [T, H/128]
- *   topk_idx i32 [T, K]          expert of slot k; any value < 0 masks the slot;
- *                                values >= E are treated as masked and flagged
+ *   topk_idx i32 [T, K]          expert of slot k; -1 masks the slot; values < -1
+ *                                or >= E are treated as masked and flagged
  *                                (MM_MOE_ERR_BAD_ROUTING from mm_moe_sync_status)
  *   topk_w   f32 [T, K]          router weight of slot k
  *   w1       MX: u8 [E, 2I, H/2] (two e2m1 per byte, low nibble = even column)
@@ -73,7 +73,7 @@ extern "C" {
 #define MM_MOE_ERR_UNSUPPORTED 2          /* not an sm_103a/sm_100-family device, or option not built */
 #define MM_MOE_ERR_CUDA 3                 /* a CUDA runtime/driver call failed */
 #define MM_MOE_ERR_TIMEOUT 4              /* a device wait passed its deadline (sync_status only) */
-#define MM_MOE_ERR_BAD_ROUTING 5          /* topk_idx held values >= E (sync_status only) */
+#define MM_MOE_ERR_BAD_ROUTING 5          /* topk_idx held values >= E or < -1 (sync_status only) */
 #define MM_MOE_ERR_WORKSPACE_TOO_SMALL 6
 
 #define MM_MOE_VARIANT_MX 0
@@ -100,11 +100,8 @@ typedef struct mm_moe_options {
                                    completion than will ever arrive, so the call ends with
                                    MM_MOE_ERR_TIMEOUT after wait_timeout_ms (tests the device-side
                                    timeout path); 0 for normal use */
-  int cta_pairs;                /* MX variant: 2 = the GEMM CTAs run as 2-CTA clusters whose two CTAs take
-                                   neighbouring weight tiles of the same pool block and load each token
-                                   tile once for both (TMA multicast); 0 or 1 = one CTA per tile group
-                                   (default: the pair's lockstep costs more than the halved token reads
-                                   save on GB300).  The results are identical either way. */
+  int cta_pairs;                /* reserved: 0 (default) or 1; any other value makes mm_moe_forward
+                                   return MM_MOE_ERR_UNSUPPORTED */
   int partials_bf16;            /* 0 (default): the L2 epilogue writes fp32 partials [K, T, H] and the
                                    combine sums them in fixed k order; 1: the partials are cast to
                                    bf16 (round to nearest even) first, halving their traffic (the

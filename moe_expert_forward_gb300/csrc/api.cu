@@ -4,6 +4,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "internal.h"
 
@@ -85,6 +87,28 @@ const DevInfo& dev_info() {
     have[dev] = true;
   }
   return infos[dev];
+}
+
+cudaError_t configure_kernel(const void* fn, int want_regs, int smem_bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> g(mu);
+  if (done.count({fn, dev})) return cudaSuccess;
+  if (want_regs > 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != want_regs) return cudaErrorInvalidConfiguration;
+  }
+  if (smem_bytes > 0) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  done.insert({fn, dev});
+  return cudaSuccess;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -273,6 +297,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       !aligned(workspace, 256) || !aligned(w1_sfp, 16) || !aligned(w2_sfp, 16))
     return MM_MOE_ERR_INVALID_ARG;
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
+  // cta_pairs is reserved: 0 and 1 mean one CTA per tile group, anything else is not built
+  if (o.cta_pairs != 0 && o.cta_pairs != 1) return MM_MOE_ERR_UNSUPPORTED;
   // the F8 epilogue stages each task's weight scales in shared memory for up to kF8MaxKB k-blocks
   if (o.variant == MM_MOE_VARIANT_F8 && (H / 128 > kF8MaxKB || I / 128 > kF8MaxKB)) return MM_MOE_ERR_UNSUPPORTED;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
@@ -309,7 +335,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 o.cta_pairs == 2, clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm};
+                 clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm};
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
@@ -417,7 +443,7 @@ const char* mm_moe_status_string(int code) {
     case MM_MOE_ERR_UNSUPPORTED: return "unsupported device or option";
     case MM_MOE_ERR_CUDA: return "CUDA error";
     case MM_MOE_ERR_TIMEOUT: return "device wait timed out";
-    case MM_MOE_ERR_BAD_ROUTING: return "topk_idx holds expert ids >= E";
+    case MM_MOE_ERR_BAD_ROUTING: return "topk_idx holds expert ids >= E or < -1";
     case MM_MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     default: return "unknown status";
   }

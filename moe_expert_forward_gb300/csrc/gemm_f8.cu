@@ -42,7 +42,10 @@ constexpr int kWgtBytes = kBN * kBK;
 constexpr int kTmemCols = 512;
 constexpr int kMaxKB = kF8MaxKB;       // k-blocks of weight scales staged per task (H, I <= 8192)
 
-enum : int { kSiteEmpty = 201, kSiteFull = 202, kSitePEmpty = 203, kSitePFull = 204, kSiteAmax = 205 };
+enum : int {
+  kSiteEmpty = 201, kSiteFull = 202, kSitePEmpty = 203, kSitePFull = 204, kSiteAmax = 205,
+  kSiteDrainCopies = 211, kSiteDrainMma = 212
+};
 
 struct Args {
   int T, H, I, E, K;
@@ -76,8 +79,8 @@ struct SmemLayout {
   static constexpr int wsc = amax + 2 * 2 * 128 * 4;                   // [2 tasks][2 rows][kMaxKB] fp32
   static constexpr int meta = wsc + 2 * 2 * kMaxKB * 4;
   static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
-  // full[S], empty[S], pfull[2], pempty[2], epi, wsc
-  static constexpr int nbars = 2 * kStages + 6;
+  // full[S], empty[S], pfull[2], pempty[2], epi, wsc, drain
+  static constexpr int nbars = 2 * kStages + 7;
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pempty = pfull + 2;
   uint64_t* epibar = pempty + 2;
   uint64_t* wscbar = epibar + 1;
+  uint64_t* drain = wscbar + 1;   // the MMA issuer's last commit
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(epibar, 256);
     mbar_init(wscbar, 256);
+    mbar_init(drain, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -183,6 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* tk = smem + SmemLayout::tok + p * kTokBytes;
       uint8_t* wgp = smem + SmemLayout::wgt + p * kWgtBytes;
       int step = 0;
+      bool armed = false;                       // a phase of full[p] was armed: its copies land before exit
+      uint32_t armed_parity = 0;
       for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
         int e, n, b, valid;
         decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
@@ -194,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t phase = ((step + kb) / kStages) & 1;
           if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
           mbar_arrive_expect_tx(&full[p], bytes);
+          armed = true;
+          armed_parity = phase;
           const int kc = kb * kBK;
           tma_load_2d(tk, tt, &full[p], kc, b * kBT, pol_t);
           if (PHASE == 1) tma_load_3d(wgp, &tmW, &full[p], kc, e * 2 * args.I + n * 128, 0, pol_w);
@@ -201,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         step += KB;
       }
+      if (armed) mbar_wait_drain(&full[p], armed_parity, st, kSiteDrainCopies);
     }
   } else if (wg == 3) {
     regs_dec_mma();
@@ -233,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
+      // every MMA this thread issued has completed before TMEM is freed
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, st, kSiteDrainMma);
       if (kProf) {
         args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
         args.prof[blockIdx.x * 8 + 1] = c_pe;
@@ -386,15 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kProf) { e_math += tr0 - tw2; e_rdv += clock64() - tr0; }
         amax = fmaxf(amax, xa[(half ^ 1) * 128 + m]);
         if (live) {
+          // s = amax / 448 and each code RNE_e4m3(a / s), both quotients IEEE-rounded
+          // (DeepGEMM PR #440: the scale is the raw amax / 448 and the value is divided by it)
           const float sf = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-          // x * (1/s) instead of x / s: the fp32 quotient moves by at most about an ulp,
-          // which changes an e4m3 code only within ~2^-20 of a rounding boundary
-          const float rsf = __frcp_rn(sf);
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const uint32_t lo = cvt_e4m3x2(acc0[4 * i] * rsf, acc0[4 * i + 1] * rsf);
-            const uint32_t hi = cvt_e4m3x2(acc0[4 * i + 2] * rsf, acc0[4 * i + 3] * rsf);
+            const uint32_t lo = cvt_e4m3x2(__fdiv_rn(acc0[4 * i], sf), __fdiv_rn(acc0[4 * i + 1], sf));
+            const uint32_t hi = cvt_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sf), __fdiv_rn(acc0[4 * i + 3], sf));
             packed[i] = lo | (hi << 16);
           }
           uint4* dst = reinterpret_cast<uint4*>(args.out_codes + row * args.I + n * 128 + 64 * half);
@@ -438,11 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // the producers and the MMA issuer have waited for the async work they issued
   __syncthreads();
-  if (*s_abort) {
-    const uint64_t t0 = globaltimer();
-    while (globaltimer() - t0 < 200000) {}
-  }
   if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -456,16 +465,9 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   const bool prof = g.prof != nullptr;
   auto kernel = prof ? gemm_f8_kernel<PHASE, true> : gemm_f8_kernel<PHASE, false>;
   // The register split assumes the kernel starts with exactly kLaunchRegs per thread.
-  static int checked[2][2] = {{0, 0}, {0, 0}};
-  if (!checked[PHASE - 1][prof]) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::total(kMaxE) + 1024);
-    if (e != cudaSuccess) return e;
-    checked[PHASE - 1][prof] = 1;
-  }
+  if (cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kernel), kLaunchRegs,
+                                       SmemLayout::total(kMaxE) + 1024))
+    return e;
   CUtensorMap tmW;
   TokenMaps tmT;
   Args a{};

@@ -87,7 +87,8 @@ constexpr int kSfColsPerStage = 12;    // 4 (tokens) + 8 (weights)
 // wait-site codes reported through the status word
 enum : int {
   kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104,
-  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108, kSiteCombine = 109, kSiteDeferred = 110
+  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108, kSiteCombine = 109, kSiteDeferred = 110,
+  kSiteDrainCopies = 111, kSiteDrainMma = 112
 };
 
 struct Args {
@@ -143,7 +144,8 @@ struct SmemLayout {
   static constexpr int meta = sfw + kStages * 2 * kSFChunk;   // blk_off[E+1], cnt[E], queue[kQueue]
   static constexpr int meta_ints(int E) { return (E + 1) + E + kQueue; }
   static constexpr int bars_after_meta(int E) { return meta + (meta_ints(E) * 4 + 15) / 16 * 16; }
-  static constexpr int nbars = 2 * kStages + 2 + 2 * kQueue;  // full[S], empty[S], tfull, tempty, qfull, qempty
+  // full[S], empty[S], tfull, tempty, qfull[Q], qempty[Q], drain
+  static constexpr int nbars = 2 * kStages + 2 + 2 * kQueue + 1;
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -344,11 +346,7 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 
 // kProf: record per-role wait and busy times (debug_flags bit 1).  A separate
 // instantiation, because even untaken timing branches slow the MMA issue loop.
-// kPair: the CTAs run as 2-CTA clusters.  The two CTAs of a pair take the same
-// tile group and compute its weight tiles 2p and 2p + 1; each loads half of
-// every token tile with a multicast copy into both, so the pair reads each
-// token tile from L2 once, and each MMA commit releases the stage in both CTAs.
-template <bool kProf, bool kPair>
+template <bool kProf>
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ Maps maps, const Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -360,9 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = tfull + 1;
-  const uint32_t rank = kPair ? cluster_rank() : 0;
-  const Queue q{tempty + 1, tempty + 1 + kQueue, s_cnt + E, kPair, rank,
-                kPair ? cluster_map(tempty + 1 + kQueue, 0) : 0u};
+  const Queue q{tempty + 1, tempty + 1 + kQueue, s_cnt + E};
+  uint64_t* drain = tempty + 1 + 2 * kQueue;   // the MMA issuer's last commit
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -374,13 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kPair ? 2 : 1);   // a pair's stage is free once both MMA issuers released it
+      mbar_init(&empty[i], 1);
     }
     mbar_init(tfull, 1);
     mbar_init(tempty, kEpiWarps);
+    mbar_init(drain, 1);
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(&q.full[i], 1);
-      mbar_init(&q.empty[i], kQueueConsumers * (kPair ? 2 : 1));
+      mbar_init(&q.empty[i], kQueueConsumers);
     }
     *s_abort = 0;
     fence_mbar_init();
@@ -398,15 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   pdl_wait();
   for (int i = threadIdx.x; i <= E; i += kThreads) s_blk[i] = args.blk_off[i];
   for (int i = threadIdx.x; i < E; i += kThreads) s_cnt[i] = args.cnt[i];
-  __syncthreads();
   tc_fence_before();
-  if (kPair) cluster_sync();   // the partner's barriers exist before anything targets them
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
   const int nblk = s_blk[E];
-  const Sched sch{s_blk, s_cnt, E, args.NB1, args.NB2, args.mode, lag, kPair ? 2 : 1, static_cast<int>(rank)};
+  const Sched sch{s_blk, s_cnt, E, args.NB1, args.NB2, args.mode, lag};
 
   const int wg = warp >> 2;
   // setmaxnreg sits inside each warpgroup's branch: after a join ptxas would
@@ -425,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       uint8_t* sw = smem + SmemLayout::sfw + p * 2 * kSFChunk;
       uint64_t w_empty = 0;
       int step = 0;                             // global k-block step of this CTA
+      bool armed = false;                       // a phase of full[p] was armed: its copies land before exit
+      uint32_t armed_parity = 0;
       for (Cursor c; !*s_abort && sch.next(c, q, st, s_abort, false, lane);) {
         const Task& t = c.t;
         const bool l1 = t.type == 1;
@@ -442,9 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                                               : (t.valid <= 64 ? (l1 ? &maps.x64 : &maps.a64)
                                                                : (l1 ? &maps.x128 : &maps.a128));
         const int rows = t.valid <= 32 ? 32 : (t.valid <= 64 ? 64 : 128);
-        // a pair: each CTA copies rows/2 rows into both; a 32-row tile comes whole from rank 0
-        const CUtensorMap* th = rows == 128 ? (l1 ? &maps.x64 : &maps.a64) : (l1 ? &maps.x32 : &maps.a32);
-        const uint32_t bytes = rows * kBK + (t.ghost ? 0u : kWgtTxBytes + 2 * kSFChunk) + kSFChunk;
+        const uint32_t bytes = rows * kBK + kWgtTxBytes + 2 * kSFChunk + kSFChunk;
         const uint8_t* sfw = (l1 ? args.sfw1 : args.sfw2) +
                              (static_cast<size_t>(t.e) * (l1 ? args.NB1 : args.NB2) + t.n) * KB * 2 * kSFChunk;
         const uint8_t* sft = (l1 ? args.pool_x_sf : args.pool2_sf) + static_cast<size_t>(t.b) * KB * kSFChunk;
@@ -454,32 +450,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
           if (kProf) w_empty += globaltimer() - t0;
           mbar_arrive_expect_tx(&full[p], bytes);
+          armed = true;
+          armed_parity = phase;
           const int kbe = t.rev ? KB - 1 - kb : kb;   // the k-block this stage carries
           const int kc = kbe * kBK;
-          if (!kPair) {
-            tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
-          } else if (rows >= 64) {
-            const int h = rows / 2;
-            tma_load_2d_mc(tk + rank * h * kBK, th, &full[p], kc, t.b * kBT + static_cast<int>(rank) * h, 0x3,
-                           pol_t);
-          } else if (rank == 0) {
-            tma_load_2d_mc(tk, tt, &full[p], kc, t.b * kBT, 0x3, pol_t);
-          }
+          tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
           bulk_load(st_, sft + static_cast<size_t>(kbe) * kSFChunk, kSFChunk, &full[p]);
-          if (!t.ghost) {
-            const uint64_t pw = t.last ? pol_w : pol_wk;
-            if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pw);
-            else tma_load_2d(wg, &maps.w2, &full[p], kc, t.e * args.H + t.n * kBN, pw);
-            bulk_load(sw, sfw + static_cast<size_t>(kbe) * 2 * kSFChunk, 2 * kSFChunk, &full[p]);
-          }
+          const uint64_t pw = t.last ? pol_w : pol_wk;
+          if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pw);
+          else tma_load_2d(wg, &maps.w2, &full[p], kc, t.e * args.H + t.n * kBN, pw);
+          bulk_load(sw, sfw + static_cast<size_t>(kbe) * 2 * kSFChunk, 2 * kSFChunk, &full[p]);
         }
         step += KB;
       }
-      if (kPair) {
-        // the partner's last release of this stage must land before the CTA may exit
-        const int j = step + ((p - step) % kStages + kStages) % kStages;
-        mbar_wait(&empty[p], ((j / kStages) & 1) ^ 1, st, s_abort, kSiteEmpty);
-      }
+      // the copies of the last armed phase have landed before the shared memory goes away
+      // (at once on a normal exit, where the MMA issuer consumed every phase)
+      if (armed) mbar_wait_drain(&full[p], armed_parity, st, kSiteDrainCopies);
       if (kProf) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
     }
   } else if (wg == 3) {
@@ -532,8 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)   // K advances 32 bytes = 2 descriptor units
                 tc_mma_mxf8f6f4(tmem, da + 2 * kk, db + 2 * kk, make_idesc(kk), sft_col, sfw_col, (kb | kk) != 0);
-              if (kPair) tc_commit_mc(&empty[s], 0x3);
-              else tc_commit(&empty[s]);
+              tc_commit(&empty[s]);
               if (++kb == KB) {
                 tc_commit(tfull);
                 kb = 0;
@@ -545,6 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         phase ^= 1;
       }
+      // every MMA and scale copy this thread issued has completed before TMEM is freed
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, st, kSiteDrainMma);
       if (kProf) {
         args.prof[blockIdx.x * 8 + 1] = w_full;
         args.prof[blockIdx.x * 8 + 2] = w_tempty;
@@ -556,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     __syncwarp();
     } else if (warp < kGatherWarp0 + kGatherWarps && args.mode == 3) {
       gather_rows(args, s_blk, s_cnt, sch, s_abort, warp - kGatherWarp0, lane, nblk);
-    } else if (warp == kSchedWarp && lane == 0 && rank == 0) {
+    } else if (warp == kSchedWarp && lane == 0) {
       // ------------------------------------------------------------------ tile-group scheduler
       // Every dependency of a group (the gather and L1 tiles of the blocks an
       // L2 group reads) has a smaller index, so the group with the smallest
@@ -574,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     uint64_t w_tfull = 0, busy = 0;
     for (Cursor c; sch.next(c, q, st, s_abort, true, lane); ++it) {
       const Task& t = c.t;
-      const bool live = !t.ghost && m < t.valid;
+      const bool live = m < t.valid;
       const size_t row = static_cast<size_t>(t.b) * kBT + m;
       const int s = live ? __ldg(args.src + row) : 0;
       const float w = (t.type == 1 && live) ? __ldg(args.topk_w + s) : 0.f;   // loaded before the wait
@@ -603,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                          (m & 31) * 16 + (m >> 5) * 4;
         l1_block(r0, r2, 2 * half, live, w, row, t.n, args, crow, sfrow);
         l1_block(r1, r3, 2 * half + 1, live, w, row, t.n, args, crow, sfrow);
-        if (args.mode == 3 && !t.ghost) {
+        if (args.mode == 3) {
           fence_proxy_async_global();              // the codes are read by TMA later
           __syncwarp();
           if (lane == 0) red_release_gpu_add(args.ctr_l1 + t.b, 1);
@@ -631,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             }
           }
         }
-        if (args.early_combine && !t.ghost) {
+        if (args.early_combine) {
           __syncwarp();   // the warp's partial stores before its release
           if (lane == 0) red_release_gpu_add(args.ctr_l2 + t.e, 1);
         }
@@ -648,13 +636,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     }
   }
 
+  // every role has waited for the async work it issued (above), so after this
+  // barrier no copy or MMA still targets this CTA's shared or tensor memory
   __syncthreads();
-  if (*s_abort) {
-    // let in-flight bulk copies and MMAs land before the TMEM and smem go away
-    const uint64_t t0 = globaltimer();
-    while (globaltimer() - t0 < 200000) {}
-  }
-  if (kPair) cluster_sync();   // neither CTA of a pair leaves while the other may still target it
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -727,58 +711,18 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   }
   using KernelFn = void (*)(Maps, Args);
   const bool prof = a.prof != nullptr;
-  const KernelFn kernels[2][2] = {{gemm_mx_kernel<false, false>, gemm_mx_kernel<false, true>},
-                                  {gemm_mx_kernel<true, false>, gemm_mx_kernel<true, true>}};
-  static int configured[2][2] = {{-1, -1}, {-1, -1}};
-  static int max_pairs[2] = {0, 0};   // co-resident 2-CTA clusters (per device last configured)
+  const KernelFn kernels[2] = {gemm_mx_kernel<false>, gemm_mx_kernel<true>};
   const size_t smem = SmemLayout::total(L.E) + 1024;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  for (int pv = 0; pv < 2; ++pv) {
-    int& conf = configured[prof][pv];
-    if (conf == dev) continue;
-    // the setmaxnreg split assumes exactly kLaunchRegs registers a thread at launch
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kernels[prof][pv]);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kernels[prof][pv], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SmemLayout::total(kMaxE) + 1024);
-    if (e != cudaSuccess) return e;
-    if (pv == 1) {
-      cudaLaunchConfig_t q = {};
-      q.gridDim = dim3(2);
-      q.blockDim = dim3(kThreads);
-      q.dynamicSmemBytes = SmemLayout::total(kMaxE) + 1024;
-      cudaLaunchAttribute ca;
-      ca.id = cudaLaunchAttributeClusterDimension;
-      ca.val.clusterDim.x = 2; ca.val.clusterDim.y = 1; ca.val.clusterDim.z = 1;
-      q.attrs = &ca;
-      q.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernels[prof][pv], &q) != cudaSuccess) {
-        cudaGetLastError();   // no clusters on this device: pairs stay off
-        n = 0;
-      }
-      max_pairs[prof] = n;
-    }
-    conf = dev;
-  }
-  // CTA pairs need an even grid of co-resident clusters
-  int grid = g.grid;
-  bool pair = g.pair && max_pairs[prof] > 0;
-  if (pair) {
-    grid = grid < 2 * max_pairs[prof] ? grid : 2 * max_pairs[prof];
-    grid &= ~1;
-    pair = grid >= 2;
-    if (!pair) grid = g.grid;
-  }
+  // the setmaxnreg split assumes exactly kLaunchRegs registers a thread at launch
+  if (cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kernels[prof]), kLaunchRegs,
+                                       SmemLayout::total(kMaxE) + 1024))
+    return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(g.grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   int na = 0;
   if (mode == 3) {
     // the fused stream waits across CTAs: launch cooperatively so that every CTA is resident
@@ -792,14 +736,9 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (pair) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 2; attr[na].val.clusterDim.y = 1; attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kernels[prof][pair ? 1 : 0], maps, a);
+  return cudaLaunchKernelEx(&cfg, kernels[prof], maps, a);
 }
 
 }  // namespace mm

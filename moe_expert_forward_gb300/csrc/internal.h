@@ -62,6 +62,12 @@ struct DevInfo {
 };
 const DevInfo& dev_info();
 
+// Once per kernel and device (thread-safe): when want_regs > 0, fail with
+// cudaErrorInvalidConfiguration unless the kernel was built with exactly that
+// many registers a thread (the setmaxnreg splits depend on it); when
+// smem_bytes > 0, raise the kernel's dynamic shared-memory limit to it.
+cudaError_t configure_kernel(const void* fn, int want_regs, int smem_bytes);
+
 // ---- launchers (return cudaError_t of the launch)
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
                             int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
@@ -94,7 +100,6 @@ struct GemmLaunch {
   unsigned long long* prof; // per-CTA role timings (debug_flags bit 1) or null
   uint64_t timeout_ns;
   int grid;
-  bool pair;                // run as 2-CTA clusters sharing token tiles (when the device allows)
   float clamp;              // activation clamp of gate and up (+inf: none)
   int precise;              // SwiGLU with expf and the IEEE division instead of the fast-math form
   bool early_combine;       // fused stream: the epilogue warps combine tokens once their experts are done

@@ -203,15 +203,9 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int bl
   CH = (CH + 32 * kDispatchWarps - 1) / (32 * kDispatchWarps) * (32 * kDispatchWarps);
   if (CH == 0) CH = 32 * kDispatchWarps;
   const size_t smem_assign = static_cast<size_t>(kDispatchWarps + 3) * E * sizeof(int) + 16;
-  static int configured_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(dispatch_assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (kDispatchWarps + 3) * kMaxE * static_cast<int>(sizeof(int)) + 16);
-    if (e != cudaSuccess) return e;
-    configured_dev = dev;
-  }
+  if (cudaError_t e = configure_kernel(reinterpret_cast<const void*>(dispatch_assign_kernel), 0,
+                                       (kDispatchWarps + 3) * kMaxE * static_cast<int>(sizeof(int)) + 16))
+    return e;
   dispatch_count_kernel<<<G, kDispatchThreads, E * sizeof(int), s>>>(topk_idx, TK, E, CH, scratch, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

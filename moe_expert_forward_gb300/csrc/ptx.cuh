@@ -83,6 +83,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Wait used while a CTA winds down, for async work this thread issued itself
+// (bulk copies landing on a stage's barrier, MMAs behind a commit): it ignores
+// the abort flag, and after `ns` it records MM_MOE_ERR_TIMEOUT at `where` (unless
+// an earlier error holds the status word) and returns false.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const Status& st, int where) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer() - t0 > st.timeout_ns) {
+      report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, where);
+      return false;
+    }
+  }
+  return true;
+}
+
 // 32-byte global store of v[0..8) at a 32-byte aligned address.
 __device__ __forceinline__ void st_global_v8(float* p, const float* v) {
   asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
@@ -120,69 +137,6 @@ __device__ __forceinline__ void st_bf16x32(__nv_bfloat16* p, const float* v) {
   }
   st_global_v8(reinterpret_cast<float*>(p), w);
   st_global_v8(reinterpret_cast<float*>(p) + 8, w + 8);
-}
-
-// ------------------------------------------------------------------ thread-block clusters
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of both CTAs: prior shared-memory work (and remote arrivals) of
-// each CTA is visible to the other afterwards.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t caddr, int v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait with cluster-scope acquire, for a phase completed by the other CTA.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const Status& st,
-                                                  volatile int* abort, int where) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait_cluster(a, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cluster(a, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > st.timeout_ns) {
-      report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, where);
-      *abort = 1;
-      return false;
-    }
-  }
-}
-// TMA tile load delivered to the same shared-memory offset, and completing the
-// mbarrier at the same offset, in every CTA of `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1,
-                                               uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
-      : "memory");
 }
 
 // ------------------------------------------------------------------ cross-CTA counters
@@ -304,13 +258,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
-               : "memory");
-}
-// Like tc_commit, arriving on the mbarrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(mask)
                : "memory");
 }
 // Copy a 32-row x 128-bit matrix from shared memory to TMEM, replicated into all

@@ -13,7 +13,6 @@ struct Task {
   int type;      // 1 = L1, 2 = L2
   int e, n, b, valid;
   bool last;     // the last pool block of its tile group
-  bool ghost;    // CTA pairs: tile n does not exist (odd tile count); the CTA only helps load tokens
   bool rev;      // walk the contraction from its last k-block down (odd blocks of a group)
 };
 
@@ -39,25 +38,14 @@ struct Cursor {
 // every consumer has released it.
 struct Queue {
   uint64_t* full;       // [kQueue], one arrival: the slot holds a group
-  uint64_t* empty;      // [kQueue], kQueueConsumers arrivals (x2 for a CTA pair): the slot is free
+  uint64_t* empty;      // [kQueue], kQueueConsumers arrivals: the slot is free
   volatile int* g;      // [kQueue]
-  // CTA pairs: both CTAs read the same groups.  Rank 0's scheduler fills both
-  // queues; rank 1's consumers release slots on rank 0's `empty` (cluster
-  // address of its first barrier, 8 bytes apart).
-  bool pair;
-  uint32_t rank;
-  uint32_t empty0;
 };
 
 struct Sched {
   const int* blk;   // [E+1] pool-block offsets per expert
   const int* cnt;   // [E]
   int E, NB1, NB2, mode, lag;
-  int pair = 1;     // CTAs per tile group: 2 = a cluster pair taking tiles 2p and 2p + 1
-  int rank = 0;     // this CTA's rank in the pair
-
-  // tile groups per expert: the pair's tile count
-  __device__ __forceinline__ int npairs(int nb) const { return (nb + pair - 1) / pair; }
 
   __device__ __forceinline__ int largest_leq(const int* a, int n, int v, int scale) const {
     int lo = 0, hi = n - 1;                  // largest i < n with a[i] * scale <= v
@@ -68,22 +56,21 @@ struct Sched {
     return lo;
   }
   __device__ __forceinline__ int groups() const {
-    return mode == 1 ? E * npairs(NB1) : (mode == 2 ? E * npairs(NB2) : E * (npairs(NB1) + npairs(NB2)));
+    return mode == 1 ? E * NB1 : (mode == 2 ? E * NB2 : E * (NB1 + NB2));
   }
   // mode 3: groups in the segments before segment u
   __device__ __forceinline__ int groups_before(int u) const {
     const int l1 = u < E ? u : E;
     int l2 = u - lag;
     l2 = l2 < 0 ? 0 : (l2 > E ? E : l2);
-    return l1 * npairs(NB1) + l2 * npairs(NB2);
+    return l1 * NB1 + l2 * NB2;
   }
   __device__ __forceinline__ void group(int g, Task& t) const {
     if (mode != 3) {
-      const int nbw = npairs(mode == 1 ? NB1 : NB2);
+      const int nbw = mode == 1 ? NB1 : NB2;
       t.type = mode;
       t.e = g / nbw;
-      t.n = (g - t.e * nbw) * pair + rank;
-      t.ghost = t.n >= (mode == 1 ? NB1 : NB2);
+      t.n = g - t.e * nbw;
       return;
     }
     int lo = 0, hi = E + lag - 1;            // the segment holding group g
@@ -92,9 +79,9 @@ struct Sched {
       if (groups_before(mid) <= g) lo = mid; else hi = mid - 1;
     }
     const int r = g - groups_before(lo);
-    const int n1 = lo < E ? npairs(NB1) : 0;
-    if (r < n1) { t.type = 1; t.e = lo; t.n = r * pair + rank; t.ghost = t.n >= NB1; }
-    else { t.type = 2; t.e = lo - lag; t.n = (r - n1) * pair + rank; t.ghost = t.n >= NB2; }
+    const int n1 = lo < E ? NB1 : 0;
+    if (r < n1) { t.type = 1; t.e = lo; t.n = r; }
+    else { t.type = 2; t.e = lo - lag; t.n = r - n1; }
   }
   __device__ __forceinline__ void block(Cursor& c) const {
     c.t.b = blk[c.t.e] + c.bl;
@@ -123,11 +110,9 @@ struct Sched {
     ++c.i;
     int g = -1;
     if (!warp_wide || lane == 0) {
-      if (q.pair ? mbar_wait_cluster(&q.full[slot], parity, st, abort, site)
-                 : mbar_wait(&q.full[slot], parity, st, abort, site)) {
+      if (mbar_wait(&q.full[slot], parity, st, abort, site)) {
         g = q.g[slot];
-        if (q.pair && q.rank != 0) mbar_arrive_cluster(q.empty0 + 8 * slot);
-        else mbar_arrive(&q.empty[slot]);
+        mbar_arrive(&q.empty[slot]);
       }
     }
     if (warp_wide) g = __shfl_sync(0xffffffffu, g, 0);
@@ -142,7 +127,7 @@ struct Sched {
 };
 
 
-// The scheduler thread of a CTA (of rank 0 of a pair, which deals for both).  Tile groups are taken from one counter shared
+// The scheduler thread of a CTA.  Tile groups are taken from one counter shared
 // by all CTAs, in increasing order, so CTAs that are free start neighbouring
 // groups at about the same time: an expert's token block is read by its tiles
 // while it is still in L2, and no CTA is left with a longer tail of static
@@ -163,10 +148,6 @@ __device__ __forceinline__ void run_scheduler(const Sched& sch, const Queue& q, 
       }
     }
     q.g[slot] = g;
-    if (q.pair) {   // the partner's copy of the slot, then its barrier (release orders the store)
-      st_cluster_u32(cluster_map(const_cast<int*>(&q.g[slot]), 1), g);
-      mbar_arrive_cluster(cluster_map(&q.full[slot], 1));
-    }
     mbar_arrive(&q.full[slot]);
     if (g < 0) break;
   }

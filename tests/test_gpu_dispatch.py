@@ -69,8 +69,9 @@ def test_dispatch_ragged_masked(M, seed, block):
     assert np.array_equal(src[:len(ref["src"])], ref["src"])
 
 
-def test_dispatch_flags_out_of_range_experts(M):
-    idx = np.array([[0, 3], [9, 1], [2, -1]], dtype=np.int32)
+@pytest.mark.parametrize("bad", [9, -2])
+def test_dispatch_flags_out_of_range_experts(M, bad):
+    idx = np.array([[0, 3], [bad, 1], [2, -1]], dtype=np.int32)
     cnt, blk, slot, src, st = _dispatch(M, idx, 4, 16)
     ref = O.route(idx, 4, 16)
     assert st == M.MM_MOE_ERR_BAD_ROUTING

@@ -1,6 +1,6 @@
 """The fused stream's early combine (epilogue warps reduce the tokens whose
 experts have finished L2, instead of a combine launch after the GEMM) gives
-the combine kernel's bits, with fp32 and bf16 partials, with CTA pairs, with
+the combine kernel's bits, with fp32 and bf16 partials, with
 masked slots, many empty experts and the largest top-k, and at full size; it
 is also checked against the oracle through every other fused-path test, which
 run with it on (the default)."""
@@ -43,7 +43,7 @@ CASES = [
     ("tiny", W.CONFIGS["tiny"], {}, None),
     ("ragged", W.Config("ragged", T=300, H=512, I=384, E=5, K=2, seed=21), {}, None),
     ("ragged-bf16-partials", W.Config("ragged", T=300, H=512, I=384, E=5, K=2, seed=21), {"partials_bf16": 1}, None),
-    ("pairs", W.Config("k3", T=120, H=384, I=256, E=6, K=3, seed=41), {"cta_pairs": 2}, None),
+    ("k3", W.Config("k3", T=120, H=384, I=256, E=6, K=3, seed=41), {}, None),
     ("masked", W.Config("masked", T=200, H=256, I=256, E=8, K=4, seed=48), {}, _masked),
     ("e1024", W.Config("e1024", T=96, H=256, I=128, E=1024, K=4, seed=34), {}, None),
     ("k16", W.Config("k16", T=40, H=256, I=256, E=32, K=16, seed=35), {}, None),

@@ -1,7 +1,7 @@
 """Edge cases of the forward against the oracle: an empty batch, fully masked
 routing, top-k equal to the number of experts, the largest expert count and the
 largest top-k the library accepts, in both GEMM paths (fused stream and two
-launches), with CTA pairs where they apply, and in the FP8 variant."""
+launches), and in the FP8 variant."""
 import numpy as np
 import pytest
 import torch
@@ -32,7 +32,7 @@ def _check_all_rows(M, cfg, inp, opt):
     return check_output(out.float().cpu().numpy(), ref, cfg.name)
 
 
-MODES = [dict(fused=1), dict(fused=0), dict(fused=1, cta_pairs=2)]
+MODES = [dict(fused=1), dict(fused=0)]
 
 
 @pytest.mark.parametrize("variant", ["mx", "f8"])
@@ -57,14 +57,14 @@ def test_all_routing_masked_gives_zeros(M, variant):
         assert torch.count_nonzero(out.float()).item() == 0, kw
 
 
-@pytest.mark.parametrize("kw", MODES, ids=["fused", "two-launch", "pairs"])
+@pytest.mark.parametrize("kw", MODES, ids=["fused", "two-launch"])
 def test_topk_equals_experts(M, kw):
     """Every token goes to every expert: each expert gets all T rows (two blocks here)."""
     cfg = W.Config("k_eq_e", T=160, H=256, I=256, E=4, K=4, seed=33)
     _check_all_rows(M, cfg, W.make_inputs(cfg, "cpu"), _opt(M, cfg, **kw))
 
 
-@pytest.mark.parametrize("kw", MODES, ids=["fused", "two-launch", "pairs"])
+@pytest.mark.parametrize("kw", MODES, ids=["fused", "two-launch"])
 def test_largest_expert_count(M, kw):
     """E = 1024 (the largest the library takes): most experts get no token, the
     shared-memory tables are at their largest, and the default lag (E) is the largest."""

@@ -39,12 +39,20 @@ def test_unreachable_wait_times_out_and_context_survives(M):
     check_output(out2.float().cpu().numpy(), ref, "after timeout")
 
 
-def test_bad_routing_is_reported(M):
+@pytest.mark.parametrize("bad", [11, -2, -7])
+def test_bad_routing_is_reported(M, bad):
+    """Expert ids >= E or < -1 are masked (the slot contributes nothing) and flagged."""
     cfg = W.Config("tiny", T=64, H=256, I=128, E=8, K=2, seed=3)
     inp = W.make_inputs(cfg, "cpu")
-    inp["topk_idx"][5, 1] = 11                  # >= E: masked and flagged
-    out, ws, prep, (code, where) = run_forward(M, cfg, to_dev(inp))
+    inp["topk_idx"][5, 1] = bad
+    dev = to_dev(inp)
+    out, ws, prep, (code, where) = run_forward(M, cfg, dev)
     assert code == M.MM_MOE_ERR_BAD_ROUTING
+    # the flagged slot is masked exactly as -1 would be
+    masked = {k: v.clone() for k, v in dev.items()}
+    masked["topk_idx"][5, 1] = -1
+    out_m, _, _, (code_m, _) = run_forward(M, cfg, masked, prepared=prep)
+    assert code_m == 0 and torch.equal(out, out_m)
 
 
 def test_host_rejections(M):

@@ -42,7 +42,9 @@ def _full_check(M, cfg, inp, opt=None):
     assert code == 0, f"device status {code} at site {where}"
     cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt)
     ref_route = O.route(inp["topk_idx"].numpy(), cfg.E, bm)
+    assert np.array_equal(cnt, ref_route["cnt"]) and np.array_equal(blk, ref_route["blk_off"])
     assert np.array_equal(slot, ref_route["slot"])
+    assert np.array_equal(src[:len(ref_route["src"])], ref_route["src"])
     rows = np.arange(cfg.T)
     ref, inter = oracle_rows(cfg, dev, rows)
     got = out.float().cpu().numpy()
@@ -135,25 +137,16 @@ def test_fused_stream_bitwise_equals_two_launch_path(M, name, lag):
     assert torch.equal(rows, pb.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()])
 
 
-@pytest.mark.parametrize("fused", [0, 1])
-@pytest.mark.parametrize("name", ["tiny", "ragged", "manyexp", "k1"])
-def test_cta_pairs_bitwise_equal_single_ctas(M, name, fused):
-    """2-CTA clusters (each CTA loading half of every token tile into both, one
-    weight tile each; tiny has an odd tile count, so one CTA of the last pair
-    only helps load) compute every tile exactly as single CTAs do."""
-    cfg = SMALL[name]
+@pytest.mark.parametrize("pairs", [2, 3, -1])
+def test_reserved_cta_pairs_values_are_rejected(M, pairs):
+    """cta_pairs is reserved: only 0 and 1 are accepted, before any launch."""
+    cfg = SMALL["tiny"]
     dev = to_dev(W.make_inputs(cfg, "cpu"))
-    out_a, ws_a, prep, st_a = run_forward(M, cfg, dev, M.options(fused=fused, cta_pairs=0))
-    out_a = out_a.clone()
-    out_b, ws_b, _, st_b = run_forward(M, cfg, dev, M.options(fused=fused, cta_pairs=2), prepared=prep)
-    assert st_a[0] == 0 and st_b[0] == 0, (st_a, st_b)
-    assert torch.equal(out_a, out_b)
-    opt = M.options()
-    pa = M.workspace_view(ws_a, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "pool2")
-    pb = M.workspace_view(ws_b, opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, "pool2")
-    _, blk, _, src, _ = read_routing(M, cfg, ws_a, opt)
-    live = torch.from_numpy(src[:blk[-1] * 128] >= 0)
-    assert torch.equal(pa.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()], pb.view(-1, cfg.I)[:blk[-1] * 128][live.cuda()])
+    with pytest.raises(M.MMError) as ei:
+        run_forward(M, cfg, dev, M.options(cta_pairs=pairs))
+    assert ei.value.code == M.MM_MOE_ERR_UNSUPPORTED
+    out, _, _, (code, _) = run_forward(M, cfg, dev, M.options(cta_pairs=1))
+    assert code == 0
 
 
 def test_fused_stream_parity_and_masking(M):
