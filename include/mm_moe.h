@@ -185,9 +185,10 @@ int mm_moe_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, i
  *   - The first call on each device looks the array's device address up
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
- *   - The array holds min(#SMs, ceil(T*K/512)) x E counts at most 65536
- *     entries; larger requests return MM_MOE_ERR_WORKSPACE_TOO_SMALL before
- *     any work is enqueued.
+ *   - The array holds 65536 counts, one per (CTA, expert): the work is
+ *     spread over at most min(#SMs, ceil(T*K/512), 65536/E) CTAs (at least
+ *     64 for E <= 1024), so every shape mm_moe_dispatch accepts fits and the
+ *     routing is the same as mm_moe_dispatch's.
  *   - All calls share the array and each call rewrites the entries it reads,
  *     so calls that may overlap on the GPU (other streams, other host
  *     threads) race with one another: serialise them. */

@@ -2,8 +2,6 @@
 // the library any scratch memory.  The per-CTA expert counts that
 // mm_moe_dispatch keeps in caller scratch live here in a fixed file-scope
 // device array instead, so this entry point performs no allocation at all.
-#include <cstdio>
-#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -53,22 +51,15 @@ extern "C" int mm_moe_dispatch_noalloc(const int32_t* topk_idx, int T, int K, in
   if (src_capacity < pairs + live * (block_m - 1)) return MM_MOE_ERR_INVALID_ARG;
   const DevInfo& d = dev_info();
   if (!(d.cc_major == 10 && d.cc_minor == 3)) return MM_MOE_ERR_UNSUPPORTED;
-  // The work is split over as many CTAs as mm_moe_dispatch would use with a
-  // full-size scratch; their counts must fit the fixed array.
-  int64_t ctas = (pairs + 511) / 512;
-  if (ctas > d.sms) ctas = d.sms;
-  if (ctas < 1) ctas = 1;
-  if (ctas * E > kNoallocScratchInts) {
-    if (getenv("MM_MOE_DEBUG"))
-      fprintf(stderr, "mm_moe_dispatch_noalloc: %lld CTAs x %d experts exceed the %lld-entry static scratch\n",
-              static_cast<long long>(ctas), E, static_cast<long long>(kNoallocScratchInts));
-    return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
-  }
+  // The fixed array bounds the CTA count at kNoallocScratchInts / E (at least
+  // 64 for E <= 1024), as a small caller scratch does for mm_moe_dispatch; the
+  // slots do not depend on the CTA count, so every valid shape fits.
+  if (E > kNoallocScratchInts) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
   int32_t* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return MM_MOE_ERR_CUDA;
-  // The count kernel rewrites all ctas x E entries before the assign kernel
-  // reads them, so nothing in the array has to be cleared between calls.
+  // The count kernel rewrites all CTAs x E entries it uses before the assign
+  // kernel reads them, so nothing in the array has to be cleared between calls.
   const cudaError_t e = launch_dispatch(topk_idx, T, K, E, block_m, cnt, blk_off, slot, src, status, scratch,
-                                        ctas * E, static_cast<cudaStream_t>(stream));
+                                        kNoallocScratchInts, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
 }
