@@ -48,11 +48,11 @@
 // and a site code and returns.
 #include <cuda.h>
 
-#include "combine.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
 #include "sched.cuh"
+#include "stream.cuh"
 
 namespace mm {
 namespace {
@@ -87,12 +87,13 @@ constexpr int kSfColsPerStage = 12;    // 4 (tokens) + 8 (weights)
 // wait-site codes reported through the status word
 enum : int {
   kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104,
-  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108, kSiteCombine = 109, kSiteDeferred = 110,
+  kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108,   // 109, 110: early combine (stream.cuh)
   kSiteDrainCopies = 111, kSiteDrainMma = 112
 };
 
 struct Args {
   int T, H, I, E, K;
+  int BT, CPB;         // pool rows per block (128) and 128-row scale chunks per block (1)
   int KB1, KB2, NB1, NB2;
   int mode;            // 1, 2 or 3 (see above)
   int lag;             // mode 3: experts by which L2 trails L1
@@ -210,134 +211,6 @@ __device__ __forceinline__ void l1_block(uint32_t (&g)[32], uint32_t (&u)[32], i
   dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
   sfrow[c] = static_cast<uint8_t>(ee + 127);
-}
-
-// Gather warps of the fused stream: this CTA gathers pool blocks b =
-// blockIdx.x, + gridDim.x, ... in order; each warp copies every other row of a
-// block (codes and UE8M0 scales) and publishes its row count (release).
-__device__ __forceinline__ void gather_rows(const Args& args, const int* s_blk, const int* s_cnt, const Sched& sch,
-                                            volatile int* s_abort, int gw, int lane, int nblk) {
-  const int KBx = args.H / 128;
-  for (int b = blockIdx.x; b < nblk && !*s_abort; b += gridDim.x) {
-    const int e = sch.largest_leq(s_blk, args.E, b, 1);
-    const int rem = s_cnt[e] - (b - s_blk[e]) * kBT;
-    const int valid = rem < kBT ? rem : kBT;
-    int done = 0;
-    for (int r = gw; r < valid; r += kGatherWarps) {
-      const size_t row = static_cast<size_t>(b) * kBT + r;
-      const int64_t tok = __ldg(args.src + row) / args.K;
-      if (args.x_bf16) {
-        const __nv_bfloat16* brow = reinterpret_cast<const __nv_bfloat16*>(args.x) + tok * args.H;
-        uint8_t* chunk0 = args.pool_x_sf + static_cast<size_t>(b) * KBx * kSFChunk + (r & 31) * 16 + (r >> 5) * 4;
-        uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
-        quant_row_mx_bf16(brow, args.H, lane, [&](int j, const uint4 (&c)[2], uint8_t sfb, bool) {
-          drow[2 * j] = c[0];
-          drow[2 * j + 1] = c[1];
-          chunk0[(j >> 2) * kSFChunk + (j & 3)] = sfb;
-        });
-        ++done;
-        continue;
-      }
-      const uint4* srow = reinterpret_cast<const uint4*>(args.x + tok * args.H);
-      uint4* drow = reinterpret_cast<uint4*>(args.pool_x + row * args.H);
-      for (int i = lane; i < args.H / 16; i += 32) drow[i] = __ldg(srow + i);
-      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(args.x_sf + tok * (args.H / 32));
-      for (int kb = lane; kb < KBx; kb += 32)
-        *reinterpret_cast<uint32_t*>(args.pool_x_sf + (static_cast<size_t>(b) * KBx + kb) * kSFChunk +
-                                     (r & 31) * 16 + (r >> 5) * 4) = __ldg(ssf + kb);
-      ++done;
-    }
-    fence_proxy_async_global();
-    __syncwarp();
-    if (lane == 0 && done) red_release_gpu_add(args.ctr_gather + b, done);
-  }
-}
-
-// Early combine (DeepGEMM PR #440, "Also in the diff": math warps reduce the
-// tokens whose selected experts have all published).  An epilogue warp comes
-// here once its CTA has no tile group left, and by then every group of the
-// stream has been dealt, so each L2 tile a token waits for belongs to a CTA
-// that finishes it without any help from this warp: no wait below can close a
-// cycle.  Pass 1 takes tokens in order: a token whose valid slots' experts
-// have all finished L2 (per-expert counts of epilogue warps, read with
-// acquire) is combined at once by the warp, any other is appended to a
-// deferred list.  Pass 2 takes the deferred tokens and waits, bounded, for
-// their experts.  The arithmetic is the combine kernel's (combine.cuh).  Every
-// branch below is warp-uniform.
-template <typename PartT>
-__device__ __forceinline__ void early_combine(const Args& args, const int* s_blk, const Status& st,
-                                              volatile int* s_abort, int lane) {
-  const int T = args.T, K = args.K, E = args.E;
-  const PartT* part = reinterpret_cast<const PartT*>(args.partials);
-  int* take = args.cmb;             // pass 1: tokens taken
-  int* ndef = args.cmb + 1;         // deferred so far
-  int* classified = args.cmb + 2;   // pass-1 tokens combined or deferred
-  int* take2 = args.cmb + 3;        // pass 2: deferred entries taken
-  auto stop = [&]() { return __shfl_sync(0xffffffffu, *s_abort ? 1 : 0, 0) != 0; };
-  auto next = [&](int* ctr) {
-    int c = 0;
-    if (lane == 0) c = atomicAdd(ctr, 1);
-    return __shfl_sync(0xffffffffu, c, 0);
-  };
-  // lane k < K checks slot k; vmask gets the valid slots
-  auto ready = [&](int t, uint32_t& vmask) -> bool {
-    bool ok = true, v = false;
-    if (lane < K) {
-      const int e = __ldg(args.topk_idx + static_cast<int64_t>(t) * K + lane);
-      v = e >= 0 && e < E;
-      if (v) ok = ld_acquire_gpu(args.ctr_l2 + e) >= kEpiWarps * args.NB2 * (s_blk[e + 1] - s_blk[e]);
-    }
-    vmask = __ballot_sync(0xffffffffu, v);
-    const bool all = __all_sync(0xffffffffu, ok);
-    __syncwarp();   // the checking lanes' acquires before every lane's partial loads
-    return all;
-  };
-  while (!stop()) {
-    const int t = next(take);
-    if (t >= T) break;
-    uint32_t vm;
-    if (ready(t, vm)) combine_token_warp<PartT, 4>(part, t, T, args.H, K, vm, args.out, lane);
-    else if (lane == 0) st_release_gpu(args.deferred + atomicAdd(ndef, 1), t + 1);
-    __syncwarp();
-    if (lane == 0) red_release_gpu_add(classified, 1);
-  }
-  while (!stop()) {
-    const int c = next(take2);
-    if (c >= T) break;
-    int t = -1;   // stays -1 when entry c will never be written (every token classified, fewer deferred)
-    if (lane == 0) {
-      const uint64_t t0 = globaltimer();
-      while (true) {
-        const int v = ld_acquire_gpu(args.deferred + c);
-        if (v > 0) { t = v - 1; break; }
-        if (ld_acquire_gpu(classified) >= T && ld_acquire_gpu(ndef) <= c) break;
-        if (*s_abort) break;
-        if (globaltimer() - t0 > st.timeout_ns) {
-          report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, kSiteDeferred);
-          *s_abort = 1;
-          break;
-        }
-      }
-    }
-    t = __shfl_sync(0xffffffffu, t, 0);
-    if (t < 0) break;
-    uint32_t vm;
-    const uint64_t t0 = globaltimer();
-    bool ok = true;
-    while (!ready(t, vm)) {
-      int late = 0;
-      if (lane == 0) late = (*s_abort || globaltimer() - t0 > st.timeout_ns) ? 1 : 0;
-      if (__shfl_sync(0xffffffffu, late, 0)) { ok = false; break; }
-    }
-    if (!ok) {   // the first error recorded wins, so an abort raised elsewhere keeps its own
-      if (lane == 0) {
-        report_error(st, 4 /*MM_MOE_ERR_TIMEOUT*/, kSiteCombine);
-        *s_abort = 1;
-      }
-      break;
-    }
-    combine_token_warp<PartT, 4>(part, t, T, args.H, K, vm, args.out, lane);
-  }
 }
 
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
@@ -543,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     }
     __syncwarp();
     } else if (warp < kGatherWarp0 + kGatherWarps && args.mode == 3) {
-      gather_rows(args, s_blk, s_cnt, sch, s_abort, warp - kGatherWarp0, lane, nblk);
+      gather_rows(args, s_blk, s_cnt, sch, s_abort, warp - kGatherWarp0, kGatherWarps, lane, nblk);
     } else if (warp == kSchedWarp && lane == 0) {
       // ------------------------------------------------------------------ tile-group scheduler
       // Every dependency of a group (the gather and L1 tiles of the blocks an
@@ -627,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       if (kProf) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
     }
     if (args.early_combine) {
-      if (args.pbf16) early_combine<__nv_bfloat16>(args, s_blk, st, s_abort, lane);
-      else early_combine<float>(args, s_blk, st, s_abort, lane);
+      if (args.pbf16) early_combine<__nv_bfloat16>(args, kEpiWarps, s_blk, st, s_abort, lane);
+      else early_combine<float>(args, kEpiWarps, s_blk, st, s_abort, lane);
     }
     if (kProf && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
@@ -663,6 +536,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   Maps maps;
   Args a{};
   a.T = L.T; a.H = L.H; a.I = L.I; a.E = L.E; a.K = L.K;
+  a.BT = kBT; a.CPB = 1;
   a.KB1 = L.H / 128; a.KB2 = L.I / 128; a.NB1 = L.I / 128; a.NB2 = (L.H + kBN - 1) / kBN;
   a.mode = mode;
   a.lag = lag < 0 ? 0 : (lag > L.E ? L.E : lag);   // a lag above E orders the stream as E does

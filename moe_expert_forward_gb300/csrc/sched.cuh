@@ -46,6 +46,7 @@ struct Sched {
   const int* blk;   // [E+1] pool-block offsets per expert
   const int* cnt;   // [E]
   int E, NB1, NB2, mode, lag;
+  int BT = kBT;     // pool rows per block
 
   __device__ __forceinline__ int largest_leq(const int* a, int n, int v, int scale) const {
     int lo = 0, hi = n - 1;                  // largest i < n with a[i] * scale <= v
@@ -85,8 +86,8 @@ struct Sched {
   }
   __device__ __forceinline__ void block(Cursor& c) const {
     c.t.b = blk[c.t.e] + c.bl;
-    const int rem = cnt[c.t.e] - c.bl * kBT;
-    c.t.valid = rem < kBT ? rem : kBT;
+    const int rem = cnt[c.t.e] - c.bl * BT;
+    c.t.valid = rem < BT ? rem : BT;
     c.t.last = c.bl + 1 == c.nb;
     c.t.rev = (c.bl & 1) != 0;
   }

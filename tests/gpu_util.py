@@ -79,17 +79,18 @@ REPORT = []
 
 # FP8 scale agreement: s = fp32(amax / 448) moves with amax, and the GPU's amax
 # comes from fp32 tensor-core partials promoted in fp32 over H/128 k-blocks,
-# the oracle's from fp64 sums rounded once to fp32.  Two scales count as the
-# same scale when they are within 2^-18 relative (32 to 64 fp32 ulps); every
-# code of a block outside that counts as a mismatch.
-F8_SCALE_RTOL = 2.0 ** -18
+# the oracle's from fp64 sums rounded once to fp32.  Measured on GB300 over the
+# full-size FP8 rows: median 1, 99.9th percentile 8, max 12 fp32 ulps apart.
+# Two scales count as the same scale when they are at most 16 ulps apart;
+# every code of a block beyond that counts as a mismatch.
+F8_SCALE_ULPS = 16
 
 
 def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict, label: str = "") -> float:
     """Fraction of intermediate e4m3 codes equal (by value) to the oracle's, with
     every code of a block whose scale differs counted as a mismatch.  MX scales
     are UE8M0 bytes and must be equal; FP8 scales are raw fp32 amax/448 and must
-    agree to F8_SCALE_RTOL (the fp32 accumulation's spread, above).  The match
+    be within F8_SCALE_ULPS (the fp32 accumulation's spread, above).  The match
     fraction and, for FP8, the scale deviations in fp32 ulps are recorded in
     REPORT."""
     rows = int(M.mm_moe_workspace_region(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, 4)[1] // 4)
@@ -113,8 +114,9 @@ def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict, label: st
             g = sf[row].astype(np.float32)
             r = np.asarray(osf, dtype=np.float32)
             # distance in fp32 ulps of the oracle's scale (positive normal floats: integer bit distance)
-            ulps.append(np.abs(g.view(np.int32).astype(np.int64) - r.view(np.int32).astype(np.int64)))
-            same_sf = np.repeat(np.abs(g.astype(np.float64) / r.astype(np.float64) - 1.0) <= F8_SCALE_RTOL, bs)
+            d = np.abs(g.view(np.int32).astype(np.int64) - r.view(np.int32).astype(np.int64))
+            ulps.append(d)
+            same_sf = np.repeat(d <= F8_SCALE_ULPS, bs)
         same = same_sf & (O.e4m3_decode(codes[row]) == O.e4m3_decode(oc))
         total += same.size
         match += int(same.sum())
@@ -123,8 +125,7 @@ def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict, label: st
     if ulps:
         u = np.concatenate(ulps)
         line += (f"; fp32 scale distance in ulps: median {np.median(u):.0f}, 99.9 % {np.percentile(u, 99.9):.0f}, "
-                 f"max {u.max()}, blocks within {F8_SCALE_RTOL:.2e} relative "
-                 f"{100 * np.mean(u <= F8_SCALE_RTOL * 2 ** 23):.3f} %")
+                 f"max {u.max()}, blocks within {F8_SCALE_ULPS} ulps {100 * np.mean(u <= F8_SCALE_ULPS):.3f} %")
     REPORT.append(line)
     return frac
 

@@ -52,7 +52,10 @@ def test_fullsize_sampled_rows(M, name):
         assert np.array_equal(src[:len(ref_route["src"])], ref_route["src"])
         got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy()
         check_output(got, ref, f"{name} {kw}")
-        assert intermediate_match(M, cfg, ws, opt, slot, inter, label=f"{name} {kw}") >= 0.999, kw
+        # >= 99.9 % is the criterion; the full-size FP8 rows, whose codes are IEEE
+        # quotients on both sides, are held to 99.99 %
+        frac = intermediate_match(M, cfg, ws, opt, slot, inter, label=f"{name} {kw}")
+        assert frac >= (0.9999 if cfg.variant == "f8" else 0.999), (kw, frac)
         assert torch.isfinite(out.float()).all()
         del out, ws, prepared
         gc.collect()
