@@ -200,6 +200,10 @@ def run_ours(args, ws_n, rank, local):
     opt.partials_bf16 = 1 if args.partials == "bf16" else 0
     if args.early_combine is not None:
         opt.early_combine = args.early_combine
+    if args.swap_ab is not None:
+        opt.swap_ab = args.swap_ab
+    if args.block_m:
+        opt.block_m = args.block_m
     if args.x == "bf16":
         # bf16 activations: the gather quantises each row (x_sf is not read)
         inp["x"], inp["x_sf"] = W.make_x_bf16(cfg, dev), None
@@ -241,8 +245,7 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.synchronize()
     for i in range(K):
         flush.zero_()
-        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16, x_bf16=opt.x_bf16,
-                      early_combine=opt.early_combine)
+        o = M.mm_moe_options.from_buffer_copy(opt)
         o.timing_events = ctypes.cast(arrays[i], ctypes.c_void_p)
         fwd(o)
     torch.cuda.synchronize()
@@ -262,8 +265,7 @@ def run_ours(args, ws_n, rank, local):
     sarr = [(ctypes.c_void_p * M.MM_MOE_NUM_TIMING_EVENTS)(*[e.cuda_event for e in row]) for row in sev]
     for i in range(n_st):
         flush.zero_()
-        o = M.options(opt.variant, fused=opt.fused, partials_bf16=opt.partials_bf16, x_bf16=opt.x_bf16,
-                      early_combine=opt.early_combine)
+        o = M.mm_moe_options.from_buffer_copy(opt)
         o.timing_events = ctypes.cast(sarr[i], ctypes.c_void_p)
         fwd(o)
     torch.cuda.synchronize()
@@ -370,6 +372,7 @@ def run_ours(args, ws_n, rank, local):
                    "l2_policy": "L2 flushed (512 MiB write) before every timed step; weights 3+ GB >> L2",
                    "parallelism": f"replicas x{ws_n} (no data-path collective)",
                    "fused_stream": fused, "early_combine": early, "partials": args.partials, "x": args.x,
+                   "swap_ab": int(opt.swap_ab), "block_m": int(opt.block_m),
                    "e2e_policy": "copies on streams of their own, two buffer sets (step i+1 in and step i-1 out "
                                  "overlap step i); no L2 flush: every step reads >= 2.5 GB of weights"},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
@@ -513,6 +516,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=2,
                     help="--impl reference: tokens of the workload the oracle processes per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--swap-ab", type=int, choices=[0, 1], default=None,
+                    help="MX: 1 = weights as the MMA's M side, each pool block's tokens as N; default: the library's")
+    ap.add_argument("--block-m", type=int, default=0, help="tokens per pool block (0: the library's choice)")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,
                     help="1: gather + L1 + L2 as one lag-ordered persistent launch; default: the library's")
     args = ap.parse_args()

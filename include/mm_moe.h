@@ -121,7 +121,18 @@ typedef struct mm_moe_options {
                                    early combine) and no combine kernel runs; 0 (default) = a combine
                                    kernel after the GEMM, which measures as fast or faster on one
                                    GB300.  Bit-identical either way. */
-  int reserved[1];
+  int swap_ab;                  /* MX variant: which operand is the tensor-core MMA's M side.  0 (default):
+                                   the tokens, in pool blocks of 128 (every MMA computes 128 token rows
+                                   x 256 weight rows); 1: the weights (128 rows per MMA) with each pool
+                                   block's tokens as N, rounded up to 16, so a block's MMA work follows
+                                   its token count and an expert whose tokens fit one block streams
+                                   its weights once (the pages' swap-AB form).  Results agree with the
+                                   oracle either way; the two forms sum the same products in a
+                                   different tensor-core order, so their bits may differ. */
+  int block_m;                  /* tokens per pool block: 0 (default) = the form's own choice (128 for
+                                   swap_ab 0; for swap_ab 1, 160 when the expected tokens per expert
+                                   T*K/E exceed 64, else 80); otherwise 128 (swap_ab 0) or 80 / 160
+                                   (swap_ab 1), anything else MM_MOE_ERR_UNSUPPORTED */
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

@@ -40,7 +40,7 @@ class mm_moe_options(ctypes.Structure):
                 ("num_sms", ctypes.c_int), ("debug_flags", ctypes.c_int), ("cta_pairs", ctypes.c_int),
                 ("partials_bf16", ctypes.c_int), ("activation_clamp", ctypes.c_float),
                 ("precise_swiglu", ctypes.c_int), ("x_bf16", ctypes.c_int), ("early_combine", ctypes.c_int),
-                ("reserved", ctypes.c_int * 1),
+                ("swap_ab", ctypes.c_int), ("block_m", ctypes.c_int),
                 ("timing_events", ctypes.c_void_p)]
 
 

@@ -13,13 +13,14 @@ namespace mm {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags, int partials_bf16) {
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags, int partials_bf16, int BT) {
   Layout L{};
-  L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = kBT;
+  L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = BT;
+  L.CPB = (BT + 127) / 128;
   const int64_t pairs = static_cast<int64_t>(T) * K;
   const int64_t live_experts = pairs < E ? pairs : E;
-  L.P = static_cast<int64_t>(align_up(static_cast<size_t>(pairs + live_experts * (kBT - 1)), kBT));
-  L.nblk_cap = L.P / kBT;
+  L.P = static_cast<int64_t>(align_up(static_cast<size_t>(pairs + live_experts * (BT - 1)), BT));
+  L.nblk_cap = L.P / BT;
   L.KB1 = H / 128;
   L.KB2 = I / 128;
   size_t o = 0;
@@ -31,12 +32,14 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
   L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
   L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
+  // MX scales: [block][kb][CPB][512-byte chunk]; F8 scales: fp32 [P][kdim / 128]
+  const size_t chunks = static_cast<size_t>(L.nblk_cap) * L.CPB * kSFChunk;
   L.pool_x_sf = o;
-  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? static_cast<size_t>(L.P) * H / 32
+  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? chunks * (H / 128)
                                                  : static_cast<size_t>(L.P) * (H / 128) * sizeof(float)), 1024);
   L.pool2 = o; o = align_up(o + static_cast<size_t>(L.P) * I, 1024);
   L.pool2_sf = o;
-  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? static_cast<size_t>(L.P) * I / 32
+  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? chunks * (I / 128)
                                                  : static_cast<size_t>(L.P) * (I / 128) * sizeof(float)), 1024);
   L.part_elem = partials_bf16 ? 2 : 4;
   L.part = o; o = align_up(o + static_cast<size_t>(pairs) * H * L.part_elem, 1024);
@@ -189,6 +192,39 @@ int check_shape(int T, int H, int I, int E, int K) {
   return MM_MOE_OK;
 }
 
+// Which MX kernel runs and its pool block size (tokens per block).
+struct Plan {
+  bool swap;   // weights as the MMA's M operand, each block's tokens as N
+  int BT;
+};
+
+// expected tokens per expert above which the swapped kernel uses 160-token blocks
+constexpr int kSwapLargeBlockTokens = 64;
+
+int make_plan(const mm_moe_options& o, int T, int K, int E, Plan* p) {
+  if (o.variant == MM_MOE_VARIANT_F8) {
+    if (o.swap_ab == 1 || (o.block_m != 0 && o.block_m != kBT)) return MM_MOE_ERR_UNSUPPORTED;
+    *p = {false, kBT};
+    return MM_MOE_OK;
+  }
+  if (o.swap_ab < -1 || o.swap_ab > 1) return MM_MOE_ERR_INVALID_ARG;
+  const bool swap = o.swap_ab == 1;
+  if (!swap) {
+    if (o.block_m != 0 && o.block_m != kBT) return MM_MOE_ERR_UNSUPPORTED;
+    *p = {false, kBT};
+    return MM_MOE_OK;
+  }
+  const int64_t per_expert = static_cast<int64_t>(T) * K / E;
+  const int bt = o.block_m ? o.block_m : (per_expert > kSwapLargeBlockTokens ? 160 : 80);
+  if (!mx_sw_block_supported(bt)) return MM_MOE_ERR_UNSUPPORTED;
+  *p = {true, bt};
+  return MM_MOE_OK;
+}
+
+Layout layout_for(const mm_moe_options& o, int T, int H, int I, int E, int K, const Plan& p) {
+  return make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16, p.BT);
+}
+
 int device_supported() {
   const DevInfo& d = dev_info();
   return (d.cc_major == 10 && d.cc_minor == 3) ? MM_MOE_OK : MM_MOE_ERR_UNSUPPORTED;
@@ -208,6 +244,8 @@ void mm_moe_default_options(mm_moe_options* opt) {
   opt->wait_timeout_ms = 2000;
   opt->num_sms = 0;
   opt->early_combine = 0;
+  opt->swap_ab = 0;
+  opt->block_m = 0;
 }
 
 int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E, int K, size_t* bytes) {
@@ -215,7 +253,9 @@ int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E,
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
-  *bytes = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16).total;
+  Plan p;
+  if (int r = make_plan(o, T, K, E, &p)) return r;
+  *bytes = layout_for(o, T, H, I, E, K, p).total;
   return MM_MOE_OK;
 }
 
@@ -301,9 +341,13 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (o.cta_pairs != 0 && o.cta_pairs != 1) return MM_MOE_ERR_UNSUPPORTED;
   // the F8 epilogue stages each task's weight scales in shared memory for up to kF8MaxKB k-blocks
   if (o.variant == MM_MOE_VARIANT_F8 && (H / 128 > kF8MaxKB || I / 128 > kF8MaxKB)) return MM_MOE_ERR_UNSUPPORTED;
+  Plan plan;
+  if (int r = make_plan(o, T, K, E, &plan)) return r;
+  // the swapped kernel keeps no per-role timings
+  if (plan.swap && (o.debug_flags & 2)) return MM_MOE_ERR_UNSUPPORTED;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
   const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
+  const Layout L = layout_for(o, T, H, I, E, K, plan);
   if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
   // early combine in the fused stream
   const bool early = fused && o.early_combine;
@@ -336,16 +380,17 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
                  clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm};
+    auto gemm = plan.swap ? launch_gemm_mx_sw : launch_gemm_mx;
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
-      if (e == cudaSuccess) e = launch_gemm_mx(g, 3, lag, (o.debug_flags & 4) ? 1 : 0, s);
+      if (e == cudaSuccess) e = gemm(g, 3, lag, (o.debug_flags & 4) ? 1 : 0, s);
       if (e == cudaSuccess) e = mark(3);
     } else {
-      if (e == cudaSuccess) e = launch_gemm_mx(g, 1, 0, 0, s);
+      if (e == cudaSuccess) e = gemm(g, 1, 0, 0, s);
       if (e == cudaSuccess) e = mark(3);
       if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
-      if (e == cudaSuccess) e = launch_gemm_mx(g, 2, 0, 0, s);
+      if (e == cudaSuccess) e = gemm(g, 2, 0, 0, s);
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,
@@ -374,7 +419,9 @@ int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T,
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!workspace) return MM_MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
+  Plan plan;
+  if (int r = make_plan(o, T, K, E, &plan)) return r;
+  const Layout L = layout_for(o, T, H, I, E, K, plan);
   const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -393,7 +440,9 @@ int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, i
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!workspace || !codes || !sf || rows < 0) return MM_MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
+  Plan plan;
+  if (int r = make_plan(o, T, K, E, &plan)) return r;
+  const Layout L = layout_for(o, T, H, I, E, K, plan);
   if (rows > L.P) return MM_MOE_ERR_INVALID_ARG;
   if (rows == 0) return MM_MOE_OK;
   const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
@@ -406,7 +455,9 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
   const mm_moe_options o = resolve(opt);
   if (int r = check_shape(T, H, I, E, K)) return r;
   if (!ptr || !bytes) return MM_MOE_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16);
+  Plan plan;
+  if (int r = make_plan(o, T, K, E, &plan)) return r;
+  const Layout L = layout_for(o, T, H, I, E, K, plan);
   const size_t offs[13] = {L.status, L.cnt, L.blk_off, L.slot, L.src, L.pool_x, L.pool_x_sf, L.pool2, L.pool2_sf,
                            L.part, L.dbg, L.prof, L.total};
   if (region < 0 || region > 11) return MM_MOE_ERR_INVALID_ARG;

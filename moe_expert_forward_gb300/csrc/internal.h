@@ -9,7 +9,7 @@
 
 namespace mm {
 
-constexpr int kBT = 128;        // tokens per pool block (MMA N upper bound; one scale chunk)
+constexpr int kBT = 128;        // tokens per pool block of the token-M kernels (one scale chunk)
 constexpr int kBK = 128;        // contraction elements per pipeline stage
 constexpr int kSFChunk = 512;   // bytes of one 128-row x 128-K scale chunk (MX)
 constexpr int kMaxE = 1024;
@@ -20,6 +20,7 @@ constexpr int kCombineCounters = 4;      // early combine: tokens taken, deferre
 // Byte offsets of every buffer inside the caller's workspace.
 struct Layout {
   int T, H, I, E, K, variant, BT;
+  int CPB;                   // 128-row scale chunks per pool block: ceil(BT / 128)
   int64_t P;                 // pool row capacity (multiple of BT)
   int64_t nblk_cap;          // P / BT
   int KB1, KB2;              // H/128, I/128
@@ -27,7 +28,16 @@ struct Layout {
   size_t status, cnt, blk_off, dscr, ctr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
 };
 
-Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0, int partials_bf16 = 0);
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0, int partials_bf16 = 0,
+                   int BT = kBT);
+
+// Byte offset, in a pool scale region laid out [block][kb][CPB chunks][512], of
+// the 4-byte word of row r of block b (r < BT) and 128-wide contraction block
+// kb: chunk r / 128 of the block, then the tcgen05.cp 32x128b order inside the
+// chunk (16-byte line r % 32, word (r % 128) / 32, byte = 32-wide sub-block).
+__host__ __device__ __forceinline__ size_t pool_sf_word(int64_t b, int kb, int KB, int CPB, int r) {
+  return ((static_cast<size_t>(b) * KB + kb) * CPB + (r >> 7)) * kSFChunk + (r & 31) * 16 + ((r & 127) >> 5) * 4;
+}
 
 // Ints of the counter region, zeroed before every forward: [2][nblk_cap]
 // per-block arrival counters, kSchedCounters, kCombineCounters, [E] L2
@@ -110,6 +120,10 @@ struct GemmLaunch {
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
 int mx_lag_auto(int E);
+// The same modes with the weights as the MMA's M operand and each pool block's
+// tokens as N (gemm_mx_sw.cu); g.L->BT must be a supported block size.
+cudaError_t launch_gemm_mx_sw(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
+bool mx_sw_block_supported(int bt);
 
 struct GemmLaunchF8 {
   const Layout* L;

@@ -230,7 +230,7 @@ __device__ __forceinline__ void token_rows(const int32_t* __restrict__ slot, int
 
 // x holds e4m3 codes [T, H] and their scales (MX: UE8M0 bytes [T, H/32]; F8: fp32 [T, H/128]).
 __global__ void __launch_bounds__(256)
-    gather_kernel(const int32_t* __restrict__ slot, int T, int K, int H, int BT, int variant,
+    gather_kernel(const int32_t* __restrict__ slot, int T, int K, int H, int BT, int CPB, int variant,
                   const uint8_t* __restrict__ x, const void* __restrict__ x_sf, uint8_t* __restrict__ pool_x,
                   uint8_t* __restrict__ pool_x_sf) {
   const int lane = threadIdx.x & 31;
@@ -257,9 +257,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int k = 0; k < kMaxK; ++k) {
           const int r = k < K ? rows[k] : -1;
-          if (r >= 0)
-            *reinterpret_cast<uint32_t*>(pool_x_sf + (static_cast<int64_t>(r / BT) * KB + kb) * kSFChunk +
-                                         sf_chunk_offset(r % BT, 0)) = w;
+          if (r >= 0) *reinterpret_cast<uint32_t*>(pool_x_sf + pool_sf_word(r / BT, kb, KB, CPB, r % BT)) = w;
         }
       } else {
         const float sc = __ldg(static_cast<const float*>(x_sf) + t * KB + kb);
@@ -277,7 +275,7 @@ __global__ void __launch_bounds__(256)
 // (quant.cuh) and every chunk written to each of the token's pool rows, so the
 // division-heavy F8 rule runs once per token rather than once per slot.
 __global__ void __launch_bounds__(256)
-    gather_quant_kernel(const int32_t* __restrict__ slot, int T, int K, int H, int BT, int variant,
+    gather_quant_kernel(const int32_t* __restrict__ slot, int T, int K, int H, int BT, int CPB, int variant,
                         const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ pool_x,
                         uint8_t* __restrict__ pool_x_sf) {
   const int lane = threadIdx.x & 31;
@@ -296,8 +294,7 @@ __global__ void __launch_bounds__(256)
           uint4* d = reinterpret_cast<uint4*>(pool_x + static_cast<int64_t>(r) * H) + 2 * j;
           d[0] = c[0];
           d[1] = c[1];
-          pool_x_sf[(static_cast<int64_t>(r / BT) * (H / 128) + (j >> 2)) * kSFChunk + sf_chunk_offset(r % BT, j & 3)] =
-              sfb;
+          pool_x_sf[pool_sf_word(r / BT, j >> 2, H / 128, CPB, r % BT) + (j & 3)] = sfb;
         }
       });
     } else {
@@ -320,10 +317,11 @@ cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, co
                           cudaStream_t s) {
   const int grid = dev_info().sms * 4;
   if (x_bf16)
-    gather_quant_kernel<<<grid, 256, 0, s>>>(W.slot, L.T, L.K, L.H, L.BT, L.variant,
+    gather_quant_kernel<<<grid, 256, 0, s>>>(W.slot, L.T, L.K, L.H, L.BT, L.CPB, L.variant,
                                              reinterpret_cast<const __nv_bfloat16*>(x), W.pool_x, W.pool_x_sf);
   else
-    gather_kernel<<<grid, 256, 0, s>>>(W.slot, L.T, L.K, L.H, L.BT, L.variant, x, x_sf, W.pool_x, W.pool_x_sf);
+    gather_kernel<<<grid, 256, 0, s>>>(W.slot, L.T, L.K, L.H, L.BT, L.CPB, L.variant, x, x_sf, W.pool_x,
+                                       W.pool_x_sf);
   return cudaGetLastError();
 }
 
@@ -424,7 +422,7 @@ cudaError_t launch_prepare_sf_mx(const uint8_t* w1_sf, const uint8_t* w2_sf, int
 }
 
 // ----------------------------------------------------------------------------- intermediate read-back
-__global__ void read_sf_mx_kernel(const uint8_t* __restrict__ pool2_sf, int64_t rows, int I, int BT,
+__global__ void read_sf_mx_kernel(const uint8_t* __restrict__ pool2_sf, int64_t rows, int I, int BT, int CPB,
                                   uint8_t* __restrict__ sf) {
   const int KB32 = I / 32;
   const int KB = I / 128;
@@ -434,7 +432,7 @@ __global__ void read_sf_mx_kernel(const uint8_t* __restrict__ pool2_sf, int64_t 
     const int j = static_cast<int>(g % KB32);
     const int64_t blk = r / BT;
     const int rr = static_cast<int>(r % BT);
-    sf[g] = pool2_sf[(blk * KB + j / 4) * kSFChunk + sf_chunk_offset(rr, j & 3)];
+    sf[g] = pool2_sf[pool_sf_word(blk, j / 4, KB, CPB, rr) + (j & 3)];
   }
 }
 
@@ -443,7 +441,8 @@ cudaError_t launch_read_intermediate(const Layout& L, const WsPtrs& W, int64_t r
   cudaError_t e = cudaMemcpyAsync(codes, W.pool2, static_cast<size_t>(rows) * L.I, cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return e;
   if (L.variant == MM_MOE_VARIANT_MX) {
-    read_sf_mx_kernel<<<dev_info().sms * 4, 256, 0, s>>>(W.pool2_sf, rows, L.I, L.BT, static_cast<uint8_t*>(sf));
+    read_sf_mx_kernel<<<dev_info().sms * 4, 256, 0, s>>>(W.pool2_sf, rows, L.I, L.BT, L.CPB,
+                                                         static_cast<uint8_t*>(sf));
     return cudaGetLastError();
   }
   return cudaMemcpyAsync(sf, W.pool2_sf, static_cast<size_t>(rows) * (L.I / 128) * sizeof(float),

@@ -17,14 +17,6 @@ namespace mm {
 constexpr int kSiteCombineWait = 109;    // a token's experts have not all finished L2
 constexpr int kSiteDeferredWait = 110;   // a deferred entry was never written
 
-// Byte offset, inside a pool scale region laid out [block][kb][CPB chunks][512],
-// of the 4-byte word of row r (within block b) and contraction block kb: chunk
-// r / 128 of the block, then the tcgen05.cp 32x128b order inside the chunk
-// (16-byte line r % 32, word (r % 128) / 32).
-__device__ __forceinline__ size_t pool_sf_word(int b, int kb, int KB, int CPB, int r) {
-  return ((static_cast<size_t>(b) * KB + kb) * CPB + (r >> 7)) * kSFChunk + (r & 31) * 16 + ((r & 127) >> 5) * 4;
-}
-
 // Gather warps of the fused stream: this CTA gathers pool blocks b =
 // blockIdx.x, + gridDim.x, ... in order; warp gw of nw copies rows gw, gw + nw,
 // ... of a block (codes and UE8M0 scales, or bf16 rows quantised on the way)
