@@ -126,13 +126,16 @@ typedef struct mm_moe_options {
                                    x 256 weight rows); 1: the weights (128 rows per MMA) with each pool
                                    block's tokens as N, rounded up to 16, so a block's MMA work follows
                                    its token count and an expert whose tokens fit one block streams
-                                   its weights once (the pages' swap-AB form).  Results agree with the
-                                   oracle either way; the two forms sum the same products in a
-                                   different tensor-core order, so their bits may differ. */
+                                   its weights once (the pages' swap-AB form); 2: the same on 2-CTA
+                                   clusters, 256 weight rows per MMA (tcgen05 cta_group::2, half of
+                                   them and half of the block's tokens in each CTA of the pair).
+                                   Results agree with the oracle either way; the forms sum the same
+                                   products in a different tensor-core order, so their bits may
+                                   differ. */
   int block_m;                  /* tokens per pool block: 0 (default) = the form's own choice (128 for
                                    swap_ab 0; for swap_ab 1, 160 when the expected tokens per expert
                                    T*K/E exceed 64, else 80); otherwise 128 (swap_ab 0) or 80 / 160
-                                   (swap_ab 1), anything else MM_MOE_ERR_UNSUPPORTED */
+                                   (swap_ab 1 or 2), anything else MM_MOE_ERR_UNSUPPORTED */
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

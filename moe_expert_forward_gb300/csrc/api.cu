@@ -3,6 +3,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -114,6 +115,35 @@ cudaError_t configure_kernel(const void* fn, int want_regs, int smem_bytes) {
   return cudaSuccess;
 }
 
+cudaError_t max_pair_clusters(const void* fn, int threads, int smem_bytes, int* clusters) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = cache.find({fn, dev});
+  if (it != cache.end()) {
+    *clusters = it->second;
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t q = {};
+  q.gridDim = dim3(2);
+  q.blockDim = dim3(threads);
+  q.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute ca;
+  ca.id = cudaLaunchAttributeClusterDimension;
+  ca.val.clusterDim.x = 2; ca.val.clusterDim.y = 1; ca.val.clusterDim.z = 1;
+  q.attrs = &ca;
+  q.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, fn, &q);
+  if (e != cudaSuccess) return e;
+  cache[{fn, dev}] = n;
+  *clusters = n;
+  return cudaSuccess;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -195,6 +225,7 @@ int check_shape(int T, int H, int I, int E, int K) {
 // Which MX kernel runs and its pool block size (tokens per block).
 struct Plan {
   bool swap;   // weights as the MMA's M operand, each block's tokens as N
+  bool pair;   // ... on 2-CTA clusters (cta_group::2)
   int BT;
 };
 
@@ -203,21 +234,22 @@ constexpr int kSwapLargeBlockTokens = 64;
 
 int make_plan(const mm_moe_options& o, int T, int K, int E, Plan* p) {
   if (o.variant == MM_MOE_VARIANT_F8) {
-    if (o.swap_ab == 1 || (o.block_m != 0 && o.block_m != kBT)) return MM_MOE_ERR_UNSUPPORTED;
-    *p = {false, kBT};
+    if (o.swap_ab > 0 || (o.block_m != 0 && o.block_m != kBT)) return MM_MOE_ERR_UNSUPPORTED;
+    *p = {false, false, kBT};
     return MM_MOE_OK;
   }
-  if (o.swap_ab < -1 || o.swap_ab > 1) return MM_MOE_ERR_INVALID_ARG;
-  const bool swap = o.swap_ab == 1;
+  if (o.swap_ab < -1 || o.swap_ab > 2) return MM_MOE_ERR_INVALID_ARG;
+  const bool swap = o.swap_ab >= 1;
+  const bool pair = o.swap_ab == 2;
   if (!swap) {
     if (o.block_m != 0 && o.block_m != kBT) return MM_MOE_ERR_UNSUPPORTED;
-    *p = {false, kBT};
+    *p = {false, false, kBT};
     return MM_MOE_OK;
   }
   const int64_t per_expert = static_cast<int64_t>(T) * K / E;
   const int bt = o.block_m ? o.block_m : (per_expert > kSwapLargeBlockTokens ? 160 : 80);
-  if (!mx_sw_block_supported(bt)) return MM_MOE_ERR_UNSUPPORTED;
-  *p = {true, bt};
+  if (!(pair ? mx_pair_block_supported(bt) : mx_sw_block_supported(bt))) return MM_MOE_ERR_UNSUPPORTED;
+  *p = {true, pair, bt};
   return MM_MOE_OK;
 }
 
@@ -343,8 +375,6 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (o.variant == MM_MOE_VARIANT_F8 && (H / 128 > kF8MaxKB || I / 128 > kF8MaxKB)) return MM_MOE_ERR_UNSUPPORTED;
   Plan plan;
   if (int r = make_plan(o, T, K, E, &plan)) return r;
-  // the swapped kernel keeps no per-role timings
-  if (plan.swap && (o.debug_flags & 2)) return MM_MOE_ERR_UNSUPPORTED;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
   const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
   const Layout L = layout_for(o, T, H, I, E, K, plan);
@@ -379,8 +409,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
                  static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm};
-    auto gemm = plan.swap ? launch_gemm_mx_sw : launch_gemm_mx;
+                 clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm, (o.debug_flags & 8) != 0};
+    auto gemm = plan.pair ? launch_gemm_mx_pair : (plan.swap ? launch_gemm_mx_sw : launch_gemm_mx);
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
       const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);

@@ -96,6 +96,7 @@ struct Args {
   int BT, CPB;         // pool rows per block (128) and 128-row scale chunks per block (1)
   int KB1, KB2, NB1, NB2;
   int mode;            // 1, 2 or 3 (see above)
+  int per_block;       // deal each (weight tile, pool block) as its own group
   int lag;             // mode 3: experts by which L2 trails L1
   int l1_extra;        // mode 3: extra L1 completions an L2 tile waits for (0; 1 = a wait that cannot end)
   const int* cnt;
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   const uint32_t tmem = *s_tmem;
 
   const int nblk = s_blk[E];
-  const Sched sch{s_blk, s_cnt, E, args.NB1, args.NB2, args.mode, lag};
+  Sched sch{s_blk, s_cnt, E, args.NB1, args.NB2, args.mode, lag};
+  sch.per_block = args.per_block != 0;
 
   const int wg = warp >> 2;
   // setmaxnreg sits inside each warpgroup's branch: after a join ptxas would
@@ -500,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       if (kProf) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
     }
     if (args.early_combine) {
-      if (args.pbf16) early_combine<__nv_bfloat16>(args, kEpiWarps, s_blk, st, s_abort, lane);
-      else early_combine<float>(args, kEpiWarps, s_blk, st, s_abort, lane);
+      if (args.pbf16) early_combine<__nv_bfloat16>(args, kEpiWarps, args.NB2, s_blk, st, s_abort, lane);
+      else early_combine<float>(args, kEpiWarps, args.NB2, s_blk, st, s_abort, lane);
     }
     if (kProf && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
@@ -539,6 +541,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.BT = kBT; a.CPB = 1;
   a.KB1 = L.H / 128; a.KB2 = L.I / 128; a.NB1 = L.I / 128; a.NB2 = (L.H + kBN - 1) / kBN;
   a.mode = mode;
+  a.per_block = g.per_block ? 1 : 0;
   a.lag = lag < 0 ? 0 : (lag > L.E ? L.E : lag);   // a lag above E orders the stream as E does
   a.l1_extra = l1_extra;
   a.cnt = W.cnt; a.blk_off = W.blk_off; a.src = W.src; a.topk_w = g.topk_w;

@@ -126,6 +126,7 @@ struct Args {
   int* deferred;
   int* status;
   uint64_t timeout_ns;
+  unsigned long long* prof;  // per-CTA role timings (kProf instantiation) or null
 };
 
 struct Maps {
@@ -185,7 +186,12 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 __device__ __forceinline__ void regs_dec_mma() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kMmaRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
 
-template <int BT>
+// kProf: per-CTA role timings into prof[blockIdx.x * 8 + i]: 0 producers' ns
+// waiting for a free stage (summed), 1 / 2 the MMA issuer's SM cycles waiting
+// for a stage's data / for a free accumulator, 3 its span in ns, 4 its tasks, 5 /
+// 6 epilogue warp 4's ns waiting for an accumulator / working, 7 the issuer's span
+// in SM cycles.  A separate instantiation: the timing branches cost issue slots.
+template <int BT, bool kProf>
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_constant__ Maps maps, const Args args) {
   using C = Cfg<BT>;
   constexpr int S = C::kStages;
@@ -261,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
       int step = 0;
       bool armed = false;
       uint32_t armed_parity = 0;
+      uint64_t w_empty = 0;
       for (Cursor c; !*s_abort && sch.next(c, q, st, s_abort, false, lane, kSiteQueueFull);) {
         const Task& t = c.t;
         const bool l1 = t.type == 1;
@@ -283,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
         const uint8_t* sft = (l1 ? args.pool_x_sf : args.pool2_sf) + static_cast<size_t>(t.b) * KB * C::kCPB * kSFChunk;
         for (; kb < KB; kb += S) {
           const uint32_t phase = ((step + kb) / S) & 1;
+          const uint64_t t0 = kProf ? globaltimer() : 0;
           if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
+          if (kProf) w_empty += globaltimer() - t0;
           mbar_arrive_expect_tx(&full[p], bytes);
           armed = true;
           armed_parity = phase;
@@ -299,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
         step += KB;
       }
       if (armed) mbar_wait_drain(&full[p], armed_parity, st, kSiteDrainCopies);
+      if (kProf) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
     }
   } else if (wg == 3) {
     regs_dec_mma();
@@ -314,6 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
         uint32_t idb = 0, acc0 = 0;
         bool two = false;   // the token scales span two chunks (N > 128)
         Cursor cur;
+        uint64_t w_full = 0, w_tempty = 0;
+        const uint64_t t_start = kProf ? globaltimer() : 0;
+        const long long c_start = kProf ? clock64() : 0;
         auto start_task = [&]() -> bool {
           if (*s_abort || !sch.next(cur, q, st, s_abort, false, lane, kSiteQueueFull)) return false;
           KB = cur.t.type == 1 ? args.KB1 : args.KB2;
@@ -322,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
           two = n16 > 128;
           const int buf = it % C::kAccBufs;
           acc0 = tmem + buf * 2 * C::kAccStride;
+          const long long t0 = kProf ? clock64() : 0;
           if (!mbar_wait(&tempty[buf], ((it / C::kAccBufs) & 1) ^ 1, st, s_abort, kSiteTmemEmpty)) return false;
+          if (kProf) w_tempty += clock64() - t0;
           tc_fence_after();
           return true;
         };
@@ -331,9 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
 #pragma unroll
           for (int s = 0; s < S; ++s) {
             if (live) {
+              const long long t1 = kProf ? clock64() : 0;
               if (!mbar_wait(&full[s], phase, st, s_abort, kSiteFull)) {
                 live = false;
               } else {
+                if (kProf) w_full += clock64() - t1;
                 tc_fence_after();
                 const uint32_t sf = tmem + C::kSfCol0 + s * C::kSfColsPerStage;
                 tc_cp_32x128b_warpx4(sf, dsfw + ((s * 2 * kSFChunk) >> 4));
@@ -364,6 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
         }
         tc_commit(drain);
         mbar_wait_drain(drain, 0, st, kSiteDrainMma);
+        if (kProf) {
+          args.prof[blockIdx.x * 8 + 1] = w_full;
+          args.prof[blockIdx.x * 8 + 2] = w_tempty;
+          args.prof[blockIdx.x * 8 + 3] = globaltimer() - t_start;
+          args.prof[blockIdx.x * 8 + 4] = it;
+          args.prof[blockIdx.x * 8 + 7] = clock64() - c_start;
+        }
       }
       __syncwarp();
     } else if (warp < kGatherWarp0 + kGatherWarps && args.mode == 3) {
@@ -378,13 +402,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
     const int half = (warp - kEpiWarp0) >> 2;    // this warp takes 16-token chunks half, half + 2, ...
     const uint32_t qoff = static_cast<uint32_t>(quad * 32) << 16;
     int it = 0;
+    uint64_t w_tfull = 0, busy = 0, t_mark = 0;
     for (Cursor c; sch.next(c, q, st, s_abort, true, lane, kSiteQueueFull); ++it) {
       const Task& t = c.t;
       const int buf = it % C::kAccBufs;
       const uint32_t a0 = tmem + qoff + buf * 2 * C::kAccStride;
       const uint32_t a1 = a0 + C::kAccStride;
       const int nch = (t.valid + 15) >> 4;
+      const uint64_t t0 = kProf ? globaltimer() : 0;
+      if (kProf && it > 0) busy += t0 - t_mark;
       if (!mbar_wait(&tfull[buf], (it / C::kAccBufs) & 1, st, s_abort, kSiteTmemFull)) break;
+      if (kProf) {
+        t_mark = globaltimer();
+        w_tfull += t_mark - t0;
+      }
       tc_fence_after();
       const size_t row0 = static_cast<size_t>(t.b) * BT;
       if (t.type == 1) {
@@ -477,9 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_sw_kernel(const __grid_co
         }
       }
     }
+    if (kProf && it > 0) busy += globaltimer() - t_mark;
+    if (kProf && warp == kEpiWarp0 && lane == 0) {
+      args.prof[blockIdx.x * 8 + 5] = w_tfull;
+      args.prof[blockIdx.x * 8 + 6] = busy;
+    }
     if (args.early_combine) {
-      if (args.pbf16) early_combine<__nv_bfloat16>(args, kEpiWarps, s_blk, st, s_abort, lane);
-      else early_combine<float>(args, kEpiWarps, s_blk, st, s_abort, lane);
+      if (args.pbf16) early_combine<__nv_bfloat16>(args, kEpiWarps, args.NB2, s_blk, st, s_abort, lane);
+      else early_combine<float>(args, kEpiWarps, args.NB2, s_blk, st, s_abort, lane);
     }
   }
 
@@ -523,6 +559,7 @@ cudaError_t launch_impl(const GemmLaunch& g, int mode, int lag, int l1_extra, cu
   a.ctr_l2 = a.cmb + kCombineCounters;
   a.deferred = a.ctr_l2 + L.E;
   a.status = W.status; a.timeout_ns = g.timeout_ns;
+  a.prof = g.prof ? g.prof + (mode == 2 ? 8 * 1024 : 0) : nullptr;
   {
     // W1 as (k, row, half): one box of {128 k, 128 rows, 2 halves} is 128 gate
     // rows followed by the matching 128 up rows (A0, then A1)
@@ -546,7 +583,7 @@ cudaError_t launch_impl(const GemmLaunch& g, int mode, int lag, int l1_extra, cu
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  auto kernel = gemm_mx_sw_kernel<BT>;
+  auto kernel = a.prof ? gemm_mx_sw_kernel<BT, true> : gemm_mx_sw_kernel<BT, false>;
   if (cudaError_t e = configure_kernel(reinterpret_cast<const void*>(kernel), kLaunchRegs, C::total(kMaxE) + 1024))
     return e;
   cudaLaunchConfig_t cfg = {};

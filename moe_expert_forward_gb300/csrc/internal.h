@@ -77,6 +77,9 @@ const DevInfo& dev_info();
 // many registers a thread (the setmaxnreg splits depend on it); when
 // smem_bytes > 0, raise the kernel's dynamic shared-memory limit to it.
 cudaError_t configure_kernel(const void* fn, int want_regs, int smem_bytes);
+// How many 2-CTA clusters of this kernel (blockDim threads, smem_bytes of dynamic
+// shared memory) the current device holds at once; cached per kernel and device.
+cudaError_t max_pair_clusters(const void* fn, int threads, int smem_bytes, int* clusters);
 
 // ---- launchers (return cudaError_t of the launch)
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
@@ -116,6 +119,7 @@ struct GemmLaunch {
   const int32_t* topk_idx;  // early combine: the routing and the bf16 output [T, H]
   void* out;
   bool pdl;                 // programmatic launch after the routing kernel
+  bool per_block;           // token-M kernel: deal (weight tile, pool block) pairs as separate groups
 };
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
@@ -124,6 +128,10 @@ int mx_lag_auto(int E);
 // tokens as N (gemm_mx_sw.cu); g.L->BT must be a supported block size.
 cudaError_t launch_gemm_mx_sw(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
 bool mx_sw_block_supported(int bt);
+// The swapped form on 2-CTA clusters (gemm_mx_pair.cu): M = 256 weight rows per
+// tcgen05 cta_group::2 MMA, half of each block's tokens in each CTA.
+cudaError_t launch_gemm_mx_pair(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
+bool mx_pair_block_supported(int bt);
 
 struct GemmLaunchF8 {
   const Layout* L;

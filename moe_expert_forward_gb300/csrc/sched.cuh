@@ -47,6 +47,11 @@ struct Sched {
   const int* cnt;   // [E]
   int E, NB1, NB2, mode, lag;
   int BT = kBT;     // pool rows per block
+  // false: a group is one weight tile with every pool block of its expert, taken
+  // back to back by one CTA; true: a group is one (weight tile, pool block) pair,
+  // so the blocks of one tile are dealt to neighbouring free CTAs, which stream
+  // the tile's k-blocks at about the same time (the second read hits L2)
+  bool per_block = false;
 
   __device__ __forceinline__ int largest_leq(const int* a, int n, int v, int scale) const {
     int lo = 0, hi = n - 1;                  // largest i < n with a[i] * scale <= v
@@ -56,44 +61,73 @@ struct Sched {
     }
     return lo;
   }
+  // units of expert-range [0, u): experts (tile groups) or pool blocks (per block)
+  __device__ __forceinline__ int units(int u) const { return per_block ? blk[u] : u; }
   __device__ __forceinline__ int groups() const {
-    return mode == 1 ? E * NB1 : (mode == 2 ? E * NB2 : E * (NB1 + NB2));
+    return mode == 1 ? units(E) * NB1 : (mode == 2 ? units(E) * NB2 : units(E) * (NB1 + NB2));
   }
   // mode 3: groups in the segments before segment u
   __device__ __forceinline__ int groups_before(int u) const {
     const int l1 = u < E ? u : E;
     int l2 = u - lag;
     l2 = l2 < 0 ? 0 : (l2 > E ? E : l2);
-    return l1 * NB1 + l2 * NB2;
+    return units(l1) * NB1 + units(l2) * NB2;
   }
-  __device__ __forceinline__ void group(int g, Task& t) const {
+  // Group g's task (expert, tile, type); *bl receives its pool block within the
+  // expert when groups are per block (0 otherwise).
+  __device__ __forceinline__ void group(int g, Task& t, int* bl) const {
+    int u, r;
     if (mode != 3) {
       const int nbw = mode == 1 ? NB1 : NB2;
       t.type = mode;
-      t.e = g / nbw;
-      t.n = g - t.e * nbw;
-      return;
+      u = per_block ? largest_leq(blk, E, g, nbw) : g / nbw;
+      r = g - units(u) * nbw;
+    } else {
+      int lo = 0, hi = E + lag - 1;            // the segment holding group g
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (groups_before(mid) <= g) lo = mid; else hi = mid - 1;
+      }
+      u = lo;
+      r = g - groups_before(lo);
+      const int n1 = lo < E ? NB1 * (per_block ? blk[lo + 1] - blk[lo] : 1) : 0;
+      if (r < n1) {
+        t.type = 1;
+      } else {
+        t.type = 2;
+        u = lo - lag;
+        r -= n1;
+      }
     }
-    int lo = 0, hi = E + lag - 1;            // the segment holding group g
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (groups_before(mid) <= g) lo = mid; else hi = mid - 1;
+    t.e = u;
+    if (per_block) {
+      const int nb = blk[u + 1] - blk[u];
+      t.n = r / nb;
+      *bl = r - t.n * nb;
+    } else {
+      t.n = r;
+      *bl = 0;
     }
-    const int r = g - groups_before(lo);
-    const int n1 = lo < E ? NB1 : 0;
-    if (r < n1) { t.type = 1; t.e = lo; t.n = r; }
-    else { t.type = 2; t.e = lo - lag; t.n = r - n1; }
   }
   __device__ __forceinline__ void block(Cursor& c) const {
     c.t.b = blk[c.t.e] + c.bl;
     const int rem = cnt[c.t.e] - c.bl * BT;
     c.t.valid = rem < BT ? rem : BT;
-    c.t.last = c.bl + 1 == c.nb;
-    c.t.rev = (c.bl & 1) != 0;
+    if (per_block) {
+      // the expert's other blocks of this tile run concurrently on other CTAs:
+      // keep the weights in L2 unless this is the tile's only reader
+      c.t.last = blk[c.t.e + 1] - blk[c.t.e] == 1;
+      c.t.rev = false;
+    } else {
+      c.t.last = c.bl + 1 == c.nb;
+      c.t.rev = (c.bl & 1) != 0;
+    }
   }
   __device__ __forceinline__ int group_blocks(int g) const {
+    if (per_block) return 1;                   // every per-block group has its block
     Task t;
-    group(g, t);
+    int bl;
+    group(g, t, &bl);
     return blk[t.e + 1] - blk[t.e];
   }
   // Advance to this CTA's next task; false when there is none (or on abort).
@@ -119,9 +153,15 @@ struct Sched {
     if (warp_wide) g = __shfl_sync(0xffffffffu, g, 0);
     c.nb = 0;
     if (g < 0) return false;
-    group(g, c.t);
-    c.nb = blk[c.t.e + 1] - blk[c.t.e];
-    c.bl = 0;
+    int bl;
+    group(g, c.t, &bl);
+    if (per_block) {
+      c.bl = bl;
+      c.nb = bl + 1;                           // this group's only block
+    } else {
+      c.nb = blk[c.t.e + 1] - blk[c.t.e];
+      c.bl = 0;
+    }
     block(c);
     return true;
   }

@@ -70,11 +70,11 @@ __device__ __forceinline__ void gather_rows(const ArgsT& args, const int* s_blk,
 // acquire) is combined at once by the warp, any other is appended to a
 // deferred list.  Pass 2 takes the deferred tokens and waits, bounded, for
 // their experts.  The arithmetic is the combine kernel's (combine.cuh).  Every
-// branch below is warp-uniform.  Each L2 task adds one per epilogue warp
-// (epi_warps of them) to ctr_l2[e].  Fields: T, K, E, H, NB2, partials, cmb,
-// topk_idx, ctr_l2, deferred, out.
+// branch below is warp-uniform.  Each of an expert's l2_tiles L2 tasks per
+// pool block adds one per epilogue warp (epi_warps of them) to ctr_l2[e].
+// Fields: T, K, E, H, partials, cmb, topk_idx, ctr_l2, deferred, out.
 template <typename PartT, typename ArgsT>
-__device__ __forceinline__ void early_combine(const ArgsT& args, int epi_warps, const int* s_blk, const Status& st,
+__device__ __forceinline__ void early_combine(const ArgsT& args, int epi_warps, int l2_tiles, const int* s_blk, const Status& st,
                                               volatile int* s_abort, int lane) {
   const int T = args.T, K = args.K, E = args.E;
   const PartT* part = reinterpret_cast<const PartT*>(args.partials);
@@ -94,7 +94,7 @@ __device__ __forceinline__ void early_combine(const ArgsT& args, int epi_warps, 
     if (lane < K) {
       const int e = __ldg(args.topk_idx + static_cast<int64_t>(t) * K + lane);
       v = e >= 0 && e < E;
-      if (v) ok = ld_acquire_gpu(args.ctr_l2 + e) >= epi_warps * args.NB2 * (s_blk[e + 1] - s_blk[e]);
+      if (v) ok = ld_acquire_gpu(args.ctr_l2 + e) >= epi_warps * l2_tiles * (s_blk[e + 1] - s_blk[e]);
     }
     vmask = __ballot_sync(0xffffffffu, v);
     const bool all = __all_sync(0xffffffffu, ok);
