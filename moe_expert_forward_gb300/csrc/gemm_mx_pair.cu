@@ -568,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_pair_kernel(const __grid_
     const int half = (warp - kEpiWarp0) >> 2;     // 16-token chunks half, half + 2, ...
     const uint32_t qoff = static_cast<uint32_t>(quad * 32) << 16;
     int it = 0;
-    uint64_t w_tfull = 0, busy = 0, t_mark = 0;
+    uint64_t w_tfull = 0, busy = 0, t_mark = 0, t_rel = 0;
+    uint64_t hold1 = 0, post1 = 0, hold2 = 0, post2 = 0;   // profiling build: per task type
     for (Cursor c; pair_next(sch, c, q, rank, st, s_abort, true, lane); ++it) {
       const Task& t = c.t;
       const bool l1 = t.type == 1;
@@ -623,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_pair_kernel(const __grid_
           if (leader) mbar_arrive(&tempty[buf]);
           else arrive_cluster(cl_map(&tempty[buf], 0));
         }
+        if (kProf) t_rel = globaltimer();
       };
       if (mine <= 1) release();
 #pragma unroll
@@ -691,6 +693,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_pair_kernel(const __grid_
           if (i + 2 >= mine) release();   // the warp's last loads have landed
         }
       }
+      if (kProf) {   // hold = accumulator ready -> released, post = released -> task done
+        const uint64_t t_end = globaltimer();
+        (l1 ? hold1 : hold2) += t_rel - t_mark;
+        (l1 ? post1 : post2) += t_end - t_rel;
+      }
       if (l1 && args.mode == 3) {
         fence_proxy_async_global();              // the codes are read by TMA later
         __syncwarp();
@@ -705,6 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_pair_kernel(const __grid_
     if (kProf && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
       args.prof[blockIdx.x * 8 + 6] = busy;
+      args.prof[4096 + blockIdx.x] = hold1;
+      args.prof[4096 + 1024 + blockIdx.x] = post1;
+      args.prof[4096 + 2048 + blockIdx.x] = hold2;
+      args.prof[4096 + 3072 + blockIdx.x] = post2;
     }
     if (args.early_combine) {
       if (args.pbf16) early_combine<__nv_bfloat16>(args, 2 * kEpiWarps, args.PB2, args.blk_off, st, s_abort, lane);
