@@ -411,7 +411,7 @@ def run_ours(args, ws_n, rank, local):
 
 # ------------------------------------------------------------------ oracle (CPU) runs
 # tokens the oracle baseline times once per workload: about 10-30 s of host work each
-CPU_TOKENS = {"tiny": 64, "flash": 16, "pro": 4, "decode": 16, "f8": 8}
+CPU_TOKENS = {"tiny": 64, "flash": 16, "pro": 4, "decode": 16, "f8": 8, "pro96": 4, "f8x": 8}
 
 
 def oracle_tokens(cfg, inp, rows):

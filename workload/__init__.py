@@ -61,6 +61,12 @@ CONFIGS: Dict[str, Config] = {
     "f8": Config("f8", T=8192, H=4096, I=2048, E=256, K=8, variant="f8", seed=4),
 }
 CONFIG_ORDER = ["tiny", "flash", "pro", "decode", "f8"]
+# Reduced cases for hardware-counter captures: the pro-shaped and FP8-shaped
+# workloads with fewer tokens and experts but the same tokens per expert (128
+# and 256) and the same H, I and top-k, so that a multi-pass profile holds a few
+# GB on the device.  They are not benchmark workloads.
+CONFIGS["pro96"] = Config("pro96", T=2048, H=7168, I=3072, E=96, K=6, seed=2)
+CONFIGS["f8x"] = Config("f8x", T=2048, H=4096, I=2048, E=64, K=8, variant="f8", seed=4)
 
 
 def _gen(seed: int, stream: int, device) -> torch.Generator:
