@@ -516,8 +516,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=2,
                     help="--impl reference: tokens of the workload the oracle processes per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--swap-ab", type=int, choices=[0, 1], default=None,
-                    help="MX: 1 = weights as the MMA's M side, each pool block's tokens as N; default: the library's")
+    ap.add_argument("--swap-ab", type=int, choices=[0, 1, 2], default=None,
+                    help="MX: 1 = weights as the MMA M side, each pool block tokens as N; 2 = the same on 2-CTA clusters; default: the library choice")
     ap.add_argument("--block-m", type=int, default=0, help="tokens per pool block (0: the library's choice)")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,
                     help="1: gather + L1 + L2 as one lag-ordered persistent launch; default: the library's")
