@@ -142,8 +142,8 @@ def workload_accounting(cfg, idx: np.ndarray, part_elem: int = 4, x_bf16: bool =
     gather quantises it)."""
     T, H, I, E, K = cfg.T, cfg.H, cfg.I, cfg.E, cfg.K
     valid = (idx >= 0) & (idx < E)
-    touched = int(np.unique(idx[valid]).size)
-    pairs = int(valid.sum())
+    touched = int(np.unique(idx[valid]).size) + cfg.S      # shared experts: touched by every token
+    pairs = int(valid.sum()) + T * cfg.S
     if cfg.variant == "mx":
         w1_b = 2 * I * H * (0.5 + 1 / 32)
         w2_b = H * I * (0.5 + 1 / 32)
@@ -190,11 +190,13 @@ def run_ours(args, ws_n, rank, local):
     B.build()
     import moe_expert_forward_gb300 as M
 
-    cfg = W.CONFIGS[args.config]
+    cfg = W.CONFIGS[args.config].with_(S=args.shared)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = W.make_inputs(cfg, dev)
     opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
+    opt.shared_experts = cfg.S
+    opt.f8_act_gran = args.f8_gran
     if args.fused is not None:
         opt.fused = args.fused
     opt.partials_bf16 = 1 if args.partials == "bf16" else 0
@@ -209,7 +211,7 @@ def run_ours(args, ws_n, rank, local):
         inp["x"], inp["x_sf"] = W.make_x_bf16(cfg, dev), None
         opt.x_bf16 = 1
     fused = bool(opt.fused) and cfg.variant == "mx"
-    w1p, w2p = M.prepare_weights(inp["w1_sf"], inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
+    w1p, w2p = M.prepare_weights(inp["w1_sf"], inp["w2_sf"], cfg.H, cfg.I, cfg.E + cfg.S, opt)
     ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt, dev)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -373,6 +375,7 @@ def run_ours(args, ws_n, rank, local):
                    "parallelism": f"replicas x{ws_n} (no data-path collective)",
                    "fused_stream": fused, "early_combine": early, "partials": args.partials, "x": args.x,
                    "swap_ab": int(opt.swap_ab), "block_m": int(opt.block_m),
+                   "shared_experts": cfg.S, "f8_act_gran": int(opt.f8_act_gran),
                    "e2e_policy": "copies on streams of their own, two buffer sets (step i+1 in and step i-1 out "
                                  "overlap step i); no L2 flush: every step reads >= 2.5 GB of weights"},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
@@ -405,7 +408,7 @@ def run_ours(args, ws_n, rank, local):
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_tokens or CPU_TOKENS[cfg.name])
+        result["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_tokens or CPU_TOKENS[cfg.name], args.f8_gran)
     return result
 
 
@@ -414,8 +417,11 @@ def run_ours(args, ws_n, rank, local):
 CPU_TOKENS = {"tiny": 64, "flash": 16, "pro": 4, "decode": 16, "f8": 8, "pro96": 4, "f8x": 8}
 
 
-def oracle_tokens(cfg, inp, rows):
+def oracle_tokens(cfg, inp, rows, f8_opt=0):
+    """Times the oracle on `rows`; f8_opt is the f8_act_gran option (0: per 128,
+    -1: the pages' shape rule, else the width)."""
     import oracle as O
+    f8_gran = O.f8_act_gran(cfg.H, cfg.I) if f8_opt == -1 else (f8_opt or 128)
     bf16_x = inp["x_sf"] is None             # the layer quantises bf16 rows first: the oracle does too
     x = inp["x"][rows].float().cpu().numpy() if bf16_x else inp["x"][rows].cpu().numpy()
     x_sf = None if bf16_x else inp["x_sf"][rows].cpu().numpy()
@@ -428,13 +434,14 @@ def oracle_tokens(cfg, inp, rows):
             cache[e] = tuple(inp[k][e].cpu().numpy() for k in ("w1", "w1_sf", "w2", "w2_sf"))
         return cache[e]
     # fetch the weights first so that only the oracle's arithmetic is timed
-    for e in np.unique(idx[idx >= 0]):
+    for e in list(np.unique(idx[(idx >= 0) & (idx < cfg.E)])) + list(range(cfg.E, cfg.E + cfg.S)):
         experts(int(e))
     t0 = time.perf_counter()
     c0 = time.process_time()
     if bf16_x:
         x, x_sf = O.quantise_x(x, cfg.variant)
-    O.forward(range(len(rows)), x, x_sf, idx, w, experts, cfg.H, cfg.I, cfg.E, cfg.variant)
+    O.forward(range(len(rows)), x, x_sf, idx, w, experts, cfg.H, cfg.I, cfg.E, cfg.variant,
+              f8_gran=f8_gran, shared=cfg.S)
     dt = time.perf_counter() - t0
     return dt, (time.process_time() - c0) / dt
 
@@ -447,9 +454,9 @@ def blas_threads() -> str:
     return "unset (numpy's BLAS default)"
 
 
-def cpu_baseline(cfg, inp, n_tokens):
+def cpu_baseline(cfg, inp, n_tokens, f8_opt=0):
     rows = list(range(min(n_tokens, cfg.T)))
-    dt, busy = oracle_tokens(cfg, inp, rows)
+    dt, busy = oracle_tokens(cfg, inp, rows, f8_opt)
     return {"value": len(rows) / dt, "unit": "tokens/s", "cores": round(busy, 2),
             "cores_available": len(os.sched_getaffinity(0)), "blas_threads": blas_threads(),
             "cores_def": "CPU seconds / wall seconds of the timed oracle call (the average number of "
@@ -462,7 +469,7 @@ def cpu_baseline(cfg, inp, n_tokens):
 
 
 def run_reference(args, ws_n, rank):
-    cfg = W.CONFIGS[args.config]
+    cfg = W.CONFIGS[args.config].with_(S=args.shared)
     if rank != 0:
         return None
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -473,10 +480,11 @@ def run_reference(args, ws_n, rank):
     n = args.ref_tokens
     rows = list(range(min(n, cfg.T)))
     used = sorted(set(int(e) for e in inp["topk_idx"][rows].cpu().numpy().ravel() if e >= 0))
+    used += list(range(cfg.E, cfg.E + cfg.S))          # shared experts
     inp.update(W.make_weights(cfg, dev, experts=used))
     times, busy = [], []
     for i in range(max(args.warmup, 0) + args.steps):
-        dt, b = oracle_tokens(cfg, inp, rows)
+        dt, b = oracle_tokens(cfg, inp, rows, args.f8_gran)
         if i >= args.warmup:
             times.append(dt)
             busy.append(b)
@@ -519,6 +527,10 @@ def main():
     ap.add_argument("--swap-ab", type=int, choices=[0, 1, 2], default=None,
                     help="MX: 1 = weights as the MMA M side, each pool block tokens as N; 2 = the same on 2-CTA clusters; default: the library choice")
     ap.add_argument("--block-m", type=int, default=0, help="tokens per pool block (0: the library's choice)")
+    ap.add_argument("--shared", type=int, default=0,
+                    help="shared experts added to the workload (used by every token with weight 1)")
+    ap.add_argument("--f8-gran", type=int, choices=[-1, 0, 64, 128], default=0,
+                    help="FP8: intermediate scale width (0: per 128, the library default; -1: the pages' shape rule)")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,
                     help="1: gather + L1 + L2 as one lag-ordered persistent launch; default: the library's")
     args = ap.parse_args()

@@ -31,11 +31,11 @@
  *                      (value 2^(b-127)) per 32 contiguous elements along the
  *                      contraction dimension; tcgen05 kind::mxf8f6f4.
  *   MM_MOE_VARIANT_F8  e4m3 activations with one fp32 scale per 1x128, e4m3
- *                      weights with one fp32 scale per 128x128 block (H and I
- *                      at most 8192, else MM_MOE_ERR_UNSUPPORTED); the
- *                      intermediate is requantised per 128 with a raw fp32
- *                      scale amax/448 (DeepGEMM PR #440, "Why the order and not
- *                      the pool size"); tcgen05 kind::f8f6f4.
+ *                      weights with one fp32 scale per 128x128 block; the
+ *                      intermediate is requantised per 128 (or per 64, see
+ *                      f8_act_gran) with a raw fp32 scale amax/448 (DeepGEMM
+ *                      PR #440, "Why the order and not the pool size");
+ *                      tcgen05 kind::f8f6f4.
  *
  * Layouts (T tokens, H hidden, I intermediate, E experts, K top-k):
  *   x        u8  [T, H]          e4m3 codes
@@ -136,6 +136,20 @@ typedef struct mm_moe_options {
                                    swap_ab 0; for swap_ab 1, 160 when the expected tokens per expert
                                    T*K/E exceed 64, else 80); otherwise 128 (swap_ab 0) or 80 / 160
                                    (swap_ab 1 or 2), anything else MM_MOE_ERR_UNSUPPORTED */
+  int f8_act_gran;              /* F8 variant: width of the intermediate's fp32 scale blocks along I (the
+                                   pages' l2_act_sf_gran_k).  0 (default) or 128: per 128; 64: per 64,
+                                   and the L2 GEMM dequantises each 64-wide half of a 128-K step with
+                                   its own scale; -1: the pages' shape rule (128 when H % 512 == 0 and
+                                   2*I % 512 == 0, else 64).  Any other value: MM_MOE_ERR_INVALID_ARG.
+                                   The MX variant ignores it (its intermediate scales are UE8M0 per 32). */
+  int shared_experts;           /* S >= 0 shared experts (default 0): experts E .. E+S-1 of w1 / w2 and
+                                   their scales, which every token uses with weight 1 after its K
+                                   routed slots; their outputs join the fixed-order top-k sum as slots
+                                   K .. K+S-1.  w1, w2 and their scale arrays then hold E + S experts
+                                   (mm_moe_weight_sf_size / mm_moe_prepare_weights take E + S), topk_idx
+                                   still names routed experts only (ids >= E are out of range), and
+                                   K + S <= 16, E + S <= 1024.  The shared experts' tiles run in the same
+                                   launches as the routed ones. */
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

@@ -41,6 +41,7 @@ class mm_moe_options(ctypes.Structure):
                 ("partials_bf16", ctypes.c_int), ("activation_clamp", ctypes.c_float),
                 ("precise_swiglu", ctypes.c_int), ("x_bf16", ctypes.c_int), ("early_combine", ctypes.c_int),
                 ("swap_ab", ctypes.c_int), ("block_m", ctypes.c_int),
+                ("f8_act_gran", ctypes.c_int), ("shared_experts", ctypes.c_int),
                 ("timing_events", ctypes.c_void_p)]
 
 
@@ -255,6 +256,9 @@ def forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, H, I, E, wor
     T, K = topk_idx.shape
     opt = opt or options()
     need = _input_bytes(opt.variant, T, H, I, E, K)
+    S = max(int(opt.shared_experts), 0)   # shared experts: the weight arrays hold E + S experts
+    wneed = _input_bytes(opt.variant, T, H, I, E + S, K)
+    need.update({k: wneed[k] for k in ("w1", "w2")})
     if opt.x_bf16:
         need["x"] = 2 * T * H          # bf16 rows; the gather quantises them, x_sf is not read
     for name, t in (("x", x), ("x_sf", x_sf), ("topk_idx", topk_idx), ("topk_w", topk_w), ("w1", w1), ("w2", w2),
@@ -263,7 +267,7 @@ def forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, H, I, E, wor
             continue
         if T > 0 or name in ("w1", "w2"):
             _need(t, need[name], name, "forward")
-    n1, n2 = mm_moe_weight_sf_size(opt, H, I, E)
+    n1, n2 = mm_moe_weight_sf_size(opt, H, I, E + S)
     _need(w1_sfp, n1, "w1_sfp", "forward")
     _need(w2_sfp, n2, "w2_sfp", "forward")
     _need(workspace, 0, "workspace", "forward")   # its size goes down with it: the library checks that

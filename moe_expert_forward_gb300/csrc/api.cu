@@ -14,9 +14,11 @@ namespace mm {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags, int partials_bf16, int BT) {
+Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags, int partials_bf16, int BT,
+                   int act_gran, int S) {
   Layout L{};
-  L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = BT;
+  L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = BT; L.S = S;
+  L.act_gran = variant == MM_MOE_VARIANT_MX ? 32 : act_gran;
   L.CPB = (BT + 127) / 128;
   const int64_t pairs = static_cast<int64_t>(T) * K;
   const int64_t live_experts = pairs < E ? pairs : E;
@@ -33,7 +35,7 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.slot = o; o = align_up(o + sizeof(int) * pairs, 256);
   L.src = o; o = align_up(o + sizeof(int) * L.P, 1024);
   L.pool_x = o; o = align_up(o + static_cast<size_t>(L.P) * H, 1024);
-  // MX scales: [block][kb][CPB][512-byte chunk]; F8 scales: fp32 [P][kdim / 128]
+  // MX scales: [block][kb][CPB][512-byte chunk]; F8 scales: fp32 [P][H / 128] and [P][I / act_gran]
   const size_t chunks = static_cast<size_t>(L.nblk_cap) * L.CPB * kSFChunk;
   L.pool_x_sf = o;
   o = align_up(o + (variant == MM_MOE_VARIANT_MX ? chunks * (H / 128)
@@ -41,7 +43,7 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.pool2 = o; o = align_up(o + static_cast<size_t>(L.P) * I, 1024);
   L.pool2_sf = o;
   o = align_up(o + (variant == MM_MOE_VARIANT_MX ? chunks * (I / 128)
-                                                 : static_cast<size_t>(L.P) * (I / 128) * sizeof(float)), 1024);
+                                                 : static_cast<size_t>(L.P) * (I / L.act_gran) * sizeof(float)), 1024);
   L.part_elem = partials_bf16 ? 2 : 4;
   L.part = o; o = align_up(o + static_cast<size_t>(pairs) * H * L.part_elem, 1024);
   L.dbg = o;
@@ -49,6 +51,10 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   o = align_up(o + L.dbg_bytes, 1024);
   L.prof = o;
   o = align_up(o + ((debug_flags & 2) ? 2 * 8 * 1024 * sizeof(unsigned long long) : 0), 1024);
+  L.ext_idx = o;
+  o = align_up(o + (S ? sizeof(int32_t) * pairs : 0), 256);
+  L.ext_w = o;
+  o = align_up(o + (S ? sizeof(float) * pairs : 0), 1024);
   L.total = o;
   return L;
 }
@@ -69,7 +75,9 @@ WsPtrs ws_ptrs(void* ws, const Layout& L) {
   W.pool2_sf = b + L.pool2_sf;
   W.part = reinterpret_cast<float*>(b + L.part);
   W.dbg = L.dbg_bytes ? reinterpret_cast<float*>(b + L.dbg) : nullptr;
-  W.prof = (L.total > L.prof) ? reinterpret_cast<unsigned long long*>(b + L.prof) : nullptr;
+  W.prof = (L.ext_idx > L.prof) ? reinterpret_cast<unsigned long long*>(b + L.prof) : nullptr;
+  W.ext_idx = L.S ? reinterpret_cast<int32_t*>(b + L.ext_idx) : nullptr;
+  W.ext_w = L.S ? reinterpret_cast<float*>(b + L.ext_w) : nullptr;
   return W;
 }
 
@@ -214,11 +222,11 @@ mm_moe_options resolve(const mm_moe_options* opt) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int check_shape(int T, int H, int I, int E, int K) {
-  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || K <= 0) return MM_MOE_ERR_INVALID_ARG;
+int check_shape(int T, int H, int I, int E, int K, int S = 0) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || K <= 0 || S < 0) return MM_MOE_ERR_INVALID_ARG;
   if (H % 128 || I % 128) return MM_MOE_ERR_INVALID_ARG;
-  if (K > kMaxK || K > E || E > kMaxE) return MM_MOE_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(T) * K > (int64_t(1) << 30)) return MM_MOE_ERR_INVALID_ARG;
+  if (K + S > kMaxK || K > E || E + S > kMaxE) return MM_MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * (K + S) > (int64_t(1) << 30)) return MM_MOE_ERR_INVALID_ARG;
   return MM_MOE_OK;
 }
 
@@ -233,6 +241,8 @@ struct Plan {
 constexpr int kSwapLargeBlockTokens = 64;
 
 int make_plan(const mm_moe_options& o, int T, int K, int E, Plan* p) {
+  if (o.f8_act_gran != 0 && o.f8_act_gran != -1 && o.f8_act_gran != 64 && o.f8_act_gran != 128)
+    return MM_MOE_ERR_INVALID_ARG;
   if (o.variant == MM_MOE_VARIANT_F8) {
     if (o.swap_ab > 0 || (o.block_m != 0 && o.block_m != kBT)) return MM_MOE_ERR_UNSUPPORTED;
     *p = {false, false, kBT};
@@ -246,15 +256,22 @@ int make_plan(const mm_moe_options& o, int T, int K, int E, Plan* p) {
     *p = {false, false, kBT};
     return MM_MOE_OK;
   }
-  const int64_t per_expert = static_cast<int64_t>(T) * K / E;
+  const int64_t per_expert = static_cast<int64_t>(T) * (K + o.shared_experts) / (E + o.shared_experts);
   const int bt = o.block_m ? o.block_m : (per_expert > kSwapLargeBlockTokens ? 160 : 80);
   if (!(pair ? mx_pair_block_supported(bt) : mx_sw_block_supported(bt))) return MM_MOE_ERR_UNSUPPORTED;
   *p = {true, pair, bt};
   return MM_MOE_OK;
 }
 
+// 0: per 128 (the default); -1: the pages' shape rule; 64 / 128 pinned
+int f8_gran(const mm_moe_options& o, int H, int I) {
+  return o.f8_act_gran == -1 ? f8_gran_rule(H, I) : (o.f8_act_gran ? o.f8_act_gran : 128);
+}
+
+// E and K are the caller's routed counts; the layout counts the shared experts in both.
 Layout layout_for(const mm_moe_options& o, int T, int H, int I, int E, int K, const Plan& p) {
-  return make_layout(T, H, I, E, K, o.variant, o.debug_flags, o.partials_bf16, p.BT);
+  const int S = o.shared_experts;
+  return make_layout(T, H, I, E + S, K + S, o.variant, o.debug_flags, o.partials_bf16, p.BT, f8_gran(o, H, I), S);
 }
 
 int device_supported() {
@@ -283,7 +300,7 @@ void mm_moe_default_options(mm_moe_options* opt) {
 int mm_moe_workspace_size(const mm_moe_options* opt, int T, int H, int I, int E, int K, size_t* bytes) {
   if (!bytes) return MM_MOE_ERR_INVALID_ARG;
   const mm_moe_options o = resolve(opt);
-  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (int r = check_shape(T, H, I, E, K, o.shared_experts)) return r;
   if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
   Plan p;
   if (int r = make_plan(o, T, K, E, &p)) return r;
@@ -354,7 +371,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
                    const void* w1_sfp, const void* w2, const void* w2_sfp, void* out, int T, int H, int I, int E,
                    int K, void* workspace, size_t workspace_bytes, const mm_moe_options* opt, void* stream) {
   const mm_moe_options o = resolve(opt);
-  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (int r = check_shape(T, H, I, E, K, o.shared_experts)) return r;
   if (o.variant != MM_MOE_VARIANT_MX && o.variant != MM_MOE_VARIANT_F8) return MM_MOE_ERR_INVALID_ARG;
   if (T == 0) {
     // nothing to compute; leave a clean status word for mm_moe_sync_status
@@ -371,8 +388,6 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (device_supported()) return MM_MOE_ERR_UNSUPPORTED;
   // cta_pairs is reserved: 0 and 1 mean one CTA per tile group, anything else is not built
   if (o.cta_pairs != 0 && o.cta_pairs != 1) return MM_MOE_ERR_UNSUPPORTED;
-  // the F8 epilogue stages each task's weight scales in shared memory for up to kF8MaxKB k-blocks
-  if (o.variant == MM_MOE_VARIANT_F8 && (H / 128 > kF8MaxKB || I / 128 > kF8MaxKB)) return MM_MOE_ERR_UNSUPPORTED;
   Plan plan;
   if (int r = make_plan(o, T, K, E, &plan)) return r;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
@@ -384,6 +399,9 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   const WsPtrs W = ws_ptrs(workspace, L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
+  // from here on the routing, the expert count and the slot count include the shared experts
+  const int32_t* idx = L.S ? W.ext_idx : topk_idx;
+  const float* wts = L.S ? W.ext_w : topk_w;
 
   cudaEvent_t* ev = static_cast<cudaEvent_t*>(o.timing_events);
   auto mark = [&](int i) -> cudaError_t { return ev && ev[i] ? cudaEventRecord(ev[i], s) : cudaSuccess; };
@@ -397,9 +415,10 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   // cleared before the routing kernels so that those and the GEMM are adjacent on the stream
   if (e == cudaSuccess) e = cudaMemsetAsync(W.ctr, 0, sizeof(int) * ctr_ints(L), s);
   if (e == cudaSuccess && W.prof) e = cudaMemsetAsync(W.prof, 0, 2 * 8 * 1024 * sizeof(unsigned long long), s);
+  if (e == cudaSuccess && L.S) e = launch_extend_routing(topk_idx, topk_w, T, K, E, L.S, W.ext_idx, W.ext_w, s);
   if (e == cudaSuccess)
-    e = launch_dispatch(topk_idx, T, K, E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, W.dscr,
-                        static_cast<int64_t>(kDispatchMaxCtas) * E, s);
+    e = launch_dispatch(idx, T, L.K, L.E, L.BT, W.cnt, W.blk_off, W.slot, W.src, W.status, W.dscr,
+                        static_cast<int64_t>(kDispatchMaxCtas) * L.E, s);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess && !fused) e = launch_gather(L, W, static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, s);
   if (e == cudaSuccess) e = mark(2);
@@ -408,12 +427,14 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (o.variant == MM_MOE_VARIANT_MX) {
     GemmLaunch g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const uint8_t*>(w1_sfp),
                  static_cast<const uint8_t*>(w2), static_cast<const uint8_t*>(w2_sfp),
-                 static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, topk_w, W.dbg, W.prof, timeout_ns, grid,
-                 clamp, o.precise_swiglu != 0, early, topk_idx, out, pdl_gemm, (o.debug_flags & 8) != 0};
+                 static_cast<const uint8_t*>(x), x_sf, o.x_bf16 != 0, wts, W.dbg, W.prof, timeout_ns, grid,
+                 clamp, o.precise_swiglu != 0, early, idx, out, pdl_gemm,
+                 // a shared expert has T / 128 blocks: deal them one by one, not as one CTA's run
+                 (o.debug_flags & 8) != 0 || L.S > 0};
     auto gemm = plan.pair ? launch_gemm_mx_pair : (plan.swap ? launch_gemm_mx_sw : launch_gemm_mx);
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
-      const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(E);
+      const int lag = o.lag_units >= 0 ? o.lag_units : mx_lag_auto(L.E);
       if (e == cudaSuccess) e = gemm(g, 3, lag, (o.debug_flags & 4) ? 1 : 0, s);
       if (e == cudaSuccess) e = mark(3);
     } else {
@@ -423,8 +444,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       if (e == cudaSuccess) e = gemm(g, 2, 0, 0, s);
     }
   } else {
-    GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), topk_w, timeout_ns,
-                   grid, W.prof, clamp, o.precise_swiglu != 0};
+    GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), wts, timeout_ns,
+                   grid, W.prof, clamp, o.precise_swiglu != 0, (o.debug_flags & 16) != 0};
     if (e == cudaSuccess) e = launch_gemm_f8_l1(g, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {
@@ -435,7 +456,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   }
   if (e == cudaSuccess) e = mark(4);
   // the fused stream's early combine has written `out` already
-  if (e == cudaSuccess && !early) e = launch_combine(L, W, topk_idx, out, pdl_combine, s);
+  if (e == cudaSuccess && !early) e = launch_combine(L, W, idx, out, pdl_combine, s);
   if (e == cudaSuccess) e = mark(5);
   if (e != cudaSuccess) {
     if (getenv("MM_MOE_DEBUG")) fprintf(stderr, "mm_moe_forward: %s\n", cudaGetErrorString(e));
@@ -447,7 +468,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
 int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
                         int32_t* cnt, int32_t* blk_off, int32_t* slot, int32_t* src, int* block_m, void* stream) {
   const mm_moe_options o = resolve(opt);
-  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (int r = check_shape(T, H, I, E, K, o.shared_experts)) return r;
   if (!workspace) return MM_MOE_ERR_INVALID_ARG;
   Plan plan;
   if (int r = make_plan(o, T, K, E, &plan)) return r;
@@ -455,10 +476,10 @@ int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T,
   const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (cnt) e = cudaMemcpyAsync(cnt, W.cnt, sizeof(int) * E, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess && blk_off) e = cudaMemcpyAsync(blk_off, W.blk_off, sizeof(int) * (E + 1), cudaMemcpyDeviceToDevice, s);
+  if (cnt) e = cudaMemcpyAsync(cnt, W.cnt, sizeof(int) * L.E, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && blk_off) e = cudaMemcpyAsync(blk_off, W.blk_off, sizeof(int) * (L.E + 1), cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && slot && T > 0)
-    e = cudaMemcpyAsync(slot, W.slot, sizeof(int) * static_cast<size_t>(T) * K, cudaMemcpyDeviceToDevice, s);
+    e = cudaMemcpyAsync(slot, W.slot, sizeof(int) * static_cast<size_t>(T) * L.K, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && src && L.P > 0)
     e = cudaMemcpyAsync(src, W.src, sizeof(int) * static_cast<size_t>(L.P), cudaMemcpyDeviceToDevice, s);
   if (block_m) *block_m = L.BT;
@@ -468,7 +489,7 @@ int mm_moe_read_routing(const void* workspace, const mm_moe_options* opt, int T,
 int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
                              int64_t rows, uint8_t* codes, void* sf, void* stream) {
   const mm_moe_options o = resolve(opt);
-  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (int r = check_shape(T, H, I, E, K, o.shared_experts)) return r;
   if (!workspace || !codes || !sf || rows < 0) return MM_MOE_ERR_INVALID_ARG;
   Plan plan;
   if (int r = make_plan(o, T, K, E, &plan)) return r;
@@ -483,23 +504,23 @@ int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, i
 int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, int T, int H, int I, int E, int K,
                             int region, void** ptr, size_t* bytes) {
   const mm_moe_options o = resolve(opt);
-  if (int r = check_shape(T, H, I, E, K)) return r;
+  if (int r = check_shape(T, H, I, E, K, o.shared_experts)) return r;
   if (!ptr || !bytes) return MM_MOE_ERR_INVALID_ARG;
   Plan plan;
   if (int r = make_plan(o, T, K, E, &plan)) return r;
   const Layout L = layout_for(o, T, H, I, E, K, plan);
   const size_t offs[13] = {L.status, L.cnt, L.blk_off, L.slot, L.src, L.pool_x, L.pool_x_sf, L.pool2, L.pool2_sf,
-                           L.part, L.dbg, L.prof, L.total};
+                           L.part, L.dbg, L.prof, L.ext_idx};
   if (region < 0 || region > 11) return MM_MOE_ERR_INVALID_ARG;
   size_t n;
   if (region == 10) n = L.dbg_bytes;
   else if (region == 11) n = L.total - L.prof;
   else if (region == 0) n = 16;
-  else if (region == 1) n = sizeof(int) * E;
-  else if (region == 2) n = sizeof(int) * (E + 1);
-  else if (region == 3) n = sizeof(int) * static_cast<size_t>(T) * K;
+  else if (region == 1) n = sizeof(int) * L.E;
+  else if (region == 2) n = sizeof(int) * (L.E + 1);
+  else if (region == 3) n = sizeof(int) * static_cast<size_t>(T) * L.K;
   else if (region == 4) n = sizeof(int) * static_cast<size_t>(L.P);
-  else if (region == 9) n = static_cast<size_t>(L.part_elem) * T * K * H;
+  else if (region == 9) n = static_cast<size_t>(L.part_elem) * T * L.K * H;
   else n = offs[region + 1] - offs[region];
   *ptr = static_cast<uint8_t*>(const_cast<void*>(workspace)) + offs[region];
   *bytes = n;

@@ -1,12 +1,15 @@
 // Grouped GEMMs of the FP8 x FP8 variant on tcgen05 (kind::f8f6f4): e4m3
 // activations with one fp32 scale per 1x128, e4m3 weights with one fp32 scale
-// per 128x128 block, intermediate requantised per 128 with the raw scale
-// amax/448 (DeepGEMM PR #440, "Why the order and not the pool size";
-// MEGAMOE_SM90_DESIGN.md §10.1).
+// per 128x128 block, intermediate requantised per 128 or per 64 with the raw
+// scale amax/448 (DeepGEMM PR #440, "Why the order and not the pool size" and
+// "Ring sizing, recycling, and why that granularity"; MEGAMOE_SM90_DESIGN.md
+// §10.1).
 //
-// fp32 scales cannot ride the MMA, so each 128-K block is multiplied into a
-// fresh TMEM partial and the epilogue promotes it: acc += partial * sx[row,kb]
-// * sw[rows,kb] (the design doc's register-side scale application, §5.3).
+// fp32 scales cannot ride the MMA, so each promotion unit (a 128-K block, or a
+// 64-K half of one when L2 reads a per-64 intermediate: the design doc's
+// dual-half scaling, §5.4) is multiplied into a fresh TMEM partial and the
+// epilogue promotes it: acc += partial * sx[row,unit] * sw[rows,kb] (the
+// design doc's register-side scale application, §5.3).
 // Tile: 128 pool rows x 256 weight rows (L1: 128 gate + 128 up rows).
 //
 // One CTA per SM, 512 threads in four warpgroups:
@@ -15,11 +18,22 @@
 //                      one pool row and 128 fp32 running sums in registers
 //                      (L1: gate and up columns of the same 64 intermediate
 //                      columns, so SwiGLU stays thread-local)
-//   WG3 (warps 12..15) warp 12: TMEM allocator + single-thread MMA issuer
-// setmaxnreg moves registers from WG0/WG3 (56 each) to WG1/WG2 (200 each);
+//   WG3 (warps 12..15) warps 12 and 13: one MMA-issuing thread each, taking
+//                      alternate promotion units (warp 12 also allocates TMEM);
+//                      warp 14: waits for each unit's partial and passes it on
+//
+// While the tensor core streams its operands, every shared-memory access of
+// another warp (an mbarrier wait included) takes hundreds of cycles, so the
+// per-unit hand-offs between the issuers and the epilogue use named barriers,
+// which touch no shared memory: "unit complete" (barriers 1, 2: warp 14, which
+// waits on the unit's commit, arrives; the epilogue syncs) and "partial free"
+// (barriers 3, 4: the epilogue arrives after its TMEM loads; the issuer of the
+// buffer syncs).  The activation and weight scales of a unit reach registers
+// by plain loads two promotions ahead.
+// setmaxnreg moves registers from WG0/WG3 (40 each) to WG1/WG2 (216 each);
 // the host refuses to launch unless the kernel was built with exactly 128
 // registers per thread, the total the split assumes.
-// TMEM: two 256-column partial buffers, alternating by k-block, so the MMAs of
+// TMEM: two 256-column partial buffers, one per issuing thread, so the MMAs of
 // block kb+1 overlap the promotion of block kb.  Every wait is bounded.
 #include <cuda.h>
 
@@ -32,15 +46,18 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kThreads = 512;
 constexpr int kLaunchRegs = 128;       // 65536 / 512
-constexpr int kSmallRegs = 56;         // producers
-constexpr int kMmaRegs = 56;           // MMA warpgroup
-constexpr int kEpiRegs = 200;          // epilogue warpgroups
+constexpr int kSmallRegs = 40;         // producers
+constexpr int kMmaRegs = 40;           // MMA warpgroup
+constexpr int kEpiRegs = 216;          // epilogue warpgroups
 static_assert(128 * kSmallRegs + 128 * kMmaRegs + 2 * 128 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kBN = 256;
 constexpr int kTokBytes = kBT * kBK;
 constexpr int kWgtBytes = kBN * kBK;
 constexpr int kTmemCols = 512;
-constexpr int kMaxKB = kF8MaxKB;       // k-blocks of weight scales staged per task (H, I <= 8192)
+constexpr int kEpiThreads = 256;       // the two epilogue warpgroups
+constexpr int kBarDone0 = 1;           // named barriers 1, 2: the partial of a unit in buffer 0 / 1 is complete
+constexpr int kBarFree0 = 3;           // named barriers 3, 4: buffer 0 / 1 has been read by the epilogue
+constexpr int kBarThreads = kEpiThreads + 32;   // the epilogue and one warp of WG3
 
 enum : int {
   kSiteEmpty = 201, kSiteFull = 202, kSitePEmpty = 203, kSitePFull = 204, kSiteAmax = 205,
@@ -56,9 +73,12 @@ struct Args {
   const int* src;
   const float* topk_w;
   const float* sw;      // weight scales [E, rows/128, kdim/128]
-  const float* sx;      // token scales [P, kdim/128]
+  const float* sx;      // token scales [P, units per row]
   uint8_t* out_codes;   // L1: intermediate codes [P, I]
-  float* out_sf;        // L1: intermediate scales [P, I/128]
+  float* out_sf;        // L1: intermediate scales [P, I/gran]
+  int gran;             // L1: intermediate scale block along I, 128 or 64
+  int units;            // promotion units per 128-K stage: 1, or 2 when L2 reads per-64 scales
+  int exact_div;        // L1: every requant code from the IEEE quotient (no fast path)
   float* partials;      // L2: [K, T, H] fp32, or bf16 when pbf16
   int pbf16;
   float clamp;          // gate and up clamped to [-clamp, clamp] before the SwiGLU (+inf: none)
@@ -76,11 +96,10 @@ struct SmemLayout {
   static constexpr int tok = 0;
   static constexpr int wgt = tok + kStages * kTokBytes;
   static constexpr int amax = wgt + kStages * kWgtBytes;              // [2 tasks][2 halves][128] fp32
-  static constexpr int wsc = amax + 2 * 2 * 128 * 4;                   // [2 tasks][2 rows][kMaxKB] fp32
-  static constexpr int meta = wsc + 2 * 2 * kMaxKB * 4;
+  static constexpr int meta = amax + 2 * 2 * 128 * 4;
   static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
-  // full[S], empty[S], pfull[2], pempty[2], epi, wsc, drain
-  static constexpr int nbars = 2 * kStages + 7;
+  // full[S], empty[S] (one commit per promotion unit: stage free and partial complete), epi, drain
+  static constexpr int nbars = 2 * kStages + 2;
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -108,6 +127,28 @@ __device__ __forceinline__ uint32_t make_idesc() {
   return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | ((128u >> 4) << 24);
 }
 
+// The e4m3 codes RNE_e4m3(fp32(a0 / s)), RNE_e4m3(fp32(a1 / s)) with IEEE
+// quotients, r = 1/s correctly rounded.  q = a * r is within 2^-23 |a/s| of the
+// exact quotient, so the IEEE quotient lies within 4 fp32 ulps of q; e4m3
+// rounding is monotonic, so when q - 4 ulps and q + 4 ulps give the same code,
+// that is the code of the IEEE quotient.  Only otherwise (a quotient next to an
+// e4m3 rounding boundary) are the divisions done.  exact: always divide.
+__device__ __forceinline__ float ulps_toward(float q, int d) {   // |q| moved by d ulps, sign kept, not past 0
+  const uint32_t b = __float_as_uint(q);
+  const uint32_t m = b & 0x7fffffffu;
+  const uint32_t mm = d < 0 ? (m > static_cast<uint32_t>(-d) ? m + d : 0u) : m + d;
+  return __uint_as_float((b & 0x80000000u) | mm);
+}
+__device__ __forceinline__ uint32_t quot_e4m3x2(float a0, float a1, float s, float r, bool exact) {
+  if (!exact) {
+    const float q0 = a0 * r, q1 = a1 * r;
+    const uint16_t lo = cvt_e4m3x2(ulps_toward(q0, -4), ulps_toward(q1, -4));
+    const uint16_t hi = cvt_e4m3x2(ulps_toward(q0, 4), ulps_toward(q1, 4));
+    if (lo == hi) return lo;
+  }
+  return cvt_e4m3x2(__fdiv_rn(a0, s), __fdiv_rn(a1, s));
+}
+
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSmallRegs)); }
 __device__ __forceinline__ void regs_dec_mma() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kMmaRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
@@ -127,15 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_blk = reinterpret_cast<int*>(smem + SmemLayout::meta);
   int* s_cnt = s_blk + E + 1;
   float* s_amax = reinterpret_cast<float*>(smem + SmemLayout::amax);
-  float* s_wsc = reinterpret_cast<float*>(smem + SmemLayout::wsc);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars_after_meta(E));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* pfull = bars + 2 * kStages;
-  uint64_t* pempty = pfull + 2;
-  uint64_t* epibar = pempty + 2;
-  uint64_t* wscbar = epibar + 1;
-  uint64_t* drain = wscbar + 1;   // the MMA issuer's last commit
+  uint64_t* epibar = bars + 2 * kStages;
+  uint64_t* drain = epibar + 1;   // the MMA issuers' last commits
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -143,19 +180,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int wg = warp >> 2;
   const Status st{args.status, args.timeout_ns};
+  const int U = args.units;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], 8);
+      mbar_init(&empty[i], U);                  // one commit per promotion unit of the stage
     }
     mbar_init(epibar, 256);
-    mbar_init(wscbar, 256);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -214,43 +247,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (wg == 3) {
     regs_dec_mma();
-    // ------------------------------------------------------------------ MMA issuer
-    if (warp == 12 && lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int g = 0;                                 // global k-block counter: partial buffer g & 1
+    // ------------------------------------------------------------------ MMA issuers
+    // Two warps issue alternate promotion units, each into its own partial
+    // buffer (unit g: buffer and warp g & 1, stage (g / U) % kStages), lane 0
+    // issuing.  Every unit is a fresh accumulation of 4 / U MMAs, so the order in
+    // which the two streams reach the tensor core changes no result.  A unit
+    // waits for its stage's data first (that usually landed while the epilogue
+    // was still promoting), then for its buffer: the epilogue's release of unit
+    // g - 2.  One commit per unit on its stage's empty barrier frees the stage
+    // (after all U units) and completes the partial.
+    if (warp == 12 || warp == 13) {
+      const int me = warp - 12;
+      const int per = 4 / U;                     // MMAs (K = 32 each) per unit
+      int g = 0;                                 // global unit counter
+      bool ok = true;
       const long long c_start = kProf ? clock64() : 0;
       long long c_pe = 0, c_full = 0;
-      for (int tile = blockIdx.x; tile < total && !*s_abort; tile += gridDim.x) {
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb, ++g) {
-          const int pb = g & 1;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int j = 0; j < KB * U; ++j, ++g) {
+          if ((g & 1) != me) continue;
+          const int sg = g / U;                  // the stage's global index
+          const int stage = sg % kStages;
           const long long tm0 = kProf ? clock64() : 0;
-          if (!mbar_wait(&pempty[pb], ((g >> 1) & 1) ^ 1, st, s_abort, kSitePEmpty)) { ok = false; break; }
+          if (lane == 0) ok = mbar_wait(&full[stage], (sg / kStages) & 1, st, s_abort, kSiteFull);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
           const long long tm1 = kProf ? clock64() : 0;
-          if (!mbar_wait(&full[stage], phase, st, s_abort, kSiteFull)) { ok = false; break; }
-          if (kProf) { c_pe += tm1 - tm0; c_full += clock64() - tm1; }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + SmemLayout::tok + stage * kTokBytes);
-          const uint32_t b0 = smem_u32(smem + SmemLayout::wgt + stage * kWgtBytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_f8f6f4(tmem + pb * kBN, make_smem_desc(a0 + kk * 32, 16, 1024, 2),
-                          make_smem_desc(b0 + kk * 32, 16, 1024, 2), make_idesc(), kk != 0);
-          tc_commit(&empty[stage]);
-          tc_commit(&pfull[pb]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (g >= 2) named_sync(kBarFree0 + me, kBarThreads);
+          if (__any_sync(0xffffffffu, *s_abort != 0)) { ok = false; break; }
+          if (kProf) { c_full += tm1 - tm0; c_pe += clock64() - tm1; }
+          if (lane == 0) {
+            tc_fence_after();
+            const int k0 = (g - sg * U) * per;   // first 32-K slice of this unit
+            const uint32_t a0 = smem_u32(smem + SmemLayout::tok + stage * kTokBytes);
+            const uint32_t b0 = smem_u32(smem + SmemLayout::wgt + stage * kWgtBytes);
+            for (int kk = 0; kk < per; ++kk)
+              tc_mma_f8f6f4(tmem + me * kBN, make_smem_desc(a0 + (k0 + kk) * 32, 16, 1024, 2),
+                            make_smem_desc(b0 + (k0 + kk) * 32, 16, 1024, 2), make_idesc(), kk != 0);
+            tc_commit(&empty[stage]);
+          }
+          __syncwarp();
         }
-        if (!ok) break;
       }
-      // every MMA this thread issued has completed before TMEM is freed
-      tc_commit(drain);
-      mbar_wait_drain(drain, 0, st, kSiteDrainMma);
-      if (kProf) {
-        args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
-        args.prof[blockIdx.x * 8 + 1] = c_pe;
-        args.prof[blockIdx.x * 8 + 2] = c_full;
-        args.prof[blockIdx.x * 8 + 6] = g;
+      if (lane == 0) {
+        // every MMA these threads issued has completed before TMEM is freed
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0, st, kSiteDrainMma);
+        if (kProf && me == 0) {
+          args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
+          args.prof[blockIdx.x * 8 + 1] = c_pe;
+          args.prof[blockIdx.x * 8 + 2] = c_full;
+          args.prof[blockIdx.x * 8 + 6] = g;
+        }
+      }
+    } else if (warp == 14) {
+      // Unit g's commit, passed on to the epilogue through barrier kBarDone0 + (g & 1).
+      // This warp is at most one unit ahead on each barrier (the partial of unit g + 2
+      // needs the epilogue's release of unit g first).  It arrives once for every unit
+      // of every task even after a failed wait, so no epilogue warp is ever left at a
+      // barrier; the epilogue checks the abort flag after each one.
+      bool ok = true;
+      int g = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        for (int j = 0; j < KB * U; ++j, ++g) {
+          const int sg = g / U;
+          if (lane == 0 && ok) ok = mbar_wait(&empty[sg % kStages], (sg / kStages) & 1, st, s_abort, kSitePFull);
+          __syncwarp();
+          named_arrive(kBarDone0 + (g & 1), kBarThreads);
+        }
       }
     }
     __syncwarp();
@@ -267,10 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c1 = PHASE == 1 ? 128 + 64 * half : 128 * half + 64;
     int g = 0;
     uint32_t ephase = 0;
-    uint32_t wphase = 0;
     const long long e_start = kProf ? clock64() : 0;
     long long e_wait = 0, e_promo = 0, e_tail = 0, e_setup = 0, e_math = 0, e_rdv = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const long long ts0 = kProf ? clock64() : 0;
       int e, n, b, valid;
       decode_tile(tile, args.nblocks, s_blk, s_cnt, E, e, n, b, valid);
       const bool live = m < valid;
@@ -278,48 +342,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = live ? __ldg(args.src + row) : 0;
       const float w = (PHASE == 1 && live) ? __ldg(args.topk_w + s) : 0.f;
       const int wrows = PHASE == 1 ? 2 * args.I / 128 : args.H / 128;   // weight scale block rows
-      // the task's weight scales (two block rows x KB) go to shared memory once: the
-      // epilogue threads load them together and meet at a bounded rendezvous; the
-      // buffer alternates between tasks, so a slow reader of the last task is never
-      // overwritten (its next writer passed this task's rendezvous first)
-      const long long ts0 = kProf ? clock64() : 0;
-      const int et = (warp - 4) * 32 + lane;
-      float* wsc = s_wsc + (wphase & 1) * 2 * kMaxKB;
-      {
-        const int ra = PHASE == 1 ? n : (2 * n < wrows ? 2 * n : wrows - 1);
-        const int rb = PHASE == 1 ? (args.I >> 7) + n : (2 * n + 1 < wrows ? 2 * n + 1 : wrows - 1);
-        for (int i = et; i < 2 * KB; i += 256) {
-          const int r = i / KB;
-          wsc[r * kMaxKB + (i - r * KB)] =
-              __ldg(args.sw + (static_cast<size_t>(e) * wrows + (r ? rb : ra)) * KB + (i - r * KB));
-        }
-      }
-      mbar_arrive(wscbar);
-      if (!mbar_wait(wscbar, wphase & 1, st, s_abort, kSiteAmax)) break;
-      ++wphase;
-      // L1: gate scales row 0, up scales row 1; L2: this half's 128 columns use row `half`
-      const float* w0s = wsc + (PHASE == 1 ? 0 : half) * kMaxKB;
-      const float* w1s = wsc + (PHASE == 1 ? 1 : half) * kMaxKB;
-      const float* sxr = args.sx + row * KB;
+      // weight scale rows: L1 gate (row n) and up (row I/128 + n) for both halves;
+      // L2 this half's 128 columns (row 2n + half, the last row past H)
+      const int ra = PHASE == 1 ? n : (2 * n + half < wrows ? 2 * n + half : wrows - 1);
+      const int rb = PHASE == 1 ? (args.I >> 7) + n : ra;
+      const float* w0g = args.sw + (static_cast<size_t>(e) * wrows + ra) * KB;
+      const float* w1g = args.sw + (static_cast<size_t>(e) * wrows + rb) * KB;
+      const int NU = KB * U;                     // promotion units of the task
+      const float* sxr = args.sx + row * NU;
       float acc0[64], acc1[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
       bool ok = true;
-      // the row's activation scale of k-block kb + 2 is loaded right after kb's is
-      // used; L1 runs two k-blocks a turn with one scale register each, so a load
-      // has two promotions to land and no register move waits on it
-      float sx0 = live ? __ldg(sxr) : 0.f;
-      float sx1 = (live && KB > 1) ? __ldg(sxr + 1) : 0.f;
       if (kProf) e_setup += clock64() - ts0;
-      auto promote = [&](int kb, float sx) -> bool {
-        const float f0 = sx * w0s[kb];
-        const float f1 = sx * w1s[kb];
+      auto promote = [&](float sx, float w0, float w1) -> bool {
         const int pb = g & 1;
         const long long tw0 = kProf ? clock64() : 0;
-        if (!mbar_wait(&pfull[pb], (g >> 1) & 1, st, s_abort, kSitePFull)) return false;
+        named_sync(kBarDone0 + pb, kBarThreads);   // warp 14 saw the unit's commit
+        if (__any_sync(0xffffffffu, *s_abort != 0)) return false;   // warp-uniform: the barriers are per warp
         const long long tw1 = kProf ? clock64() : 0;
         tc_fence_after();
-        // one 32-column slice at a time keeps at most 128 sums + 32 loaded values live
+        const float f0 = sx * w0;
+        const float f1 = sx * w1;
+        // one 32-column slice at a time keeps at most 128 sums + 32 loaded values
+        // live; the buffer is released once its last slice has landed
         const uint32_t tb = tlane + pb * kBN;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tb + c0, v);
@@ -336,29 +382,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j) acc1[j] = fmaf(__uint_as_float(v[j]), f1, acc1[j]);
         tmem_ld_32x32b_x32(tb + c1 + 32, v);
         tmem_ld_wait();
+        tc_fence_before();
+        named_arrive(kBarFree0 + pb, kBarThreads);   // the buffer may take unit g + 2
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc1[32 + j] = fmaf(__uint_as_float(v[j]), f1, acc1[32 + j]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[pb]);
         if (kProf) { e_wait += tw1 - tw0; e_promo += clock64() - tw1; }
         ++g;
         return true;
       };
-      if constexpr (PHASE == 1) {
-        for (int kb = 0; kb < KB; kb += 2) {
-          if (!promote(kb, sx0)) { ok = false; break; }
-          if (kb + 2 < KB) sx0 = live ? __ldg(sxr + kb + 2) : 0.f;
-          if (kb + 1 < KB) {
-            if (!promote(kb + 1, sx1)) { ok = false; break; }
-            if (kb + 3 < KB) sx1 = live ? __ldg(sxr + kb + 3) : 0.f;
+      // Scale operands (row scale, gate / up or column-block weight scale) reach
+      // registers a group of four units ahead of their promotions.  Every load
+      // instruction of these warps waits behind the TMEM traffic, so when the
+      // task's units come in fours (the rows then 16-byte aligned) one vector load
+      // per operand serves the group; otherwise four scalar loads do.
+      const bool vec = (NU & 3) == 0;
+      auto load4 = [&](int q, float4& s4, float4& a4, float4& b4) {
+        if (vec) {
+          s4 = live ? __ldg(reinterpret_cast<const float4*>(sxr) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (U == 1) {
+            a4 = __ldg(reinterpret_cast<const float4*>(w0g) + q);
+            b4 = __ldg(reinterpret_cast<const float4*>(w1g) + q);
+          } else {                               // units 4q .. 4q+3 take weight k-blocks 2q, 2q, 2q+1, 2q+1
+            const float2 a2 = __ldg(reinterpret_cast<const float2*>(w0g) + q);
+            const float2 b2 = __ldg(reinterpret_cast<const float2*>(w1g) + q);
+            a4 = make_float4(a2.x, a2.x, a2.y, a2.y);
+            b4 = make_float4(b2.x, b2.x, b2.y, b2.y);
           }
+        } else {
+          float sv[4], av[4], bv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int u = 4 * q + i < NU ? 4 * q + i : NU - 1;
+            sv[i] = live ? __ldg(sxr + u) : 0.f;
+            av[i] = __ldg(w0g + u / U);
+            bv[i] = __ldg(w1g + u / U);
+          }
+          s4 = make_float4(sv[0], sv[1], sv[2], sv[3]);
+          a4 = make_float4(av[0], av[1], av[2], av[3]);
+          b4 = make_float4(bv[0], bv[1], bv[2], bv[3]);
         }
-      } else {   // one k-block a turn: the two-a-turn body spills here (measured slower)
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!promote(kb, sx0)) { ok = false; break; }
-          sx0 = sx1;
-          if (kb + 2 < KB) sx1 = live ? __ldg(sxr + kb + 2) : 0.f;
+      };
+      float4 s4, a4, b4;
+      float4 ns4 = make_float4(0.f, 0.f, 0.f, 0.f), na4 = ns4, nb4 = ns4;
+      load4(0, s4, a4, b4);
+      for (int u = 0; u < NU; ++u) {
+        const int i = u & 3;
+        if (i == 0 && u + 4 < NU) load4((u >> 2) + 1, ns4, na4, nb4);
+        const float sx = i == 0 ? s4.x : (i == 1 ? s4.y : (i == 2 ? s4.z : s4.w));
+        const float w0 = i == 0 ? a4.x : (i == 1 ? a4.y : (i == 2 ? a4.z : a4.w));
+        const float w1 = i == 0 ? b4.x : (i == 1 ? b4.y : (i == 2 ? b4.z : b4.w));
+        if (!promote(sx, w0, w1)) { ok = false; break; }
+        if (i == 3) {                            // the next group, loaded four promotions ago
+          s4 = ns4;
+          a4 = na4;
+          b4 = nb4;
         }
       }
       if (!ok) break;
@@ -387,33 +464,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             amax = fmaxf(amax, fabsf(acc0[j]));
           }
         }
-        // the 128-column requant block spans both halves: exchange row amax
-        // one rendezvous per task: the exchange buffer alternates between tasks, and a
-        // thread writes it again two tasks later only after everyone passed the next rendezvous
         const long long tr0 = kProf ? clock64() : 0;
-        float* xa = s_amax + (ephase & 1) * 256;
-        xa[half * 128 + m] = amax;
-        mbar_arrive(epibar);
-        if (!mbar_wait(epibar, ephase, st, s_abort, kSiteAmax)) break;
-        ephase ^= 1;
+        if (args.gran == 128) {
+          // the 128-column requant block spans both halves: exchange row amax
+          // one rendezvous per task: the exchange buffer alternates between tasks, and a
+          // thread writes it again two tasks later only after everyone passed the next rendezvous
+          float* xa = s_amax + (ephase & 1) * 256;
+          xa[half * 128 + m] = amax;
+          mbar_arrive(epibar);
+          if (!__all_sync(0xffffffffu, mbar_wait(epibar, ephase, st, s_abort, kSiteAmax))) break;
+          ephase ^= 1;
+          amax = fmaxf(amax, xa[(half ^ 1) * 128 + m]);
+        }   // per 64: this thread's 64 columns are the block
         if (kProf) { e_math += tr0 - tw2; e_rdv += clock64() - tr0; }
-        amax = fmaxf(amax, xa[(half ^ 1) * 128 + m]);
         if (live) {
           // s = amax / 448 and each code RNE_e4m3(a / s), both quotients IEEE-rounded
           // (DeepGEMM PR #440: the scale is the raw amax / 448 and the value is divided by it)
           const float sf = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+          const float rsf = __frcp_rn(sf);
+          const bool exact = args.exact_div != 0;
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const uint32_t lo = cvt_e4m3x2(__fdiv_rn(acc0[4 * i], sf), __fdiv_rn(acc0[4 * i + 1], sf));
-            const uint32_t hi = cvt_e4m3x2(__fdiv_rn(acc0[4 * i + 2], sf), __fdiv_rn(acc0[4 * i + 3], sf));
+            const uint32_t lo = quot_e4m3x2(acc0[4 * i], acc0[4 * i + 1], sf, rsf, exact);
+            const uint32_t hi = quot_e4m3x2(acc0[4 * i + 2], acc0[4 * i + 3], sf, rsf, exact);
             packed[i] = lo | (hi << 16);
           }
           uint4* dst = reinterpret_cast<uint4*>(args.out_codes + row * args.I + n * 128 + 64 * half);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-          if (half == 0) args.out_sf[row * (args.I / 128) + n] = sf;
+          if (args.gran == 64) args.out_sf[row * (args.I / 64) + 2 * n + half] = sf;
+          else if (half == 0) args.out_sf[row * (args.I / 128) + n] = sf;
         }
       } else {
         if (live && n * kBN + 128 * half < args.H) {
@@ -439,6 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kProf) e_tail += clock64() - tw2;
     }
+    // after an abort an issuer may wait for the release of a buffer this warpgroup will
+    // never read: one more arrival on each "partial free" barrier lets it see the flag
+    // (an arrival nobody waits for is harmless)
+    __syncwarp();
+    named_arrive(kBarFree0, kBarThreads);
+    named_arrive(kBarFree0 + 1, kBarThreads);
     if (kProf && warp == 4 && lane == 0) {
       args.prof[blockIdx.x * 8 + 3] = e_wait;
       args.prof[blockIdx.x * 8 + 4] = e_promo;
@@ -478,11 +566,14 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   a.sw = g.wsf;
   a.clamp = g.clamp;   // both phases: L1 applies it, L2 ignores it
   a.precise = g.precise;
+  a.gran = L.act_gran;
+  a.exact_div = g.exact_div ? 1 : 0;
   const uint8_t* pool;
   int kdim;
   if (PHASE == 1) {
     a.kblocks = L.H / 128;
     a.nblocks = L.I / 128;
+    a.units = 1;
     a.sx = reinterpret_cast<const float*>(W.pool_x_sf);
     a.out_codes = W.pool2;
     a.out_sf = reinterpret_cast<float*>(W.pool2_sf);
@@ -497,6 +588,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   } else {
     a.kblocks = L.I / 128;
     a.nblocks = (L.H + kBN - 1) / kBN;
+    a.units = L.act_gran == 64 ? 2 : 1;
     a.sx = reinterpret_cast<const float*>(W.pool2_sf);
     a.partials = W.part;
     a.pbf16 = L.part_elem == 2;

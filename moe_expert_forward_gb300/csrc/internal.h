@@ -25,11 +25,19 @@ struct Layout {
   int64_t nblk_cap;          // P / BT
   int KB1, KB2;              // H/128, I/128
   int part_elem;             // bytes of one partial: 4 (fp32) or 2 (bf16)
+  int act_gran;              // F8: intermediate scale block along I (128 or 64); MX: 32
+  int S;                     // shared experts (the last S of E and of K; 0 = none)
+  size_t ext_idx, ext_w;     // shared experts: the routing extended by S slots, int32 / fp32 [T, K]
   size_t status, cnt, blk_off, dscr, ctr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
 };
 
+// E and K count the shared experts: E = routed + S, K = routed slots + S.
 Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0, int partials_bf16 = 0,
-                   int BT = kBT);
+                   int BT = kBT, int act_gran = 128, int S = 0);
+// The F8 intermediate's scale width by the shape rule of DeepGEMM PR #440 ("Ring
+// sizing, recycling, and why that granularity"): 128 when H % 512 == 0 and
+// 2I % 512 == 0, else 64.
+inline int f8_gran_rule(int H, int I) { return (H % 512 == 0 && (2 * I) % 512 == 0) ? 128 : 64; }
 
 // Byte offset, in a pool scale region laid out [block][kb][CPB chunks][512], of
 // the 4-byte word of row r of block b (r < BT) and 128-wide contraction block
@@ -62,6 +70,8 @@ struct WsPtrs {
   float* part;
   float* dbg;
   unsigned long long* prof;
+  int32_t* ext_idx;          // shared experts: extended routing (null without)
+  float* ext_w;
 };
 WsPtrs ws_ptrs(void* ws, const Layout& L);
 
@@ -85,7 +95,6 @@ cudaError_t max_pair_clusters(const void* fn, int threads, int smem_bytes, int* 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int block_m, int32_t* cnt,
                             int32_t* blk_off, int32_t* slot, int32_t* src, int32_t* status, int32_t* scratch,
                             int64_t scratch_ints, cudaStream_t s);
-constexpr int kF8MaxKB = 64;             // F8 variant: H and I at most 64 x 128
 constexpr int kDispatchMaxCtas = 256;   // the dispatch scratch holds per-CTA counts [CTAs][E]
 // x_bf16: x is bf16 [T, H] and each row is quantised on its way into the pool
 cudaError_t launch_gather(const Layout& L, const WsPtrs& W, const uint8_t* x, const void* x_sf, bool x_bf16,
@@ -95,6 +104,11 @@ cudaError_t launch_combine(const Layout& L, const WsPtrs& W, const int32_t* topk
                            cudaStream_t s);
 cudaError_t launch_prepare_sf_mx(const uint8_t* w1_sf, const uint8_t* w2_sf, int H, int I, int E,
                                  uint8_t* w1_sfp, uint8_t* w2_sfp, cudaStream_t s);
+// topk_idx [T, K] / topk_w -> [T, K + S]: routed slots copied (ids in [E, E+S)
+// turned into -2, out of range for the routing kernels), then S slots naming
+// experts E .. E+S-1 with weight 1.
+cudaError_t launch_extend_routing(const int32_t* topk_idx, const float* topk_w, int T, int K, int E, int S,
+                                  int32_t* ext_idx, float* ext_w, cudaStream_t s);
 cudaError_t launch_read_intermediate(const Layout& L, const WsPtrs& W, int64_t rows, uint8_t* codes,
                                      void* sf, cudaStream_t s);
 
@@ -144,6 +158,7 @@ struct GemmLaunchF8 {
   unsigned long long* prof;  // per-CTA role cycles (debug_flags bit 1) or null
   float clamp;               // activation clamp of gate and up (+inf: none)
   int precise;               // SwiGLU with expf and the IEEE division instead of the fast-math form
+  bool exact_div;            // L1 requant: divide for every code (debug_flags bit 4), not only near a boundary
 };
 cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s);
 cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s);

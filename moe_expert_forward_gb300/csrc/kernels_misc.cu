@@ -219,8 +219,9 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int T, int K, int E, int bl
 // each of its pool rows slot[t*K + k] (masked slots are skipped; padding rows
 // are never written, the GEMM epilogues ignore them).  MX scales go to the
 // 512-byte chunk layout the MMA consumes; F8 scales to a plain [P, H/128] fp32
-// array.  Every lane holds the token's K pool rows; the shuffles that spread
-// them run with the warp converged.
+// array (a GEMM epilogue thread reads four k-blocks of its row with one load).
+// Every lane holds the token's K pool rows; the shuffles that spread them run
+// with the warp converged.
 __device__ __forceinline__ void token_rows(const int32_t* __restrict__ slot, int64_t t, int K, int lane,
                                            int (&rows)[kMaxK]) {
   const int myrow = lane < K ? __ldg(slot + t * K + lane) : -1;
@@ -422,6 +423,39 @@ cudaError_t launch_prepare_sf_mx(const uint8_t* w1_sf, const uint8_t* w2_sf, int
 }
 
 // ----------------------------------------------------------------------------- intermediate read-back
+// Shared experts: every token's routing grows by S slots naming experts
+// E .. E+S-1 with weight 1, after its K routed slots.  A routed id in [E, E+S)
+// would otherwise name a shared expert, so it becomes -2, which the routing
+// kernels mask and flag like any other id out of range.
+__global__ void extend_routing_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w, int T, int K,
+                                      int E, int S, int32_t* __restrict__ xidx, float* __restrict__ xw) {
+  const int KS = K + S;
+  const int64_t n = static_cast<int64_t>(T) * KS;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / KS;
+    const int j = static_cast<int>(i - t * KS);
+    if (j < K) {
+      const int e = idx[t * K + j];
+      xidx[i] = (e >= E && e < E + S) ? -2 : e;
+      xw[i] = w[t * K + j];
+    } else {
+      xidx[i] = E + (j - K);
+      xw[i] = 1.0f;
+    }
+  }
+}
+
+cudaError_t launch_extend_routing(const int32_t* topk_idx, const float* topk_w, int T, int K, int E, int S,
+                                  int32_t* ext_idx, float* ext_w, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(T) * (K + S);
+  int blocks = static_cast<int>((n + 255) / 256);
+  if (blocks > dev_info().sms * 8) blocks = dev_info().sms * 8;
+  if (blocks < 1) blocks = 1;
+  extend_routing_kernel<<<blocks, 256, 0, s>>>(topk_idx, topk_w, T, K, E, S, ext_idx, ext_w);
+  return cudaGetLastError();
+}
+
 __global__ void read_sf_mx_kernel(const uint8_t* __restrict__ pool2_sf, int64_t rows, int I, int BT, int CPB,
                                   uint8_t* __restrict__ sf) {
   const int KB32 = I / 32;
@@ -445,7 +479,7 @@ cudaError_t launch_read_intermediate(const Layout& L, const WsPtrs& W, int64_t r
                                                          static_cast<uint8_t*>(sf));
     return cudaGetLastError();
   }
-  return cudaMemcpyAsync(sf, W.pool2_sf, static_cast<size_t>(rows) * (L.I / 128) * sizeof(float),
+  return cudaMemcpyAsync(sf, W.pool2_sf, static_cast<size_t>(rows) * (L.I / L.act_gran) * sizeof(float),
                          cudaMemcpyDeviceToDevice, s);
 }
 

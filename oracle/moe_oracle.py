@@ -16,11 +16,19 @@ combine), with every expert local:
   4. a_j        = silu(g_j) * u_j * w[t,k]               (scaled SwiGLU, the
                   router weight folded in: "07 · MegaMoE" §8; design doc §10.1)
   5. requantise a to e4m3 per block along I (UE8M0 per 32 for the MX format,
-     "07 · MegaMoE" §8; raw fp32 amax/448 per 128 for the FP8 format, DeepGEMM
-     PR #440 "Why the order and not the pool size" on the raw scale)
+     "07 · MegaMoE" §8; raw fp32 amax/448 per 128 or per 64 for the FP8
+     format, DeepGEMM PR #440 "Why the order and not the pool size" on the raw
+     scale and "Ring sizing, recycling, and why that granularity" on the width)
   6. y_k[h]     = W2_hat[h] . a_hat                      (fp64)
   7. out[t,h]   = bf16_rne(sum_k y_k[h])                 (the combine is a plain
                   sum because the weight was applied in step 4: "07 · MegaMoE" §9)
+
+Shared experts (optional, `shared` > 0): experts E .. E+shared-1, which every
+token uses with weight 1 after its K routed slots; their outputs are slots
+K .. K+shared-1 of the same fixed-order sum.  The pages leave shared experts
+out of the fused kernel (PR #440 "What a per-rank token count changes": no
+shared-expert fusion, as in #383); this is the plain reading of a shared expert
+as a routed expert every token selects with weight 1.
 
 Where floating point decides an integer (the requantised codes and their
 scale), the decision is taken in fp32, the precision the pages' epilogues run in
@@ -159,6 +167,13 @@ def requant_f8(a32: np.ndarray, block: int = 128) -> Tuple[np.ndarray, np.ndarra
     return codes.reshape(n), s, deq.reshape(n)
 
 
+def f8_act_gran(H: int, I: int) -> int:
+    """Width of the FP8 intermediate's scale blocks along I by the pages' shape rule
+    (DeepGEMM PR #440, "Ring sizing, recycling, and why that granularity"): 128
+    when H % 512 == 0 and 2 * I % 512 == 0, else 64."""
+    return 128 if H % 512 == 0 and (2 * I) % 512 == 0 else 64
+
+
 def quantise_x(x: np.ndarray, variant: str) -> Tuple[np.ndarray, np.ndarray]:
     """bf16 activations (given as their exact fp32 / fp64 values) [T, H] -> the
     layer's FP8 input: (e4m3 codes u8 [T, H], scales).  The pages feed the
@@ -248,12 +263,15 @@ def expert_from_arrays(w1, w1_sf, w2, w2_sf) -> ExpertFn:
 
 
 def forward_pair(x_hat: np.ndarray, w: float, W1: np.ndarray, W2: np.ndarray, I: int,
-                 variant: str, clamp: Optional[float] = None):
+                 variant: str, clamp: Optional[float] = None, f8_gran: int = 128):
     """Steps 3-6 for one (token, expert) pair.  Returns (y fp64 [H], codes, sf, a fp64).
 
     clamp: the optional activation clamp of "MEGAMOE_SM90_DESIGN.md" §10 (L1
     epilogue: SwiGLU + FP8 quantization): gate and up are each limited to
-    [-clamp, clamp] before the SwiGLU."""
+    [-clamp, clamp] before the SwiGLU.
+    f8_gran: the FP8 format's requant block along I, 128 or 64 (PR #440's
+    l2_act_sf_gran_k); with 64 the L2 contraction dequantises each 64-wide half
+    of a 128-K step with its own scale ("MEGAMOE_SM90_DESIGN.md" §5.4)."""
     g = W1[:I] @ x_hat
     u = W1[I:] @ x_hat
     if clamp is not None:
@@ -265,14 +283,15 @@ def forward_pair(x_hat: np.ndarray, w: float, W1: np.ndarray, W2: np.ndarray, I:
     if variant == "mx":
         codes, sf, a_hat = requant_mx(a32, 32)
     else:
-        codes, sf, a_hat = requant_f8(a32, 128)
+        codes, sf, a_hat = requant_f8(a32, f8_gran)
     y = W2 @ a_hat
     return y, codes, sf, a
 
 
 def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.ndarray,
             topk_w: np.ndarray, experts: ExpertFn, H: int, I: int, E: int, variant: str,
-            keep_intermediate: bool = False, partials_bf16: bool = False, clamp: Optional[float] = None):
+            keep_intermediate: bool = False, partials_bf16: bool = False, clamp: Optional[float] = None,
+            f8_gran: int = 128, shared: int = 0):
     """Output rows out[t, :] (bf16 values as fp64) for the tokens in `rows`.
 
     Each (token, slot) pair is computed independently (forward_pair); the pairs
@@ -283,15 +302,22 @@ def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.n
     partials_bf16: the combine of the pages' own design ("MEGAMOE_SM90_DESIGN.md"
     §11, L2 BF16 epilogue + combine): every per-slot output y_k is cast to bf16
     (round to nearest even) before the top-k sum, which then runs in fixed k order
-    and is cast to bf16 once more.  Read here as bf16_rne of the fp64 y_k."""
+    and is cast to bf16 once more.  Read here as bf16_rne of the fp64 y_k.
+
+    f8_gran: the FP8 intermediate's scale width, 128 or 64 (f8_act_gran gives the pages' shape rule).
+    shared: shared experts E .. E+shared-1 (`experts` serves them too), used by
+    every token with weight 1 as slots K .. K+shared-1."""
     rows = [int(t) for t in rows]
     K = topk_idx.shape[1]
+    gran = int(f8_gran)
     pairs: Dict[int, list] = {}
     for t in rows:
         for k in range(K):
             e = int(topk_idx[t, k])
             if 0 <= e < E:
-                pairs.setdefault(e, []).append((t, k))
+                pairs.setdefault(e, []).append((t, k, float(topk_w[t, k])))
+        for j in range(shared):
+            pairs.setdefault(E + j, []).append((t, K + j, 1.0))
     x_hat = {t: dequant_x(x[t], x_sf[t], variant) for t in rows}
     y = {}
     inter = {}
@@ -299,15 +325,15 @@ def forward(rows: Iterable[int], x: np.ndarray, x_sf: np.ndarray, topk_idx: np.n
         w1, w1_sf, w2, w2_sf = experts(e)
         W1 = dequant_weight(w1, w1_sf, variant)
         W2 = dequant_weight(w2, w2_sf, variant)
-        for (t, k) in pairs[e]:
-            yk, codes, sf, _ = forward_pair(x_hat[t], topk_w[t, k], W1, W2, I, variant, clamp)
+        for (t, k, w) in pairs[e]:
+            yk, codes, sf, _ = forward_pair(x_hat[t], w, W1, W2, I, variant, clamp, gran)
             y[(t, k)] = yk
             if keep_intermediate:
                 inter[(t, k)] = (codes, sf)
     out = np.zeros((len(rows), H), dtype=np.float64)
     for i, t in enumerate(rows):
         acc = np.zeros(H, dtype=np.float64)
-        for k in range(K):                           # fixed k order
+        for k in range(K + shared):                  # fixed slot order, shared experts last
             if (t, k) in y:
                 acc = acc + (bf16_rne(y[(t, k)]) if partials_bf16 else y[(t, k)])
         out[i] = bf16_rne(acc)

@@ -39,10 +39,11 @@ def to_dev(inp: dict, device="cuda") -> dict:
 
 
 def run_forward(M, cfg, dev_inp: dict, opt=None, ws=None, out=None, prepared=None):
-    """One forward through the C ABI.  Returns (out, ws, prepared, status)."""
+    """One forward through the C ABI (with cfg.S shared experts).  Returns (out, ws, prepared, status)."""
     opt = opt or M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8)
+    opt.shared_experts = cfg.S
     if prepared is None:
-        prepared = M.prepare_weights(dev_inp["w1_sf"], dev_inp["w2_sf"], cfg.H, cfg.I, cfg.E, opt)
+        prepared = M.prepare_weights(dev_inp["w1_sf"], dev_inp["w2_sf"], cfg.H, cfg.I, cfg.E + cfg.S, opt)
     if ws is None:
         ws = M.alloc_workspace(cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, opt)
     if out is None:
@@ -64,13 +65,21 @@ def host_experts(dev_inp: dict):
     return get
 
 
-def oracle_rows(cfg, dev_inp: dict, rows, keep_intermediate=True, partials_bf16=False, clamp=None):
+def f8_gran(cfg, opt=None) -> int:
+    """The FP8 intermediate's scale width a call uses: 128 by default, the oracle's
+    shape rule for -1, else the pinned width."""
+    g = int(opt.f8_act_gran) if opt is not None else 0
+    return O.f8_act_gran(cfg.H, cfg.I) if g == -1 else (g or 128)
+
+
+def oracle_rows(cfg, dev_inp: dict, rows, keep_intermediate=True, partials_bf16=False, clamp=None, f8_gran=128):
     x = dev_inp["x"].cpu().numpy()
     x_sf = dev_inp["x_sf"].cpu().numpy()
     idx = dev_inp["topk_idx"].cpu().numpy()
     w = dev_inp["topk_w"].cpu().numpy()
     return O.forward(rows, x, x_sf, idx, w, host_experts(dev_inp), cfg.H, cfg.I, cfg.E, cfg.variant,
-                     keep_intermediate=keep_intermediate, partials_bf16=partials_bf16, clamp=clamp)
+                     keep_intermediate=keep_intermediate, partials_bf16=partials_bf16, clamp=clamp,
+                     f8_gran=f8_gran, shared=cfg.S)
 
 
 # Lines printed in pytest's terminal summary (tests/conftest.py): what the
@@ -95,7 +104,7 @@ def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict, label: st
     REPORT."""
     rows = int(M.mm_moe_workspace_region(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, 4)[1] // 4)
     codes = torch.empty(rows, cfg.I, dtype=torch.uint8, device="cuda")
-    bs = 32 if cfg.variant == "mx" else 128
+    bs = 32 if cfg.variant == "mx" else f8_gran(cfg, opt)
     sf = torch.empty(rows, cfg.I // bs, dtype=torch.uint8 if cfg.variant == "mx" else torch.float32, device="cuda")
     r = M.mm_moe_read_intermediate(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, rows, codes.data_ptr(),
                                    sf.data_ptr(), torch.cuda.current_stream().cuda_stream)
@@ -131,9 +140,9 @@ def intermediate_match(M, cfg, ws, opt, slot: np.ndarray, inter: dict, label: st
 
 
 def read_routing(M, cfg, ws, opt):
-    cnt = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
-    blk = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
-    slot = torch.empty(cfg.T, cfg.K, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(cfg.E + cfg.S, dtype=torch.int32, device="cuda")      # shared experts included
+    blk = torch.empty(cfg.E + cfg.S + 1, dtype=torch.int32, device="cuda")
+    slot = torch.empty(cfg.T, cfg.K + cfg.S, dtype=torch.int32, device="cuda")
     nsrc = M.mm_moe_workspace_region(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, 4)[1] // 4
     src = torch.empty(nsrc, dtype=torch.int32, device="cuda")
     r, bm = M.mm_moe_read_routing(ws.data_ptr(), opt, cfg.T, cfg.H, cfg.I, cfg.E, cfg.K, cnt.data_ptr(),

@@ -118,8 +118,45 @@ def test_options_struct_layout_matches_the_header(M, tmp_path):
         assert getattr(M.mm_moe_options, n).offset == off, n
 
 
+def test_f8_scale_width_option_host_checks(M):
+    """f8_act_gran takes 0 (per 128), -1 (the pages' shape rule), 64 or 128; the
+    per-64 intermediate holds twice the scales of the per-128 one (fp32 [P, I / 64])."""
+    T, H, I, E, K = 300, 512, 384, 5, 2
+    for g in (32, 96, 256, -2):
+        with pytest.raises(M.MMError) as ei:
+            M.mm_moe_workspace_size(M.options(M.MM_MOE_VARIANT_F8, f8_act_gran=g), T, H, I, E, K)
+        assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG
+    n = {g: M.mm_moe_workspace_size(M.options(M.MM_MOE_VARIANT_F8, f8_act_gran=g), T, H, I, E, K)
+         for g in (0, -1, 64, 128)}
+    assert n[0] == n[128] < n[64] == n[-1]        # H = 512, 2I = 768: the rule takes 64
+    _, sf_bytes = M.mm_moe_workspace_region(0, M.options(M.MM_MOE_VARIANT_F8, f8_act_gran=64), T, H, I, E, K, 8)
+    _, sf128 = M.mm_moe_workspace_region(0, M.options(M.MM_MOE_VARIANT_F8, f8_act_gran=128), T, H, I, E, K, 8)
+    assert sf_bytes >= 2 * (sf128 - 1023)
+
+
+def test_shared_experts_host_checks(M):
+    """Shared experts add S slots per token and S experts: K + S <= 16 and
+    E + S <= 1024, and the workspace grows with them."""
+    T, H, I, E, K = 64, 256, 128, 8, 2
+    base = M.mm_moe_workspace_size(M.options(), T, H, I, E, K)
+    one = M.mm_moe_workspace_size(M.options(shared_experts=1), T, H, I, E, K)
+    assert one > base
+    assert M.mm_moe_workspace_size(M.options(shared_experts=14), T, H, I, E, K) > one
+    for bad in (dict(shared_experts=15), dict(shared_experts=-1)):
+        with pytest.raises(M.MMError) as ei:
+            M.mm_moe_workspace_size(M.options(**bad), T, H, I, E, K)
+        assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG
+    with pytest.raises(M.MMError):
+        M.mm_moe_workspace_size(M.options(shared_experts=2), T, H, I, 1023, K)
+    # the routing regions count the shared slots and experts
+    _, cnt_bytes = M.mm_moe_workspace_region(0, M.options(shared_experts=3), T, H, I, E, K, 1)
+    _, slot_bytes = M.mm_moe_workspace_region(0, M.options(shared_experts=3), T, H, I, E, K, 3)
+    assert cnt_bytes == 4 * (E + 3) and slot_bytes == 4 * T * (K + 3)
+
+
 def test_default_options(M):
     o = M.mm_moe_default_options()
     assert (o.variant, o.fused, o.lag_units, o.wait_timeout_ms) == (M.MM_MOE_VARIANT_MX, 1, -1, 2000)
+    assert (o.f8_act_gran, o.shared_experts) == (0, 0)
     assert (o.cta_pairs, o.partials_bf16, o.precise_swiglu, o.x_bf16, o.early_combine) == (0, 0, 0, 0, 0)
     assert o.activation_clamp == 0.0 and not o.timing_events

@@ -28,7 +28,8 @@ def _worker(rank, world, port, q):
     ws, r, local = bench.dist_setup(world)
     bench.barrier(ws)
     m = bench.max_over_ranks(float(10 + 5 * rank), ws)
-    args = type("A", (), {"config": "tiny", "ref_tokens": 2, "steps": 1, "warmup": 0, "x": "fp8"})()
+    args = type("A", (), {"config": "tiny", "ref_tokens": 2, "steps": 1, "warmup": 0, "x": "fp8", "shared": 0,
+                          "f8_gran": 0})()
     res = bench.run_reference(args, ws, r)
     q.put((rank, ws, m, res is None, None if res is None else res["impl"]))
     dist.destroy_process_group()

@@ -68,7 +68,9 @@ def test_smallest_shapes(M, variant, kw):
         _check(M, cfg, _inputs(cfg, 0.0), **kw)
 
 
-def test_f8_largest_contraction(M):
-    """H = I = 8192, the largest the FP8 epilogue stages scales for (64 k-blocks)."""
+def test_f8_long_contraction(M):
+    """H = I = 8192 and H = 12288: 64 and 96 k-blocks of promotion per task."""
     cfg = W.Config("f8_big", T=16, H=8192, I=8192, E=1, K=1, variant="f8", seed=53)
+    _check(M, cfg, _inputs(cfg, 0.0))
+    cfg = W.Config("f8_bigger", T=16, H=12288, I=1024, E=2, K=1, variant="f8", seed=54)
     _check(M, cfg, _inputs(cfg, 0.0))

@@ -36,8 +36,8 @@ def _deq_all(cfg, inp):
     return x, wq(inp["w1"], inp["w1_sf"]), wq(inp["w2"], inp["w2_sf"])
 
 
-def _requant_torch(a32: torch.Tensor, variant: str) -> torch.Tensor:
-    """Independent requant: library e4m3 cast, frexp-based exponent."""
+def _requant_torch(a32: torch.Tensor, variant: str, gran: int = 128) -> torch.Tensor:
+    """Independent requant: library e4m3 cast, frexp-based exponent; FP8 blocks of `gran`."""
     n = a32.shape[-1]
     if variant == "mx":
         b = a32.reshape(*a32.shape[:-1], n // 32, 32)
@@ -46,26 +46,29 @@ def _requant_torch(a32: torch.Tensor, variant: str) -> torch.Tensor:
         e = torch.where(m <= 0.875, ex - 9, ex - 8).clamp(-127, 127).double()
         q = (b.double() * torch.exp2(-e)[..., None]).float().to(torch.float8_e4m3fn)
         return (q.double() * torch.exp2(e)[..., None]).reshape(a32.shape)
-    b = a32.reshape(*a32.shape[:-1], n // 128, 128)
+    b = a32.reshape(*a32.shape[:-1], n // gran, gran)
     s = b.abs().amax(-1).clamp_min(1e-10) / 448.0
     q = (b / s[..., None]).to(torch.float8_e4m3fn)
     return (q.double() * s.double()[..., None]).reshape(a32.shape)
 
 
-def brute_force(cfg, inp, partials_bf16=False, clamp=None):
+def brute_force(cfg, inp, partials_bf16=False, clamp=None, gran=128):
+    """Dense per-slot loop; shared experts (cfg.S) as slots K .. K+S-1 that every
+    token uses with weight 1."""
     x, W1, W2 = _deq_all(cfg, inp)
-    idx, w = inp["topk_idx"].long(), inp["topk_w"].double()
     T, I = cfg.T, cfg.I
+    idx = torch.cat([inp["topk_idx"].long(), torch.arange(cfg.E, cfg.E + cfg.S).expand(T, cfg.S)], 1)
+    w = torch.cat([inp["topk_w"].double(), torch.ones(T, cfg.S, dtype=torch.float64)], 1)
     out = torch.zeros(T, cfg.H, dtype=torch.float64)
-    for k in range(cfg.K):
-        valid = (idx[:, k] >= 0) & (idx[:, k] < cfg.E)
-        e = idx[:, k].clamp(0, cfg.E - 1)
+    for k in range(cfg.K + cfg.S):
+        valid = (idx[:, k] >= 0) & (idx[:, k] < cfg.E + cfg.S)
+        e = idx[:, k].clamp(0, cfg.E + cfg.S - 1)
         h = torch.einsum("tnh,th->tn", W1[e], x)
         g, u = h[:, :I], h[:, I:]
         if clamp is not None:
             g, u = g.clamp(-clamp, clamp), u.clamp(-clamp, clamp)
         a = torch.nn.functional.silu(g) * u * w[:, k:k + 1]
-        ah = _requant_torch(a.float(), cfg.variant)
+        ah = _requant_torch(a.float(), cfg.variant, gran)
         y = torch.einsum("thi,ti->th", W2[e], ah)
         if partials_bf16:                  # library cast, round to nearest even
             y = y.to(torch.bfloat16).double()
@@ -73,13 +76,13 @@ def brute_force(cfg, inp, partials_bf16=False, clamp=None):
     return out
 
 
-def run_oracle(cfg, inp, rows=None, partials_bf16=False, clamp=None):
+def run_oracle(cfg, inp, rows=None, partials_bf16=False, clamp=None, f8_gran=128):
     npi = W.to_numpy(inp)
     rows = np.arange(cfg.T) if rows is None else rows
     out, inter = O.forward(rows, npi["x"], npi["x_sf"], npi["topk_idx"], npi["topk_w"],
                            O.expert_from_arrays(npi["w1"], npi["w1_sf"], npi["w2"], npi["w2_sf"]),
                            cfg.H, cfg.I, cfg.E, cfg.variant, keep_intermediate=True, partials_bf16=partials_bf16,
-                           clamp=clamp)
+                           clamp=clamp, f8_gran=f8_gran, shared=cfg.S)
     return out, inter
 
 
@@ -229,3 +232,91 @@ def test_oracle_intermediate_codes_are_the_requant_of_the_activation():
     codes, sf = inter[(t, k)]
     assert np.array_equal(O.e4m3_decode(codes) * np.repeat(2.0 ** (sf.astype(int) - 127), 32),
                           _requant_torch(a.float()[None], "mx")[0].numpy())
+
+
+# ------------------------------------------------------------------ FP8 intermediate scale width
+def test_oracle_f8_gran_rule_on_the_pages_shapes():
+    """DeepGEMM PR #440 runs its benchmark shapes (flash: H=4096, I=2048; pro:
+    H=7168, I=3072) at the default width, 128; a hidden size or 2I that is not a
+    multiple of 512 takes 64."""
+    assert O.f8_act_gran(4096, 2048) == 128
+    assert O.f8_act_gran(7168, 3072) == 128
+    assert O.f8_act_gran(256, 256) == 64       # H % 512 != 0
+    assert O.f8_act_gran(512, 128) == 64       # 2I = 256
+    assert O.f8_act_gran(1024, 384) == 64      # 2I = 768
+    assert O.f8_act_gran(1024, 256) == 128
+
+
+@pytest.mark.parametrize("gran", [64, 128])
+def test_oracle_f8_scale_width_matches_dense_brute_force(gran):
+    """Per-64 and per-128 intermediate scales against the torch brute force; the
+    two widths give different outputs on random data."""
+    cfg = TINY_F8.with_(seed=13)
+    inp = W.make_inputs(cfg, "cpu")
+    out, inter = run_oracle(cfg, inp, f8_gran=gran)
+    ref = O.bf16_rne(brute_force(cfg, inp, gran=gran).numpy())
+    assert np.mean(out == ref) > 0.999
+    assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
+    codes, sf = next(iter(inter.values()))
+    assert sf.shape == (cfg.I // gran,)
+    other, _ = run_oracle(cfg, inp, f8_gran=192 - gran)
+    assert not np.array_equal(out, other)
+
+
+def test_oracle_f8_per64_equals_per128_when_halves_share_amax():
+    """A 128-block whose two 64-halves have the same amax has the same scale and
+    codes at either width (closed form of the raw-scale rule)."""
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal(256).astype(np.float32)
+    for b in range(2):                           # every half of both blocks peaks at +-3.5
+        for h in range(2):
+            seg = a[128 * b + 64 * h: 128 * b + 64 * h + 64]
+            seg[np.argmax(np.abs(seg))] = np.float32(3.5) * np.sign(seg[np.argmax(np.abs(seg))])
+    c64, s64, d64 = O.requant_f8(a, 64)
+    c128, s128, d128 = O.requant_f8(a, 128)
+    assert np.array_equal(c64, c128) and np.array_equal(d64, d128)
+    assert np.array_equal(s64, np.repeat(s128, 2))
+
+
+# ------------------------------------------------------------------ shared experts
+SHARED = [TINY_MX.with_(seed=14, S=1), TINY_MX.with_(seed=15, S=2, K=3), TINY_F8.with_(seed=16, S=1)]
+
+
+@pytest.mark.parametrize("cfg", SHARED, ids=["mx_s1", "mx_s2_k3", "f8_s1"])
+def test_oracle_shared_experts_match_dense_brute_force(cfg):
+    inp = W.make_inputs(cfg, "cpu")
+    gran = 128 if cfg.variant == "mx" else O.f8_act_gran(cfg.H, cfg.I)
+    out, inter = run_oracle(cfg, inp, f8_gran=gran)
+    ref = O.bf16_rne(brute_force(cfg, inp, gran=gran).numpy())
+    assert np.mean(out == ref) > 0.999
+    assert np.max(np.abs(out - ref)) <= 2.0 ** -7 * np.max(np.abs(ref))
+    assert all((t, cfg.K + j) in inter for t in range(cfg.T) for j in range(cfg.S))
+
+
+def test_oracle_shared_expert_alone_is_a_dense_mlp():
+    """Every routed slot masked: the output is the shared expert's SwiGLU MLP
+    (weight 1) on every token."""
+    cfg = TINY_MX.with_(seed=17, S=1)
+    inp = W.make_inputs(cfg, "cpu")
+    inp["topk_idx"].fill_(-1)
+    out, _ = run_oracle(cfg, inp)
+    x, W1, W2 = _deq_all(cfg, inp)
+    h = x @ W1[cfg.E].T
+    a = torch.nn.functional.silu(h[:, :cfg.I]) * h[:, cfg.I:]
+    ref = _requant_torch(a.float(), "mx") @ W2[cfg.E].T
+    assert np.mean(out == O.bf16_rne(ref.numpy())) > 0.999
+    assert np.abs(out).max() > 0
+
+
+def test_oracle_shared_expert_equals_a_routed_expert_every_token_picks():
+    """The shared slot is the plain reading of a routed slot to expert E with weight
+    1 appended to every token's routing."""
+    cfg = TINY_MX.with_(seed=18, S=1)
+    inp = W.make_inputs(cfg, "cpu")
+    out, _ = run_oracle(cfg, inp)
+    routed = cfg.with_(E=cfg.E + 1, K=cfg.K + 1, S=0)
+    inp2 = dict(inp)
+    inp2["topk_idx"] = torch.cat([inp["topk_idx"], torch.full((cfg.T, 1), cfg.E, dtype=torch.int32)], 1)
+    inp2["topk_w"] = torch.cat([inp["topk_w"], torch.ones(cfg.T, 1)], 1)
+    out2, _ = run_oracle(routed, inp2)
+    assert np.array_equal(out, out2)

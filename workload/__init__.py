@@ -43,6 +43,7 @@ class Config:
     routing: str = "uniform"   # "uniform" | "zipf"
     zipf_s: float = 1.1
     seed: int = 0
+    S: int = 0                 # shared experts: experts E .. E+S-1, used by every token (not routed)
 
     @property
     def flops(self) -> float:
@@ -179,7 +180,7 @@ def make_expert(cfg: Config, e: int, device="cpu"):
 
 
 def weight_shapes(cfg: Config):
-    E, H, I = cfg.E, cfg.H, cfg.I
+    E, H, I = cfg.E + cfg.S, cfg.H, cfg.I
     if cfg.variant == "mx":
         return {"w1": ((E, 2 * I, H // 2), torch.uint8), "w1_sf": ((E, 2 * I, H // 32), torch.uint8),
                 "w2": ((E, H, I // 2), torch.uint8), "w2_sf": ((E, H, I // 32), torch.uint8)}
@@ -188,10 +189,11 @@ def weight_shapes(cfg: Config):
 
 
 def make_weights(cfg: Config, device="cpu", experts: Optional[list] = None):
-    """Stacked weights [E, ...]; experts not listed in `experts` stay zero."""
+    """Stacked weights [E + S, ...] (shared experts last); experts not listed in
+    `experts` stay zero."""
     shp = weight_shapes(cfg)
     out = {k: torch.zeros(s, dtype=dt, device=device) for k, (s, dt) in shp.items()}
-    for e in (range(cfg.E) if experts is None else experts):
+    for e in (range(cfg.E + cfg.S) if experts is None else experts):
         w1, s1, w2, s2 = make_expert(cfg, e, device)
         out["w1"][e].copy_(w1)
         out["w1_sf"][e].copy_(s1)
