@@ -256,10 +256,78 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
  *             gathered rows, 106 a pool block's L1 tiles, 107 / 108 the
  *             tile-group queue, 109 an early-combine token's experts, 110 an
  *             early-combine deferred entry;
- *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 203 a free
- *             partial buffer, 204 a finished partial, 205 the epilogue's
- *             rendezvous (amax exchange, staged weight scales). */
+ *             111 / 112 the exit drain of bulk copies / MMAs (after an earlier
+ *             error); swapped and paired kernels 121-152 likewise;
+ *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 204 a finished
+ *             partial (the waiter warp), 205 the epilogue's amax rendezvous,
+ *             211 / 212 the exit drains. */
 int mm_moe_sync_status(const void* workspace, void* stream, int* where);
+
+/* ---------------------------------------------------------------------------
+ * Expert parallelism over N ranks: the pages' EP dispatch and combine (llm-infra-
+ * atlas "07 · MegaMoE" §7 count -> push metadata -> pull data, §9 combine;
+ * DeepGEMM PR #440 "How it works").  Rank r owns experts [r*E/N, (r+1)*E/N)
+ * (E % N == 0).  One EP forward, on every rank:
+ *   1. mm_moe_ep_count: this rank's pairs per expert -> counts[E] (device).
+ *   2. the caller exchanges the counts (an all-gather: counts_all[N][E] on the host),
+ *      and mm_moe_ep_plan gives every routed pair its row in the owner's receive
+ *      buffer and this rank's receive row count;
+ *   3. mm_moe_ep_push_meta: each pair's (source rank, pair index, local expert,
+ *      weight) is stored into its owner's receive-metadata buffer;
+ *   4. barrier; mm_moe_ep_pull: the owner copies each received row's activations
+ *      and scales from the source rank's x into its own receive buffers, and writes
+ *      the local routing (one slot a row) that mm_moe_forward then runs on with
+ *      E/N experts and K = 1 (the received pairs as tokens);
+ *   5. barrier; mm_moe_ep_combine: each rank sums, for each of its tokens, the
+ *      bf16 outputs of its pairs' rows at their owners, in k order, in fp32, and
+ *      rounds once to bf16: the bf16-partials combine of the pages (each pair's
+ *      output reaches the combine as bf16).
+ * Peer buffers are reached through device arrays of N device pointers (peer_*[r]
+ * is rank r's buffer, [rank] this rank's own), read or written with plain
+ * loads and stores from this GPU's kernels; no TMA and no multicast touches a
+ * peer's memory.  The barriers between steps are the caller's (host collectives
+ * with a timeout), so no kernel waits on another rank.  Every call is
+ * stream-ordered and asynchronous; none allocates.
+ * Receive-row order on an owner: local expert, then source rank, then the
+ * source's pairs in ascending (token, slot): with tokens numbered rank-major, the
+ * same order as mm_moe_dispatch's over all ranks' tokens. */
+
+/* counts[e] (device int32 [E], overwritten) = pairs of topk_idx [T, K] (device)
+ * with expert e; ids < 0 or >= E are not counted. */
+int mm_moe_ep_count(const int32_t* topk_idx, int T, int K, int E, int32_t* counts, void* stream);
+
+/* Host planning (no GPU).  counts_all: host [N][E], counts_all[r][e] = rank r's
+ * pairs with expert e (this rank's row must equal its own topk_idx); topk_idx:
+ * host [T, K] of this rank.  Writes send_row (host [T*K]): the pair's row in its
+ * owner's receive buffer (owner = expert / (E/N)), -1 for masked or out-of-range
+ * ids; *recv_rows: the rows this rank receives; recv_expert (host [recv_capacity],
+ * optional): each received row's local expert.  MM_MOE_ERR_INVALID_ARG on bad
+ * sizes, counts that disagree with topk_idx, or recv_capacity < *recv_rows. */
+int mm_moe_ep_plan(const int32_t* counts_all, const int32_t* topk_idx, int T, int K, int E, int N, int rank,
+                   int32_t* send_row, int64_t* recv_rows, int32_t* recv_expert, int64_t recv_capacity);
+
+/* Step 3.  topk_idx, topk_w [T, K] and send_row [T*K] are this rank's (device);
+ * peer_meta: device array of N pointers to each rank's receive metadata, int32
+ * [rows][4] = (source rank, pair index t*K+k, local expert, weight bits). */
+int mm_moe_ep_push_meta(const int32_t* topk_idx, const float* topk_w, const int32_t* send_row, int T, int K,
+                        int E, int N, int rank, void* const* peer_meta, void* stream);
+
+/* Step 4.  meta: this rank's receive metadata (device int32 [rows][4], written by
+ * step 3 on every rank); peer_x / peer_x_sf: device arrays of N pointers to each
+ * rank's x [T_r, H] (e4m3 bytes) and x_sf (MX: UE8M0 [T_r, H/32]; F8: fp32
+ * [T_r, H/128]); K: slots per token on every rank.  Writes x_recv [rows, H],
+ * x_sf_recv (same layout), topk_idx_recv / topk_w_recv [rows] (K = 1 routing over
+ * the E/N local experts). */
+int mm_moe_ep_pull(const int32_t* meta, int64_t rows, int K, int H, int variant, const void* const* peer_x,
+                   const void* const* peer_x_sf, void* x_recv, void* x_sf_recv, int32_t* topk_idx_recv,
+                   float* topk_w_recv, void* stream);
+
+/* Step 5.  peer_out: device array of N pointers to each rank's bf16 [rows_r, H]
+ * output of its local forward; topk_idx [T, K] and send_row [T*K] this rank's
+ * (device).  out [T, H] bf16: the fixed-k-order sum, 0 for a token with no
+ * valid slot. */
+int mm_moe_ep_combine(const int32_t* topk_idx, const int32_t* send_row, int T, int K, int E, int N, int H,
+                      const void* const* peer_out, void* out, void* stream);
 
 /* Human-readable name of a return code. */
 const char* mm_moe_status_string(int code);

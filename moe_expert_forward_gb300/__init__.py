@@ -31,7 +31,8 @@ STAGES = ["dispatch", "gather", "l1", "l2", "combine"]
 EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_size", "mm_moe_prepare_weights",
            "mm_moe_forward", "mm_moe_dispatch_scratch_size", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
            "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region",
-           "mm_moe_dispatch_noalloc"]
+           "mm_moe_dispatch_noalloc", "mm_moe_ep_count", "mm_moe_ep_plan", "mm_moe_ep_push_meta", "mm_moe_ep_pull",
+           "mm_moe_ep_combine"]
 
 
 class mm_moe_options(ctypes.Structure):
@@ -80,6 +81,11 @@ def lib() -> ctypes.CDLL:
             "mm_moe_dispatch_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _I64, _P, _P]),
             "mm_moe_workspace_region": (_I, [_P, _OPT, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P),
                                              ctypes.POINTER(_SZ)]),
+            "mm_moe_ep_count": (_I, [_P, _I, _I, _I, _P, _P]),
+            "mm_moe_ep_plan": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, ctypes.POINTER(_I64), _P, _I64]),
+            "mm_moe_ep_push_meta": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+            "mm_moe_ep_pull": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+            "mm_moe_ep_combine": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -280,3 +286,42 @@ def forward(x, x_sf, topk_idx, topk_w, w1, w1_sfp, w2, w2_sfp, out, H, I, E, wor
 def sync_status(workspace, stream=None):
     code, where = mm_moe_sync_status(_ptr(workspace), _stream(stream))
     return code, where
+
+
+# ------------------------------------------------------------------ expert parallelism (C entry points)
+def mm_moe_ep_count(topk_idx, T, K, E, counts, stream) -> int:
+    return lib().mm_moe_ep_count(topk_idx, T, K, E, counts, stream)
+
+
+def mm_moe_ep_plan(counts_all, topk_idx, T, K, E, N, rank, recv_expert=True):
+    """Host planning (numpy in, numpy out): counts_all int32 [N, E], topk_idx int32
+    [T, K] of this rank.  Returns (send_row int32 [T*K], recv_rows, recv_expert
+    int32 [recv_rows] or None)."""
+    import numpy as np
+    counts_all = np.ascontiguousarray(counts_all, dtype=np.int32)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    send_row = np.empty(max(T * K, 1), dtype=np.int32)
+    rows = _I64(0)
+    _check(lib().mm_moe_ep_plan(counts_all.ctypes.data, topk_idx.ctypes.data, T, K, E, N, rank,
+                                send_row.ctypes.data, ctypes.byref(rows), None, 0), "mm_moe_ep_plan")
+    rex = None
+    if recv_expert:
+        rex = np.empty(max(rows.value, 1), dtype=np.int32)
+        _check(lib().mm_moe_ep_plan(counts_all.ctypes.data, topk_idx.ctypes.data, T, K, E, N, rank,
+                                    send_row.ctypes.data, ctypes.byref(rows), rex.ctypes.data, rex.size),
+               "mm_moe_ep_plan")
+        rex = rex[:rows.value]
+    return send_row[:T * K], rows.value, rex
+
+
+def mm_moe_ep_push_meta(topk_idx, topk_w, send_row, T, K, E, N, rank, peer_meta, stream) -> int:
+    return lib().mm_moe_ep_push_meta(topk_idx, topk_w, send_row, T, K, E, N, rank, peer_meta, stream)
+
+
+def mm_moe_ep_pull(meta, rows, K, H, variant, peer_x, peer_x_sf, x_recv, x_sf_recv, idx_recv, w_recv, stream) -> int:
+    return lib().mm_moe_ep_pull(meta, rows, K, H, variant, peer_x, peer_x_sf, x_recv, x_sf_recv, idx_recv, w_recv,
+                                stream)
+
+
+def mm_moe_ep_combine(topk_idx, send_row, T, K, E, N, H, peer_out, out, stream) -> int:
+    return lib().mm_moe_ep_combine(topk_idx, send_row, T, K, E, N, H, peer_out, out, stream)

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmm_moe.so")
-SOURCES = ["api.cu", "kernels_misc.cu", "gemm_mx.cu", "gemm_mx_sw.cu", "gemm_mx_pair.cu", "gemm_f8.cu", "dispatch_noalloc.cu"]
+SOURCES = ["api.cu", "kernels_misc.cu", "gemm_mx.cu", "gemm_mx_sw.cu", "gemm_mx_pair.cu", "gemm_f8.cu", "dispatch_noalloc.cu", "ep.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "sched.cuh", "quant.cuh", "combine.cuh", "stream.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

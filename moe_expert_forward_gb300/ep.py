@@ -1,0 +1,134 @@
+"""Expert parallelism over N ranks, driven through the library's EP entry points
+(include/mm_moe.h, mm_moe_ep_*).
+
+Rank r owns experts [r*E/N, (r+1)*E/N).  One forward runs, on every rank:
+count -> exchange counts -> plan -> push metadata -> barrier -> pull rows ->
+local forward (K = 1 over the received pairs) -> barrier -> combine
+(llm-infra-atlas "07 · MegaMoE" §7 count / push metadata / pull data and §9
+combine; DeepGEMM PR #440 "How it works").  The kernels read and write peers'
+buffers through device tables of their addresses; the exchange of the counts and
+the barriers are host collectives, so no kernel waits on another rank.
+
+`plan_distributed` is the host side of a multi-process run (torch.distributed:
+an all-gather of the counts).  `forward_on_one_device` runs N ranks whose buffers
+all live on one GPU, step by step from the host, which checks the whole data path
+on a single device; a multi-GPU run differs only in where the peers' buffers live.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+from . import (MM_MOE_VARIANT_MX, MMError, _check, alloc_workspace, forward, mm_moe_ep_combine, mm_moe_ep_count,
+               mm_moe_ep_plan, mm_moe_ep_pull, mm_moe_ep_push_meta, options, prepare_weights, sync_status)
+
+
+def host_counts(topk_idx: np.ndarray, E: int) -> np.ndarray:
+    """Pairs per expert of one rank's routing (ids outside [0, E) not counted)."""
+    idx = np.asarray(topk_idx).reshape(-1)
+    idx = idx[(idx >= 0) & (idx < E)]
+    return np.bincount(idx, minlength=E).astype(np.int32)
+
+
+def plan_distributed(topk_idx: np.ndarray, E: int, group=None):
+    """All-gather every rank's per-expert counts, then plan this rank's pairs.
+    Returns (counts_all [N, E], send_row [T*K], recv_rows, recv_expert)."""
+    import torch
+    import torch.distributed as dist
+    N = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    mine = torch.from_numpy(host_counts(topk_idx, E))
+    parts = [torch.empty_like(mine) for _ in range(N)]
+    dist.all_gather(parts, mine, group=group)
+    counts_all = torch.stack(parts).numpy()
+    T, K = np.asarray(topk_idx).shape
+    send_row, rows, rex = mm_moe_ep_plan(counts_all, topk_idx, T, K, E, N, rank)
+    return counts_all, send_row, rows, rex
+
+
+def pointer_table(tensors: Sequence, device):
+    """Device int64 array of the tensors' addresses (a peer-pointer table)."""
+    import torch
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+class RankState:
+    """One rank's buffers: its tokens, its plan and its receive buffers."""
+
+    def __init__(self, rank: int, x, x_sf, topk_idx, topk_w, E: int, N: int, variant: int):
+        self.rank, self.E, self.N, self.variant = rank, E, N, variant
+        self.x, self.x_sf, self.topk_idx, self.topk_w = x, x_sf, topk_idx, topk_w
+        self.T, self.K = topk_idx.shape
+        self.H = x.shape[1]
+
+
+def forward_on_one_device(states: List[RankState], w1, w1_sf, w2, w2_sf, I: int, opt=None, stream=None):
+    """Run the EP forward for every rank in `states` (buffers on one device).
+    w1 / w1_sf / w2 / w2_sf hold all E experts in the layouts of mm_moe.h; rank r
+    uses experts [r*E/N, (r+1)*E/N).  Returns the per-rank bf16 outputs [T_r, H]
+    and the per-rank plans (send_row, recv_rows, recv_expert)."""
+    import torch
+    N = len(states)
+    E, H, variant = states[0].E, states[0].H, states[0].variant
+    Eloc = E // N
+    dev = states[0].x.device
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    base_opt = opt if opt is not None else options(variant)
+    # 1. counts on the device, gathered on the host (the all-gather of a multi-GPU run)
+    counts = []
+    for st in states:
+        c = torch.empty(E, dtype=torch.int32, device=dev)
+        _check(mm_moe_ep_count(st.topk_idx.data_ptr(), st.T, st.K, E, c.data_ptr(), s), "mm_moe_ep_count")
+        counts.append(c)
+    counts_all = torch.stack(counts).cpu().numpy()
+    # 2. plans and receive buffers
+    plans = []
+    for st in states:
+        send_row, rows, rex = mm_moe_ep_plan(counts_all, st.topk_idx.cpu().numpy(), st.T, st.K, E, N, st.rank)
+        st.send_row = torch.from_numpy(np.ascontiguousarray(send_row)).to(dev)
+        st.rows = rows
+        st.meta = torch.zeros(max(rows, 1), 4, dtype=torch.int32, device=dev)
+        plans.append((send_row, rows, rex))
+    # 3. metadata pushed into the owners' buffers
+    peer_meta = pointer_table([st.meta for st in states], dev)
+    for st in states:
+        _check(mm_moe_ep_push_meta(st.topk_idx.data_ptr(), st.topk_w.data_ptr(), st.send_row.data_ptr(), st.T, st.K,
+                                   E, N, st.rank, peer_meta.data_ptr(), s), "mm_moe_ep_push_meta")
+    torch.cuda.synchronize()                                  # barrier
+    # 4. rows pulled from the source ranks, then each rank's local forward
+    peer_x = pointer_table([st.x for st in states], dev)
+    peer_xsf = pointer_table([st.x_sf for st in states], dev)
+    sf_row = H // 32 if variant == MM_MOE_VARIANT_MX else H // 128
+    sf_dtype = torch.uint8 if variant == MM_MOE_VARIANT_MX else torch.float32
+    for st in states:
+        R = st.rows
+        st.out_recv = torch.zeros(max(R, 1), H, dtype=torch.bfloat16, device=dev)
+        if R == 0:
+            continue
+        x_recv = torch.empty(R, H, dtype=torch.uint8, device=dev)
+        xsf_recv = torch.empty(R, sf_row, dtype=sf_dtype, device=dev)
+        idx_recv = torch.empty(R, 1, dtype=torch.int32, device=dev)
+        w_recv = torch.empty(R, 1, dtype=torch.float32, device=dev)
+        _check(mm_moe_ep_pull(st.meta.data_ptr(), R, st.K, H, variant, peer_x.data_ptr(), peer_xsf.data_ptr(),
+                              x_recv.data_ptr(), xsf_recv.data_ptr(), idx_recv.data_ptr(), w_recv.data_ptr(), s),
+               "mm_moe_ep_pull")
+        lo, hi = st.rank * Eloc, (st.rank + 1) * Eloc
+        w1p, w2p = prepare_weights(w1_sf[lo:hi].contiguous(), w2_sf[lo:hi].contiguous(), H, I, Eloc, base_opt)
+        ws = alloc_workspace(R, H, I, Eloc, 1, base_opt, dev)
+        forward(x_recv, xsf_recv, idx_recv, w_recv, w1[lo:hi].contiguous(), w1p, w2[lo:hi].contiguous(), w2p,
+                st.out_recv, H, I, Eloc, ws, base_opt)
+        code, where = sync_status(ws)
+        if code != 0:
+            raise MMError(code, f"rank {st.rank} local forward (site {where})")
+    torch.cuda.synchronize()                                  # barrier
+    # 5. combine from the owners' outputs
+    peer_out = pointer_table([st.out_recv for st in states], dev)
+    outs = []
+    for st in states:
+        out = torch.empty(st.T, H, dtype=torch.bfloat16, device=dev)
+        _check(mm_moe_ep_combine(st.topk_idx.data_ptr(), st.send_row.data_ptr(), st.T, st.K, E, N, H,
+                                 peer_out.data_ptr(), out.data_ptr(), s), "mm_moe_ep_combine")
+        outs.append(out)
+    torch.cuda.synchronize()
+    return outs, plans
