@@ -97,9 +97,11 @@ typedef struct mm_moe_options {
                                    call stops after L1; bit 1: the GEMM kernels record per-CTA
                                    wait/busy times of their roles into the PROF workspace region;
                                    bit 2: in the fused stream every L2 tile waits for one more L1
-                                   completion than will ever arrive, so the call ends with
-                                   MM_MOE_ERR_TIMEOUT after wait_timeout_ms (tests the device-side
-                                   timeout path); 0 for normal use */
+                                   completion than will ever arrive, and in the FP8 L1 GEMM the
+                                   last stage of each CTA's last task is never loaded, so the call
+                                   ends with MM_MOE_ERR_TIMEOUT after wait_timeout_ms (tests the
+                                   device-side timeout path); bit 4: FP8 requant divides for every
+                                   code (the fast path is bit-equal; for tests); 0 for normal use */
   int cta_pairs;                /* reserved: 0 (default) or 1; any other value makes mm_moe_forward
                                    return MM_MOE_ERR_UNSUPPORTED */
   int partials_bf16;            /* 0 (default): the L2 epilogue writes fp32 partials [K, T, H] and the
@@ -258,9 +260,9 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
  *             early-combine deferred entry;
  *             111 / 112 the exit drain of bulk copies / MMAs (after an earlier
  *             error); swapped and paired kernels 121-152 likewise;
- *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 204 a finished
- *             partial (the waiter warp), 205 the epilogue's amax rendezvous,
- *             211 / 212 the exit drains. */
+ *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 203 a free
+ *             partial buffer, 204 a finished partial (the commit waiter), 205
+ *             the epilogue's amax rendezvous, 211 / 212 the exit drains. */
 int mm_moe_sync_status(const void* workspace, void* stream, int* where);
 
 /* ---------------------------------------------------------------------------

@@ -445,7 +445,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
     }
   } else {
     GemmLaunchF8 g{&L, &W, static_cast<const uint8_t*>(w1), static_cast<const float*>(w1_sfp), wts, timeout_ns,
-                   grid, W.prof, clamp, o.precise_swiglu != 0, (o.debug_flags & 16) != 0};
+                   grid, W.prof, clamp, o.precise_swiglu != 0, (o.debug_flags & 16) != 0, (o.debug_flags & 4) != 0};
     if (e == cudaSuccess) e = launch_gemm_f8_l1(g, s);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) {

@@ -23,13 +23,14 @@
 //                      warp 14: waits for each unit's partial and passes it on
 //
 // While the tensor core streams its operands, every shared-memory access of
-// another warp (an mbarrier wait included) takes hundreds of cycles, so the
-// per-unit hand-offs between the issuers and the epilogue use named barriers,
-// which touch no shared memory: "unit complete" (barriers 1, 2: warp 14, which
-// waits on the unit's commit, arrives; the epilogue syncs) and "partial free"
-// (barriers 3, 4: the epilogue arrives after its TMEM loads; the issuer of the
-// buffer syncs).  The activation and weight scales of a unit reach registers
-// by plain loads two promotions ahead.
+// another warp (an mbarrier wait included) takes hundreds of cycles.  So the
+// epilogue learns that a unit's partial is complete through a named barrier
+// (barriers 1, 2), which touches no shared memory: warp 14 waits on the unit's
+// commit and arrives, the eight epilogue warps sync.  The release of a buffer
+// back to its issuer stays an mbarrier, whose wait is bounded: a named barrier
+// between two single-warp parties cannot be made safe on the abort path (one
+// side running two phases ahead completes a phase without the other).  The
+// activation and weight scales of a unit reach registers a group of units ahead.
 // setmaxnreg moves registers from WG0/WG3 (40 each) to WG1/WG2 (216 each);
 // the host refuses to launch unless the kernel was built with exactly 128
 // registers per thread, the total the split assumes.
@@ -56,8 +57,7 @@ constexpr int kWgtBytes = kBN * kBK;
 constexpr int kTmemCols = 512;
 constexpr int kEpiThreads = 256;       // the two epilogue warpgroups
 constexpr int kBarDone0 = 1;           // named barriers 1, 2: the partial of a unit in buffer 0 / 1 is complete
-constexpr int kBarFree0 = 3;           // named barriers 3, 4: buffer 0 / 1 has been read by the epilogue
-constexpr int kBarThreads = kEpiThreads + 32;   // the epilogue and one warp of WG3
+constexpr int kBarThreads = kEpiThreads + 32;   // the epilogue and warp 14
 
 enum : int {
   kSiteEmpty = 201, kSiteFull = 202, kSitePEmpty = 203, kSitePFull = 204, kSiteAmax = 205,
@@ -79,6 +79,7 @@ struct Args {
   int gran;             // L1: intermediate scale block along I, 128 or 64
   int units;            // promotion units per 128-K stage: 1, or 2 when L2 reads per-64 scales
   int exact_div;        // L1: every requant code from the IEEE quotient (no fast path)
+  int unreachable;      // the last stage of this CTA's last task is never loaded (a wait that cannot end)
   float* partials;      // L2: [K, T, H] fp32, or bf16 when pbf16
   int pbf16;
   float clamp;          // gate and up clamped to [-clamp, clamp] before the SwiGLU (+inf: none)
@@ -98,8 +99,8 @@ struct SmemLayout {
   static constexpr int amax = wgt + kStages * kWgtBytes;              // [2 tasks][2 halves][128] fp32
   static constexpr int meta = amax + 2 * 2 * 128 * 4;
   static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
-  // full[S], empty[S] (one commit per promotion unit: stage free and partial complete), epi, drain
-  static constexpr int nbars = 2 * kStages + 2;
+  // full[S], empty[S] (one commit per promotion unit: stage free and partial complete), pempty[2], epi, drain
+  static constexpr int nbars = 2 * kStages + 4;
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars_after_meta(E));
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
-  uint64_t* epibar = bars + 2 * kStages;
+  uint64_t* pempty = bars + 2 * kStages;   // [2]: buffer read by all eight epilogue warps
+  uint64_t* epibar = pempty + 2;
   uint64_t* drain = epibar + 1;   // the MMA issuers' last commits
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -187,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], U);                  // one commit per promotion unit of the stage
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&pempty[i], 8);
     mbar_init(epibar, 256);
     mbar_init(drain, 2);
     *s_abort = 0;
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kb = ((p - step) % kStages + kStages) % kStages;
         for (; kb < KB; kb += kStages) {
           const uint32_t phase = ((step + kb) / kStages) & 1;
+          if (args.unreachable && kb == KB - 1 && tile + static_cast<int>(gridDim.x) >= total) break;
           if (!mbar_wait(&empty[p], phase ^ 1, st, s_abort, kSiteEmpty)) break;
           mbar_arrive_expect_tx(&full[p], bytes);
           armed = true;
@@ -248,57 +252,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (wg == 3) {
     regs_dec_mma();
     // ------------------------------------------------------------------ MMA issuers
-    // Two warps issue alternate promotion units, each into its own partial
-    // buffer (unit g: buffer and warp g & 1, stage (g / U) % kStages), lane 0
-    // issuing.  Every unit is a fresh accumulation of 4 / U MMAs, so the order in
+    // Two threads (lane 0 of warps 12, 13) issue alternate promotion units, each
+    // into its own partial buffer (unit g: buffer and thread g & 1, stage (g / U) %
+    // kStages).  Every unit is a fresh accumulation of 4 / U MMAs, so the order in
     // which the two streams reach the tensor core changes no result.  A unit
     // waits for its stage's data first (that usually landed while the epilogue
     // was still promoting), then for its buffer: the epilogue's release of unit
-    // g - 2.  One commit per unit on its stage's empty barrier frees the stage
+    // g - 2 (bounded mbarrier waits).  One commit per unit on its stage's empty barrier frees the stage
     // (after all U units) and completes the partial.
-    if (warp == 12 || warp == 13) {
+    if ((warp == 12 || warp == 13) && lane == 0) {
       const int me = warp - 12;
-      const int per = 4 / U;                     // MMAs (K = 32 each) per unit
       int g = 0;                                 // global unit counter
+      int stage = 0;                             // stage of the current 128-K step, and its phase
+      uint32_t phase = 0;
       bool ok = true;
       const long long c_start = kProf ? clock64() : 0;
       long long c_pe = 0, c_full = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        for (int j = 0; j < KB * U; ++j, ++g) {
-          if ((g & 1) != me) continue;
-          const int sg = g / U;                  // the stage's global index
-          const int stage = sg % kStages;
-          const long long tm0 = kProf ? clock64() : 0;
-          if (lane == 0) ok = mbar_wait(&full[stage], (sg / kStages) & 1, st, s_abort, kSiteFull);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          const long long tm1 = kProf ? clock64() : 0;
-          if (g >= 2) named_sync(kBarFree0 + me, kBarThreads);
-          if (__any_sync(0xffffffffu, *s_abort != 0)) { ok = false; break; }
-          if (kProf) { c_full += tm1 - tm0; c_pe += clock64() - tm1; }
-          if (lane == 0) {
+        for (int kb = 0; kb < KB && ok; ++kb) {
+          for (int h = 0; h < U; ++h, ++g) {
+            if ((g & 1) != me) continue;
+            const long long tm0 = kProf ? clock64() : 0;
+            if (!mbar_wait(&full[stage], phase, st, s_abort, kSiteFull)) { ok = false; break; }
+            const long long tm1 = kProf ? clock64() : 0;
+            if (!mbar_wait(&pempty[me], ((g >> 1) & 1) ^ 1, st, s_abort, kSitePEmpty)) { ok = false; break; }
+            if (kProf) { c_full += tm1 - tm0; c_pe += clock64() - tm1; }
             tc_fence_after();
-            const int k0 = (g - sg * U) * per;   // first 32-K slice of this unit
             const uint32_t a0 = smem_u32(smem + SmemLayout::tok + stage * kTokBytes);
             const uint32_t b0 = smem_u32(smem + SmemLayout::wgt + stage * kWgtBytes);
-            for (int kk = 0; kk < per; ++kk)
-              tc_mma_f8f6f4(tmem + me * kBN, make_smem_desc(a0 + (k0 + kk) * 32, 16, 1024, 2),
-                            make_smem_desc(b0 + (k0 + kk) * 32, 16, 1024, 2), make_idesc(), kk != 0);
+            const uint32_t acc = tmem + me * kBN;
+            if (U == 1) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f8f6f4(acc, make_smem_desc(a0 + kk * 32, 16, 1024, 2), make_smem_desc(b0 + kk * 32, 16, 1024, 2),
+                              make_idesc(), kk != 0);
+            } else {                             // the unit's 64-K half: two of the stage's four 32-K slices
+              const uint32_t k0 = h * 64;
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk)
+                tc_mma_f8f6f4(acc, make_smem_desc(a0 + k0 + kk * 32, 16, 1024, 2),
+                              make_smem_desc(b0 + k0 + kk * 32, 16, 1024, 2), make_idesc(), kk != 0);
+            }
             tc_commit(&empty[stage]);
           }
-          __syncwarp();
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (lane == 0) {
-        // every MMA these threads issued has completed before TMEM is freed
-        tc_commit(drain);
-        mbar_wait_drain(drain, 0, st, kSiteDrainMma);
-        if (kProf && me == 0) {
-          args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
-          args.prof[blockIdx.x * 8 + 1] = c_pe;
-          args.prof[blockIdx.x * 8 + 2] = c_full;
-          args.prof[blockIdx.x * 8 + 6] = g;
-        }
+      // every MMA these threads issued has completed before TMEM is freed
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, st, kSiteDrainMma);
+      if (kProf && me == 0) {
+        args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
+        args.prof[blockIdx.x * 8 + 1] = c_pe;
+        args.prof[blockIdx.x * 8 + 2] = c_full;
+        args.prof[blockIdx.x * 8 + 6] = g;
       }
     } else if (warp == 14) {
       // Unit g's commit, passed on to the epilogue through barrier kBarDone0 + (g & 1).
@@ -359,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pb = g & 1;
         const long long tw0 = kProf ? clock64() : 0;
         named_sync(kBarDone0 + pb, kBarThreads);   // warp 14 saw the unit's commit
-        if (__any_sync(0xffffffffu, *s_abort != 0)) return false;   // warp-uniform: the barriers are per warp
+        if (__any_sync(0xffffffffu, *s_abort != 0)) {   // warp-uniform: the barriers count whole warps
+          ++g;                                          // this unit's barrier is passed
+          return false;
+        }
         const long long tw1 = kProf ? clock64() : 0;
         tc_fence_after();
         const float f0 = sx * w0;
@@ -383,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(tb + c1 + 32, v);
         tmem_ld_wait();
         tc_fence_before();
-        named_arrive(kBarFree0 + pb, kBarThreads);   // the buffer may take unit g + 2
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[pb]);     // the buffer may take unit g + 2
 #pragma unroll
         for (int j = 0; j < 32; ++j) acc1[32 + j] = fmaf(__uint_as_float(v[j]), f1, acc1[32 + j]);
         if (kProf) { e_wait += tw1 - tw0; e_promo += clock64() - tw1; }
@@ -521,12 +532,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kProf) e_tail += clock64() - tw2;
     }
-    // after an abort an issuer may wait for the release of a buffer this warpgroup will
-    // never read: one more arrival on each "partial free" barrier lets it see the flag
-    // (an arrival nobody waits for is harmless)
+    // After an abort every epilogue warp still syncs the "unit complete" barrier of
+    // each remaining unit (warp 14 arrives for every unit, so the syncs return at
+    // once): warps that saw the flag at different units all reach the same total,
+    // so none is left waiting for another.
     __syncwarp();
-    named_arrive(kBarFree0, kBarThreads);
-    named_arrive(kBarFree0 + 1, kBarThreads);
+    {
+      const int ntasks = blockIdx.x < total ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+      for (const int units = ntasks * KB * U; g < units; ++g) named_sync(kBarDone0 + (g & 1), kBarThreads);
+    }
     if (kProf && warp == 4 && lane == 0) {
       args.prof[blockIdx.x * 8 + 3] = e_wait;
       args.prof[blockIdx.x * 8 + 4] = e_promo;
@@ -568,6 +582,7 @@ cudaError_t launch_impl(const GemmLaunchF8& g, cudaStream_t s) {
   a.precise = g.precise;
   a.gran = L.act_gran;
   a.exact_div = g.exact_div ? 1 : 0;
+  a.unreachable = (PHASE == 1 && g.unreachable) ? 1 : 0;
   const uint8_t* pool;
   int kdim;
   if (PHASE == 1) {

@@ -159,6 +159,7 @@ struct GemmLaunchF8 {
   float clamp;               // activation clamp of gate and up (+inf: none)
   int precise;               // SwiGLU with expf and the IEEE division instead of the fast-math form
   bool exact_div;            // L1 requant: divide for every code (debug_flags bit 4), not only near a boundary
+  bool unreachable;          // L1: the last stage of each CTA's last task is never loaded (debug_flags bit 2)
 };
 cudaError_t launch_gemm_f8_l1(const GemmLaunchF8& g, cudaStream_t s);
 cudaError_t launch_gemm_f8_l2(const GemmLaunchF8& g, cudaStream_t s);

@@ -71,3 +71,22 @@ def test_host_rejections(M):
         M.forward(dev["x"], dev["x_sf"], dev["topk_idx"], dev["topk_w"], dev["w1"].view(-1)[1:], w1p, dev["w2"],
                   w2p, out, cfg.H, cfg.I, cfg.E, ws, opt)
     assert ei.value.code == M.MM_MOE_ERR_INVALID_ARG
+
+
+def test_f8_unreachable_wait_times_out_and_context_survives(M):
+    """FP8: the last stage of every CTA's last L1 task is never loaded.  The issuer's
+    wait for it runs out, the abort reaches the commit waiter, the epilogue and
+    the other issuer through their named barriers (every phase keeps its count),
+    and the next call on the same context is correct."""
+    cfg = W.Config("f8_ragged", T=300, H=512, I=384, E=5, K=2, variant="f8", seed=25)
+    dev = to_dev(W.make_inputs(cfg, "cpu"))
+    opt = M.options(M.MM_MOE_VARIANT_F8, debug_flags=4, wait_timeout_ms=50)
+    t0 = time.time()
+    out, ws, prep, (code, where) = run_forward(M, cfg, dev, opt)
+    assert code == M.MM_MOE_ERR_TIMEOUT
+    assert where == 202, where          # a stage's data
+    assert time.time() - t0 < 30
+    out2, _, _, (code2, _) = run_forward(M, cfg, dev, M.options(M.MM_MOE_VARIANT_F8), ws=ws, prepared=prep)
+    assert code2 == 0
+    ref, _ = oracle_rows(cfg, dev, np.arange(cfg.T), keep_intermediate=False)
+    check_output(out2.float().cpu().numpy(), ref, "FP8 after timeout")
