@@ -99,8 +99,8 @@ struct SmemLayout {
   static constexpr int amax = wgt + kStages * kWgtBytes;              // [2 tasks][2 halves][128] fp32
   static constexpr int meta = amax + 2 * 2 * 128 * 4;
   static constexpr int bars_after_meta(int E) { return meta + ((2 * E + 1) * 4 + 15) / 16 * 16; }
-  // full[S], empty[S] (one commit per promotion unit: stage free and partial complete), pempty[2], epi, drain
-  static constexpr int nbars = 2 * kStages + 4;
+  // full[S], empty[S] (one commit per promotion unit: stage free and partial complete), pempty[2], epi, drain[2]
+  static constexpr int nbars = 2 * kStages + 5;
   static constexpr int total(int E) { return bars_after_meta(E) + nbars * 8 + 16; }
 };
 static_assert(SmemLayout::total(kMaxE) + 1024 <= 232448, "shared memory budget");
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = bars + kStages;
   uint64_t* pempty = bars + 2 * kStages;   // [2]: buffer read by all eight epilogue warps
   uint64_t* epibar = pempty + 2;
-  uint64_t* drain = epibar + 1;   // the MMA issuers' last commits
+  uint64_t* drain = epibar + 1;   // [2]: each MMA issuer's last commit
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + SmemLayout::nbars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) mbar_init(&pempty[i], 8);
     mbar_init(epibar, 256);
-    mbar_init(drain, 2);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -298,9 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      // every MMA these threads issued has completed before TMEM is freed
-      tc_commit(drain);
-      mbar_wait_drain(drain, 0, st, kSiteDrainMma);
+      // every MMA this thread issued has completed before TMEM is freed (its own
+      // barrier: the other issuer may still be waiting out a deadline)
+      tc_commit(&drain[me]);
+      mbar_wait_drain(&drain[me], 0, st, kSiteDrainMma);
       if (kProf && me == 0) {
         args.prof[blockIdx.x * 8 + 0] = clock64() - c_start;
         args.prof[blockIdx.x * 8 + 1] = c_pe;

@@ -84,7 +84,9 @@ def test_f8_unreachable_wait_times_out_and_context_survives(M):
     t0 = time.time()
     out, ws, prep, (code, where) = run_forward(M, cfg, dev, opt)
     assert code == M.MM_MOE_ERR_TIMEOUT
-    assert where == 202, where          # a stage's data
+    # the first deadline to pass is the issuer's wait for the stage that is never
+    # loaded (202) or the commit waiter's wait for that unit's MMAs (204)
+    assert where in (202, 204), where
     assert time.time() - t0 < 30
     out2, _, _, (code2, _) = run_forward(M, cfg, dev, M.options(M.MM_MOE_VARIANT_F8), ws=ws, prepared=prep)
     assert code2 == 0
