@@ -63,26 +63,43 @@ __global__ void ep_pull_kernel(const int4* __restrict__ meta, int64_t rows, int 
   }
 }
 
-// One warp per token: out[t] = bf16(sum over k of its pairs' bf16 outputs at
-// their owners), the sum in fp32 in k order; 8 bf16 (16 bytes) a lane a step.
+// One warp per (token, 1024-column part): out[t] = bf16(sum over k of its pairs'
+// bf16 outputs at their owners), the sum in fp32 in k order; 8 bf16 (16 bytes) a
+// lane a step.  Lane k < K resolves slot k's source row once; the row addresses
+// are then broadcast, so every step issues its K independent loads back to back.
+constexpr int kCombinePart = 128;   // 16-byte chunks (1024 bf16 columns) a warp sums
+
 __global__ void ep_combine_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ send_row, int T,
                                   int K, int E, int Eloc, int H, const void* const* __restrict__ peer_out,
                                   __nv_bfloat16* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t t = warp0; t < T; t += nwarps) {
-    for (int c = lane; c < H / 8; c += 32) {
+  const int parts = (H / 8 + kCombinePart - 1) / kCombinePart;
+  for (int64_t w = warp0; w < static_cast<int64_t>(T) * parts; w += nwarps) {
+    const int64_t t = w / parts;
+    const int c0 = static_cast<int>(w - t * parts) * kCombinePart;
+    const int c1 = c0 + kCombinePart < H / 8 ? c0 + kCombinePart : H / 8;
+    const uint4* mine = nullptr;
+    if (lane < K) {
+      const int e = idx[t * K + lane];
+      const int row = send_row[t * K + lane];
+      if (e >= 0 && e < E && row >= 0)
+        mine = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(peer_out[e / Eloc]) +
+                                              static_cast<int64_t>(row) * H);
+    }
+    const uint4* src[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k)
+      src[k] = reinterpret_cast<const uint4*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(mine), k));
+    for (int c = c0 + lane; c < c1; c += 32) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int k = 0; k < K; ++k) {
-        const int e = idx[t * K + k];
-        const int row = send_row[t * K + k];
-        if (e < 0 || e >= E || row < 0) continue;
-        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(peer_out[e / Eloc]) +
-                                   static_cast<int64_t>(row) * H;
-        const uint4 v = reinterpret_cast<const uint4*>(src)[c];
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        if (k >= K || !src[k]) continue;
+        const uint4 v = src[k][c];
         const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -212,7 +229,8 @@ int mm_moe_ep_combine(const int32_t* topk_idx, const int32_t* send_row, int T, i
   if (ep_shape(T, K, E, N) || H <= 0 || H % 128 || !peer_out) return MM_MOE_ERR_INVALID_ARG;
   if (T == 0) return MM_MOE_OK;
   if (!topk_idx || !send_row || !out || !aligned16(out)) return MM_MOE_ERR_INVALID_ARG;
-  ep_combine_kernel<<<grid_for(T, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  const int64_t warps = static_cast<int64_t>(T) * ((H / 8 + 127) / 128);
+  ep_combine_kernel<<<grid_for(warps, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       topk_idx, send_row, T, K, E, E / N, H, peer_out, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError() == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
 }
