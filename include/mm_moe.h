@@ -331,6 +331,28 @@ int mm_moe_ep_pull(const int32_t* meta, int64_t rows, int K, int H, int variant,
 int mm_moe_ep_combine(const int32_t* topk_idx, const int32_t* send_row, int T, int K, int E, int N, int H,
                       const void* const* peer_out, void* out, void* stream);
 
+/* Push form of step 5 (the pages' combine, Atlas §9): every owner stores each
+ * received row's bf16 output (out_recv [rows, H], its local forward's output) into
+ * the source rank's partial buffer at the pair's place: peer_partials[r] is rank
+ * r's bf16 [T_r * K, H] (row t*K + k).  meta is the owner's receive metadata
+ * (step 3).  Rows of masked slots are never written. */
+int mm_moe_ep_push_out(const int32_t* meta, int64_t rows, int H, const void* out_recv,
+                       void* const* peer_partials, void* stream);
+
+/* After every owner's push (a barrier): out[t] = bf16(sum over k of partials[t*K + k]
+ * for the slots with 0 <= topk_idx < E), the sum in fp32 in k order; 0 for a token
+ * with no valid slot.  partials: this rank's bf16 [T*K, H]. */
+int mm_moe_ep_combine_local(const int32_t* topk_idx, int T, int K, int E, int H, const void* partials,
+                            void* out, void* stream);
+
+/* The pages' num_tokens_bound contract (PR #440): with every rank's token count at
+ * most num_tokens_bound (the same bound on every rank), a rank receives at most
+ * *rows = N * num_tokens_bound * min(K, E/N) rows (each token sends one row to each
+ * distinct expert it picks, at most E/N of them on one rank), so receive buffers of
+ * that size can be allocated once, alike on every rank.  mm_moe_ep_plan refuses a
+ * receive count above the capacity it is given. */
+int mm_moe_ep_recv_capacity(int num_tokens_bound, int K, int E, int N, int64_t* rows);
+
 /* Human-readable name of a return code. */
 const char* mm_moe_status_string(int code);
 

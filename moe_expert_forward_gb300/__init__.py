@@ -32,7 +32,7 @@ EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_
            "mm_moe_forward", "mm_moe_dispatch_scratch_size", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
            "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region",
            "mm_moe_dispatch_noalloc", "mm_moe_ep_count", "mm_moe_ep_plan", "mm_moe_ep_push_meta", "mm_moe_ep_pull",
-           "mm_moe_ep_combine"]
+           "mm_moe_ep_combine", "mm_moe_ep_push_out", "mm_moe_ep_combine_local", "mm_moe_ep_recv_capacity"]
 
 
 class mm_moe_options(ctypes.Structure):
@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
             "mm_moe_ep_push_meta": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
             "mm_moe_ep_pull": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
             "mm_moe_ep_combine": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+            "mm_moe_ep_push_out": (_I, [_P, _I64, _I, _P, _P, _P]),
+            "mm_moe_ep_combine_local": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+            "mm_moe_ep_recv_capacity": (_I, [_I, _I, _I, _I, ctypes.POINTER(_I64)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -293,10 +296,11 @@ def mm_moe_ep_count(topk_idx, T, K, E, counts, stream) -> int:
     return lib().mm_moe_ep_count(topk_idx, T, K, E, counts, stream)
 
 
-def mm_moe_ep_plan(counts_all, topk_idx, T, K, E, N, rank, recv_expert=True):
+def mm_moe_ep_plan(counts_all, topk_idx, T, K, E, N, rank, recv_expert=True, recv_capacity=None):
     """Host planning (numpy in, numpy out): counts_all int32 [N, E], topk_idx int32
     [T, K] of this rank.  Returns (send_row int32 [T*K], recv_rows, recv_expert
-    int32 [recv_rows] or None)."""
+    int32 [recv_rows] or None).  recv_capacity (e.g. mm_moe_ep_recv_capacity of the
+    token bound): the library refuses a receive count above it."""
     import numpy as np
     counts_all = np.ascontiguousarray(counts_all, dtype=np.int32)
     topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
@@ -305,11 +309,14 @@ def mm_moe_ep_plan(counts_all, topk_idx, T, K, E, N, rank, recv_expert=True):
     _check(lib().mm_moe_ep_plan(counts_all.ctypes.data, topk_idx.ctypes.data, T, K, E, N, rank,
                                 send_row.ctypes.data, ctypes.byref(rows), None, 0), "mm_moe_ep_plan")
     rex = None
-    if recv_expert:
-        rex = np.empty(max(rows.value, 1), dtype=np.int32)
+    if recv_expert or recv_capacity is not None:
+        cap = rows.value if recv_capacity is None else int(recv_capacity)
+        rex = np.empty(max(cap, rows.value, 1), dtype=np.int32)
+        if recv_capacity is not None:
+            rex = rex[:max(cap, 1)]
         _check(lib().mm_moe_ep_plan(counts_all.ctypes.data, topk_idx.ctypes.data, T, K, E, N, rank,
-                                    send_row.ctypes.data, ctypes.byref(rows), rex.ctypes.data, rex.size),
-               "mm_moe_ep_plan")
+                                    send_row.ctypes.data, ctypes.byref(rows), rex.ctypes.data,
+                                    rex.size if recv_capacity is None else int(recv_capacity)), "mm_moe_ep_plan")
         rex = rex[:rows.value]
     return send_row[:T * K], rows.value, rex
 
@@ -325,3 +332,17 @@ def mm_moe_ep_pull(meta, rows, K, H, variant, peer_x, peer_x_sf, x_recv, x_sf_re
 
 def mm_moe_ep_combine(topk_idx, send_row, T, K, E, N, H, peer_out, out, stream) -> int:
     return lib().mm_moe_ep_combine(topk_idx, send_row, T, K, E, N, H, peer_out, out, stream)
+
+
+def mm_moe_ep_push_out(meta, rows, H, out_recv, peer_partials, stream) -> int:
+    return lib().mm_moe_ep_push_out(meta, rows, H, out_recv, peer_partials, stream)
+
+
+def mm_moe_ep_combine_local(topk_idx, T, K, E, H, partials, out, stream) -> int:
+    return lib().mm_moe_ep_combine_local(topk_idx, T, K, E, H, partials, out, stream)
+
+
+def mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N) -> int:
+    n = _I64(0)
+    _check(lib().mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N, ctypes.byref(n)), "mm_moe_ep_recv_capacity")
+    return n.value

@@ -14,6 +14,8 @@
 namespace mm {
 namespace {
 
+constexpr int kCombinePart = 128;   // 16-byte chunks (1024 bf16 columns) a warp sums
+
 __global__ void ep_count_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int32_t* __restrict__ counts) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -67,8 +69,6 @@ __global__ void ep_pull_kernel(const int4* __restrict__ meta, int64_t rows, int 
 // bf16 outputs at their owners), the sum in fp32 in k order; 8 bf16 (16 bytes) a
 // lane a step.  Lane k < K resolves slot k's source row once; the row addresses
 // are then broadcast, so every step issues its K independent loads back to back.
-constexpr int kCombinePart = 128;   // 16-byte chunks (1024 bf16 columns) a warp sums
-
 __global__ void ep_combine_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ send_row, int T,
                                   int K, int E, int Eloc, int H, const void* const* __restrict__ peer_out,
                                   __nv_bfloat16* __restrict__ out) {
@@ -100,6 +100,61 @@ __global__ void ep_combine_kernel(const int32_t* __restrict__ idx, const int32_t
       for (int k = 0; k < kMaxK; ++k) {
         if (k >= K || !src[k]) continue;
         const uint4 v = src[k][c];
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(p[i]);
+          acc[2 * i] += f.x;
+          acc[2 * i + 1] += f.y;
+        }
+      }
+      uint4 o;
+      __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      reinterpret_cast<uint4*>(out + t * H)[c] = o;
+    }
+  }
+}
+
+// One warp per received row: its bf16 output to the pair's row of the source
+// rank's partial buffer.
+__global__ void ep_push_out_kernel(const int4* __restrict__ meta, int64_t rows, int H,
+                                   const __nv_bfloat16* __restrict__ out_recv, void* const* __restrict__ peer_partials) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t j = warp0; j < rows; j += nwarps) {
+    const int4 m = meta[j];
+    const uint4* src = reinterpret_cast<const uint4*>(out_recv + j * H);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(peer_partials[m.x]) +
+                                          static_cast<int64_t>(m.y) * H);
+    for (int i = lane; i < H / 8; i += 32) dst[i] = src[i];
+  }
+}
+
+// One warp per (token, 1024-column part): the token's K bf16 partials summed in
+// fp32 in k order, rounded once to bf16.
+__global__ void ep_combine_local_kernel(const int32_t* __restrict__ idx, int T, int K, int E, int H,
+                                        const __nv_bfloat16* __restrict__ part, __nv_bfloat16* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int parts = (H / 8 + kCombinePart - 1) / kCombinePart;
+  for (int64_t w = warp0; w < static_cast<int64_t>(T) * parts; w += nwarps) {
+    const int64_t t = w / parts;
+    const int c0 = static_cast<int>(w - t * parts) * kCombinePart;
+    const int c1 = c0 + kCombinePart < H / 8 ? c0 + kCombinePart : H / 8;
+    const int e_mine = lane < K ? idx[t * K + lane] : -1;
+    const uint32_t valid = __ballot_sync(0xffffffffu, e_mine >= 0 && e_mine < E);
+    for (int c = c0 + lane; c < c1; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kMaxK; ++k) {
+        if (k >= K || !((valid >> k) & 1u)) continue;
+        const uint4 v = reinterpret_cast<const uint4*>(part + (t * K + k) * H)[c];
         const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -233,6 +288,34 @@ int mm_moe_ep_combine(const int32_t* topk_idx, const int32_t* send_row, int T, i
   ep_combine_kernel<<<grid_for(warps, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
       topk_idx, send_row, T, K, E, E / N, H, peer_out, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError() == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_ep_push_out(const int32_t* meta, int64_t rows, int H, const void* out_recv,
+                       void* const* peer_partials, void* stream) {
+  if (rows < 0 || H <= 0 || H % 128) return MM_MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MM_MOE_OK;
+  if (!meta || !out_recv || !peer_partials || !aligned16(meta) || !aligned16(out_recv)) return MM_MOE_ERR_INVALID_ARG;
+  ep_push_out_kernel<<<grid_for(rows, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const int4*>(meta), rows, H, static_cast<const __nv_bfloat16*>(out_recv), peer_partials);
+  return cudaGetLastError() == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_ep_combine_local(const int32_t* topk_idx, int T, int K, int E, int H, const void* partials,
+                            void* out, void* stream) {
+  if (T < 0 || K <= 0 || K > kMaxK || E <= 0 || H <= 0 || H % 128) return MM_MOE_ERR_INVALID_ARG;
+  if (T == 0) return MM_MOE_OK;
+  if (!topk_idx || !partials || !out || !aligned16(partials) || !aligned16(out)) return MM_MOE_ERR_INVALID_ARG;
+  const int64_t warps = static_cast<int64_t>(T) * ((H / 8 + kCombinePart - 1) / kCombinePart);
+  ep_combine_local_kernel<<<grid_for(warps, 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      topk_idx, T, K, E, H, static_cast<const __nv_bfloat16*>(partials), static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError() == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_ep_recv_capacity(int num_tokens_bound, int K, int E, int N, int64_t* rows) {
+  if (!rows || num_tokens_bound < 0 || ep_shape(0, K, E, N)) return MM_MOE_ERR_INVALID_ARG;
+  const int per = K < E / N ? K : E / N;
+  *rows = static_cast<int64_t>(N) * num_tokens_bound * per;
+  return MM_MOE_OK;
 }
 
 }  // extern "C"

@@ -9,8 +9,11 @@ combine; DeepGEMM PR #440 "How it works").  The kernels read and write peers'
 buffers through device tables of their addresses; the exchange of the counts and
 the barriers are host collectives, so no kernel waits on another rank.
 
-`plan_distributed` is the host side of a multi-process run (torch.distributed:
-an all-gather of the counts).  `forward_on_one_device` runs N ranks whose buffers
+The combine comes in the pages' push form (each owner stores every received row's
+bf16 output into the token's rank, which then sums its slots locally) and a pull
+form (each rank reads its slots' outputs from their owners); both give the same
+bits.  `plan_distributed` is the host side of a multi-process run
+(torch.distributed: an all-gather of the counts).  `forward_on_one_device` runs N ranks whose buffers
 all live on one GPU, step by step from the host, which checks the whole data path
 on a single device; a multi-GPU run differs only in where the peers' buffers live.
 """
@@ -20,8 +23,9 @@ from typing import List, Optional, Sequence
 
 import numpy as np
 
-from . import (MM_MOE_VARIANT_MX, MMError, _check, alloc_workspace, forward, mm_moe_ep_combine, mm_moe_ep_count,
-               mm_moe_ep_plan, mm_moe_ep_pull, mm_moe_ep_push_meta, options, prepare_weights, sync_status)
+from . import (MM_MOE_VARIANT_MX, MMError, _check, alloc_workspace, forward, mm_moe_ep_combine,
+               mm_moe_ep_combine_local, mm_moe_ep_count, mm_moe_ep_plan, mm_moe_ep_pull, mm_moe_ep_push_meta,
+               mm_moe_ep_push_out, mm_moe_ep_recv_capacity, options, prepare_weights, sync_status)
 
 
 def host_counts(topk_idx: np.ndarray, E: int) -> np.ndarray:
@@ -63,10 +67,13 @@ class RankState:
         self.H = x.shape[1]
 
 
-def forward_on_one_device(states: List[RankState], w1, w1_sf, w2, w2_sf, I: int, opt=None, stream=None):
+def forward_on_one_device(states: List[RankState], w1, w1_sf, w2, w2_sf, I: int, opt=None, stream=None,
+                          combine: str = "push", num_tokens_bound: Optional[int] = None):
     """Run the EP forward for every rank in `states` (buffers on one device).
     w1 / w1_sf / w2 / w2_sf hold all E experts in the layouts of mm_moe.h; rank r
-    uses experts [r*E/N, (r+1)*E/N).  Returns the per-rank bf16 outputs [T_r, H]
+    uses experts [r*E/N, (r+1)*E/N).  combine: "push" (the pages' form) or "pull".
+    num_tokens_bound: receive buffers sized once by mm_moe_ep_recv_capacity (every
+    rank's T must be within the bound).  Returns the per-rank bf16 outputs [T_r, H]
     and the per-rank plans (send_row, recv_rows, recv_expert)."""
     import torch
     N = len(states)
@@ -84,11 +91,15 @@ def forward_on_one_device(states: List[RankState], w1, w1_sf, w2, w2_sf, I: int,
     counts_all = torch.stack(counts).cpu().numpy()
     # 2. plans and receive buffers
     plans = []
+    cap = None
+    if num_tokens_bound is not None:
+        cap = mm_moe_ep_recv_capacity(num_tokens_bound, states[0].K, E, N)
     for st in states:
-        send_row, rows, rex = mm_moe_ep_plan(counts_all, st.topk_idx.cpu().numpy(), st.T, st.K, E, N, st.rank)
+        send_row, rows, rex = mm_moe_ep_plan(counts_all, st.topk_idx.cpu().numpy(), st.T, st.K, E, N, st.rank,
+                                             recv_capacity=cap)
         st.send_row = torch.from_numpy(np.ascontiguousarray(send_row)).to(dev)
         st.rows = rows
-        st.meta = torch.zeros(max(rows, 1), 4, dtype=torch.int32, device=dev)
+        st.meta = torch.zeros(max(rows if cap is None else cap, 1), 4, dtype=torch.int32, device=dev)
         plans.append((send_row, rows, rex))
     # 3. metadata pushed into the owners' buffers
     peer_meta = pointer_table([st.meta for st in states], dev)
@@ -122,13 +133,27 @@ def forward_on_one_device(states: List[RankState], w1, w1_sf, w2, w2_sf, I: int,
         if code != 0:
             raise MMError(code, f"rank {st.rank} local forward (site {where})")
     torch.cuda.synchronize()                                  # barrier
-    # 5. combine from the owners' outputs
-    peer_out = pointer_table([st.out_recv for st in states], dev)
+    # 5. combine
     outs = []
-    for st in states:
-        out = torch.empty(st.T, H, dtype=torch.bfloat16, device=dev)
-        _check(mm_moe_ep_combine(st.topk_idx.data_ptr(), st.send_row.data_ptr(), st.T, st.K, E, N, H,
-                                 peer_out.data_ptr(), out.data_ptr(), s), "mm_moe_ep_combine")
-        outs.append(out)
+    if combine == "push":
+        # each owner stores its rows' outputs at the pairs' places in the token ranks
+        parts = [torch.empty(max(st.T * st.K, 1), H, dtype=torch.bfloat16, device=dev) for st in states]
+        peer_part = pointer_table(parts, dev)
+        for st in states:
+            _check(mm_moe_ep_push_out(st.meta.data_ptr(), st.rows, H, st.out_recv.data_ptr(), peer_part.data_ptr(), s),
+                   "mm_moe_ep_push_out")
+        torch.cuda.synchronize()                              # barrier
+        for st, part in zip(states, parts):
+            out = torch.empty(st.T, H, dtype=torch.bfloat16, device=dev)
+            _check(mm_moe_ep_combine_local(st.topk_idx.data_ptr(), st.T, st.K, E, H, part.data_ptr(), out.data_ptr(),
+                                           s), "mm_moe_ep_combine_local")
+            outs.append(out)
+    else:
+        peer_out = pointer_table([st.out_recv for st in states], dev)
+        for st in states:
+            out = torch.empty(st.T, H, dtype=torch.bfloat16, device=dev)
+            _check(mm_moe_ep_combine(st.topk_idx.data_ptr(), st.send_row.data_ptr(), st.T, st.K, E, N, H,
+                                     peer_out.data_ptr(), out.data_ptr(), s), "mm_moe_ep_combine")
+            outs.append(out)
     torch.cuda.synchronize()
     return outs, plans

@@ -157,3 +157,21 @@ def test_two_gloo_ranks_exchange_counts_and_metadata(M):
         assert np.array_equal(gpair, r["src"][first[rank] + np.arange(nrows)])
         assert np.array_equal(rex, idx_all.reshape(-1)[gpair] - rank * Eloc)
         assert np.array_equal(meta[:, 3].view(np.float32), w_all.reshape(-1)[gpair])
+
+
+def test_recv_capacity_bounds_every_routing(M):
+    """num_tokens_bound: N * bound * min(K, E/N) rows cover the worst routing (every
+    token of every rank picks as many of one rank's experts as it can); the plan
+    refuses a receive count above the capacity it is given."""
+    assert M.mm_moe_ep_recv_capacity(64, 6, 256, 8) == 8 * 64 * 6
+    assert M.mm_moe_ep_recv_capacity(64, 6, 16, 8) == 8 * 64 * 2       # 2 experts a rank
+    N, T, K, E = 2, 16, 3, 8
+    Eloc = E // N
+    worst = [np.tile(np.arange(K, dtype=np.int32), (T, 1)) for _ in range(N)]   # all pairs to rank 0
+    counts_all = np.stack([np.bincount(w.reshape(-1), minlength=E) for w in worst]).astype(np.int32)
+    cap = M.mm_moe_ep_recv_capacity(T, K, E, N)
+    _, rows, _ = M.mm_moe_ep_plan(counts_all, worst[0], T, K, E, N, 0, recv_capacity=cap)
+    assert rows == N * T * K == cap                      # K <= E/N: the bound is reached
+    small = M.mm_moe_ep_recv_capacity(T // 2, K, E, N)  # a bound below the ranks' token counts
+    with pytest.raises(M.MMError):
+        M.mm_moe_ep_plan(counts_all, worst[0], T, K, E, N, 0, recv_capacity=small)

@@ -23,7 +23,7 @@ def M():
     return M
 
 
-def _run(M, cfg, N, mask=0.0, all_to_rank0=False):
+def _run(M, cfg, N, mask=0.0, all_to_rank0=False, combine="push", bound=None):
     from moe_expert_forward_gb300 import ep
     inp = W.make_inputs(cfg, "cpu")                     # all ranks' tokens, rank-major
     g = torch.Generator().manual_seed(cfg.seed)
@@ -38,7 +38,8 @@ def _run(M, cfg, N, mask=0.0, all_to_rank0=False):
     states = [ep.RankState(r, dev["x"][r * Tr:(r + 1) * Tr].contiguous(), dev["x_sf"][r * Tr:(r + 1) * Tr].contiguous(),
                            dev["topk_idx"][r * Tr:(r + 1) * Tr].contiguous(),
                            dev["topk_w"][r * Tr:(r + 1) * Tr].contiguous(), cfg.E, N, variant) for r in range(N)]
-    outs, plans = ep.forward_on_one_device(states, dev["w1"], dev["w1_sf"], dev["w2"], dev["w2_sf"], cfg.I)
+    outs, plans = ep.forward_on_one_device(states, dev["w1"], dev["w1_sf"], dev["w2"], dev["w2_sf"], cfg.I,
+                                           combine=combine, num_tokens_bound=bound)
     got = torch.cat(outs)
     # single GPU, bf16 partials, all tokens together
     single, _, _, (code, _) = run_forward(M, cfg, dev, M.options(variant, partials_bf16=1))
@@ -57,6 +58,16 @@ def test_ep_matches_oracle_and_single_gpu(M, cfg, N):
     ref, _ = oracle_rows(cfg, dev, np.arange(cfg.T), keep_intermediate=False, partials_bf16=True)
     check_output(got.float().cpu().numpy(), ref, f"{cfg.name} EP x{N}")
     assert torch.equal(got, single)
+
+
+@pytest.mark.parametrize("N", [2, 4])
+def test_ep_pull_combine_equals_push(M, N):
+    """The pull form of the combine (each rank reads its slots from the owners) and
+    receive buffers sized by the token bound give the same bits as the push form."""
+    cfg = CFGS[0].with_(seed=84)
+    got_pull, single, _, _ = _run(M, cfg, N, combine="pull", bound=cfg.T // N)
+    got_push, _, _, _ = _run(M, cfg, N, combine="push")
+    assert torch.equal(got_pull, got_push) and torch.equal(got_push, single)
 
 
 def test_ep_masked_slots_and_idle_ranks(M):
