@@ -262,7 +262,8 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
  *             error); swapped and paired kernels 121-152 likewise;
  *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 203 a free
  *             partial buffer, 204 a finished partial (the commit waiter), 205
- *             the epilogue's amax rendezvous, 211 / 212 the exit drains. */
+ *             the epilogue's amax rendezvous, 211 / 212 the exit drains;
+ *   EP        301 a cross-rank barrier (mm_moe_ep_barrier's own status word). */
 int mm_moe_sync_status(const void* workspace, void* stream, int* where);
 
 /* ---------------------------------------------------------------------------
@@ -352,6 +353,26 @@ int mm_moe_ep_combine_local(const int32_t* topk_idx, int T, int K, int E, int H,
  * that size can be allocated once, alike on every rank.  mm_moe_ep_plan refuses a
  * receive count above the capacity it is given. */
 int mm_moe_ep_recv_capacity(int num_tokens_bound, int K, int E, int N, int64_t* rows);
+
+/* Bounded cross-rank barrier for the EP steps (the pages' NVLink barrier,
+ * llm-infra-atlas "07 · MegaMoE" §10), an alternative to a host barrier:
+ * peer_flags is a device array of N pointers to each rank's uint32 [N] flag array
+ * (zeroed once at allocation, peer-accessible); `epoch` must grow by at least one
+ * per call.  The kernel stores epoch into slot `rank` of every rank's array, then
+ * waits until all N slots of its own array have reached epoch.  After timeout_ms
+ * (0: 2000) it records MM_MOE_ERR_TIMEOUT in status (device int32[4]; [1] = 301,
+ * [2] = the first rank missing) and returns, so a lost rank never hangs the GPU.
+ * N <= 64. */
+int mm_moe_ep_barrier(void* const* peer_flags, int N, int rank, uint32_t epoch, unsigned timeout_ms, int32_t* status,
+                      void* stream);
+
+/* Every rank's barrier in one cooperative launch on one device (block r is rank
+ * r), for a device that holds all ranks' flag arrays; ranks whose bit is set in
+ * `absent` skip theirs.  This is how the barrier is exercised on one GPU without
+ * separate launches that wait on one another.  MM_MOE_ERR_UNSUPPORTED when the
+ * device cannot hold N co-resident blocks. */
+int mm_moe_ep_barrier_ranks(void* const* peer_flags, int N, uint32_t epoch, unsigned timeout_ms, uint64_t absent,
+                            int32_t* status, void* stream);
 
 /* Human-readable name of a return code. */
 const char* mm_moe_status_string(int code);

@@ -32,7 +32,8 @@ EXPORTS = ["mm_moe_default_options", "mm_moe_workspace_size", "mm_moe_weight_sf_
            "mm_moe_forward", "mm_moe_dispatch_scratch_size", "mm_moe_dispatch", "mm_moe_read_routing", "mm_moe_read_intermediate",
            "mm_moe_sync_status", "mm_moe_status_string", "mm_moe_workspace_region",
            "mm_moe_dispatch_noalloc", "mm_moe_ep_count", "mm_moe_ep_plan", "mm_moe_ep_push_meta", "mm_moe_ep_pull",
-           "mm_moe_ep_combine", "mm_moe_ep_push_out", "mm_moe_ep_combine_local", "mm_moe_ep_recv_capacity"]
+           "mm_moe_ep_combine", "mm_moe_ep_push_out", "mm_moe_ep_combine_local", "mm_moe_ep_recv_capacity",
+           "mm_moe_ep_barrier", "mm_moe_ep_barrier_ranks"]
 
 
 class mm_moe_options(ctypes.Structure):
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
             "mm_moe_ep_push_out": (_I, [_P, _I64, _I, _P, _P, _P]),
             "mm_moe_ep_combine_local": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
             "mm_moe_ep_recv_capacity": (_I, [_I, _I, _I, _I, ctypes.POINTER(_I64)]),
+            "mm_moe_ep_barrier": (_I, [_P, _I, _I, ctypes.c_uint32, ctypes.c_uint, _P, _P]),
+            "mm_moe_ep_barrier_ranks": (_I, [_P, _I, ctypes.c_uint32, ctypes.c_uint, ctypes.c_uint64, _P, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -346,3 +349,11 @@ def mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N) -> int:
     n = _I64(0)
     _check(lib().mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N, ctypes.byref(n)), "mm_moe_ep_recv_capacity")
     return n.value
+
+
+def mm_moe_ep_barrier(peer_flags, N, rank, epoch, timeout_ms, status, stream) -> int:
+    return lib().mm_moe_ep_barrier(peer_flags, N, rank, epoch, timeout_ms, status, stream)
+
+
+def mm_moe_ep_barrier_ranks(peer_flags, N, epoch, timeout_ms, absent, status, stream) -> int:
+    return lib().mm_moe_ep_barrier_ranks(peer_flags, N, epoch, timeout_ms, absent, status, stream)

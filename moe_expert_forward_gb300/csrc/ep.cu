@@ -10,11 +10,13 @@
 #include <vector>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mm {
 namespace {
 
 constexpr int kCombinePart = 128;   // 16-byte chunks (1024 bf16 columns) a warp sums
+constexpr int kSiteEpBarrier = 301;  // status site of a cross-rank barrier that ran out
 
 __global__ void ep_count_kernel(const int32_t* __restrict__ idx, int64_t n, int E, int32_t* __restrict__ counts) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -172,6 +174,49 @@ __global__ void ep_combine_local_kernel(const int32_t* __restrict__ idx, int T, 
   }
 }
 
+// Cross-rank barrier (the pages' NVLink barrier, llm-infra-atlas "07 · MegaMoE"
+// §10), bounded: rank `rank` stores `epoch` into slot `rank` of every rank's flag
+// array (system-scope release), then waits until every slot of its own array has
+// reached `epoch` (system-scope acquire) or the deadline passes, which it records
+// as MM_MOE_ERR_TIMEOUT with site 301 and the first missing rank.  Epochs only
+// grow, so the flags are never reset.  One thread does the work.
+__device__ bool ep_barrier_body(uint32_t* const* peer_flags, int N, int rank, uint32_t epoch, uint64_t timeout_ns,
+                                int32_t* status) {
+  for (int r = 0; r < N; ++r)
+    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(peer_flags[r] + rank), "r"(epoch) : "memory");
+  const uint32_t* mine = peer_flags[rank];
+  const uint64_t t0 = globaltimer();
+  for (int r = 0; r < N; ++r) {
+    for (;;) {
+      uint32_t v;
+      asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(mine + r) : "memory");
+      if (static_cast<int32_t>(v - epoch) >= 0) break;
+      if (globaltimer() - t0 > timeout_ns) {
+        if (atomicCAS(status, 0, MM_MOE_ERR_TIMEOUT) == 0) {
+          status[1] = kSiteEpBarrier;
+          status[2] = r;
+        }
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+__global__ void ep_barrier_kernel(uint32_t* const* peer_flags, int N, int rank, uint32_t epoch, uint64_t timeout_ns,
+                                  int32_t* status) {
+  if (threadIdx.x == 0) ep_barrier_body(peer_flags, N, rank, epoch, timeout_ns, status);
+}
+
+// All ranks' barriers in one launch on one device: block r runs rank r's barrier
+// (the blocks are co-resident: a cooperative launch).  Ranks set in `absent`
+// skip theirs, which makes the others' waits run out.
+__global__ void ep_barrier_ranks_kernel(uint32_t* const* peer_flags, int N, uint32_t epoch, uint64_t timeout_ns,
+                                        uint64_t absent, int32_t* status) {
+  const int rank = blockIdx.x;
+  if (threadIdx.x == 0 && !((absent >> rank) & 1)) ep_barrier_body(peer_flags, N, rank, epoch, timeout_ns, status);
+}
+
 int grid_for(int64_t items, int per_block) {
   int64_t b = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(dev_info().sms) * 8;
@@ -316,6 +361,30 @@ int mm_moe_ep_recv_capacity(int num_tokens_bound, int K, int E, int N, int64_t* 
   const int per = K < E / N ? K : E / N;
   *rows = static_cast<int64_t>(N) * num_tokens_bound * per;
   return MM_MOE_OK;
+}
+
+int mm_moe_ep_barrier(void* const* peer_flags, int N, int rank, uint32_t epoch, unsigned timeout_ms, int32_t* status,
+                      void* stream) {
+  if (!peer_flags || !status || N <= 0 || N > 64 || rank < 0 || rank >= N) return MM_MOE_ERR_INVALID_ARG;
+  const uint64_t ns = static_cast<uint64_t>(timeout_ms ? timeout_ms : 2000) * 1000000ull;
+  ep_barrier_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<uint32_t* const*>(peer_flags), N, rank, epoch, ns, status);
+  return cudaGetLastError() == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+}
+
+int mm_moe_ep_barrier_ranks(void* const* peer_flags, int N, uint32_t epoch, unsigned timeout_ms, uint64_t absent,
+                            int32_t* status, void* stream) {
+  if (!peer_flags || !status || N <= 0 || N > 64) return MM_MOE_ERR_INVALID_ARG;
+  int coop = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop || N > dev_info().sms)
+    return MM_MOE_ERR_UNSUPPORTED;
+  const uint64_t ns = static_cast<uint64_t>(timeout_ms ? timeout_ms : 2000) * 1000000ull;
+  uint32_t* const* flags = reinterpret_cast<uint32_t* const*>(peer_flags);
+  void* kargs[] = {const_cast<uint32_t* const**>(&flags), &N, &epoch, const_cast<uint64_t*>(&ns), &absent, &status};
+  const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ep_barrier_ranks_kernel), dim3(N),
+                                                    dim3(32), kargs, 0, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
 }
 
 }  // extern "C"

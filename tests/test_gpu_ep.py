@@ -87,3 +87,50 @@ def test_ep_flash_shape(M):
     cfg = W.CONFIGS["flash"]
     got, single, _, _ = _run(M, cfg, 2)
     assert torch.equal(got, single)
+
+
+def _flags(N):
+    """N ranks' flag arrays (uint32 [N] each, zeroed) and the device table of them."""
+    from moe_expert_forward_gb300 import ep
+    arrays = [torch.zeros(N, dtype=torch.int32, device="cuda") for _ in range(N)]
+    return arrays, ep.pointer_table(arrays, "cuda")
+
+
+@pytest.mark.parametrize("N", [2, 4, 8])
+def test_ep_barrier_all_ranks_arrive(M, N):
+    """All ranks' barriers in one cooperative launch (block r is rank r): every
+    flag reaches each epoch in turn and no wait runs out."""
+    arrays, table = _flags(N)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for epoch in (1, 2, 3):
+        assert M.mm_moe_ep_barrier_ranks(table.data_ptr(), N, epoch, 2000, 0, status.data_ptr(), s) == 0
+        torch.cuda.synchronize()
+        assert int(status[0]) == 0
+        assert all(torch.all(a == epoch) for a in arrays)
+
+
+def test_ep_barrier_missing_rank_times_out(M):
+    """Rank 2 of 4 never arrives: the others' waits run out after the deadline and
+    report MM_MOE_ERR_TIMEOUT at site 301, naming rank 2; the context stays usable."""
+    N = 4
+    arrays, table = _flags(N)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert M.mm_moe_ep_barrier_ranks(table.data_ptr(), N, 1, 50, 1 << 2, status.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    assert int(status[0]) == M.MM_MOE_ERR_TIMEOUT and int(status[1]) == 301 and int(status[2]) == 2
+    status.zero_()
+    assert M.mm_moe_ep_barrier_ranks(table.data_ptr(), N, 2, 2000, 0, status.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0
+
+
+def test_ep_barrier_single_rank(M):
+    """The per-rank entry point with one rank: its own arrival completes it."""
+    arrays, table = _flags(1)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert M.mm_moe_ep_barrier(table.data_ptr(), 1, 0, 5, 100, status.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0 and int(arrays[0][0]) == 5
