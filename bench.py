@@ -206,6 +206,8 @@ def run_ours(args, ws_n, rank, local):
         opt.swap_ab = args.swap_ab
     if args.block_m:
         opt.block_m = args.block_m
+    opt.ring_blocks = args.ring_blocks
+    opt.lag_units = args.lag
     if args.x == "bf16":
         # bf16 activations: the gather quantises each row (x_sf is not read)
         inp["x"], inp["x_sf"] = W.make_x_bf16(cfg, dev), None
@@ -376,6 +378,7 @@ def run_ours(args, ws_n, rank, local):
                    "fused_stream": fused, "early_combine": early, "partials": args.partials, "x": args.x,
                    "swap_ab": int(opt.swap_ab), "block_m": int(opt.block_m),
                    "shared_experts": cfg.S, "f8_act_gran": int(opt.f8_act_gran),
+                   "ring_blocks": int(opt.ring_blocks), "lag_units": int(opt.lag_units),
                    "e2e_policy": "copies on streams of their own, two buffer sets (step i+1 in and step i-1 out "
                                  "overlap step i); no L2 flush: every step reads >= 2.5 GB of weights"},
         "tflops": acc["flops"] / (step_ms * 1e-3) / 1e12,
@@ -531,6 +534,10 @@ def main():
                     help="shared experts added to the workload (used by every token with weight 1)")
     ap.add_argument("--f8-gran", type=int, choices=[-1, 0, 64, 128], default=0,
                     help="FP8: intermediate scale width (0: per 128, the library default; -1: the pages' shape rule)")
+    ap.add_argument("--ring-blocks", type=int, default=0,
+                    help="MX fused stream: the intermediate as a ring of this many pool blocks (0: the whole pool)")
+    ap.add_argument("--lag", type=int, default=-1,
+                    help="fused stream: experts by which L2 trails L1 (-1: the library's choice)")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,
                     help="1: gather + L1 + L2 as one lag-ordered persistent launch; default: the library's")
     args = ap.parse_args()

@@ -152,6 +152,20 @@ typedef struct mm_moe_options {
                                    still names routed experts only (ids >= E are out of range), and
                                    K + S <= 16, E + S <= 1024.  The shared experts' tiles run in the same
                                    launches as the routed ones. */
+  int ring_blocks;              /* the intermediate as a wrapping ring of R pool blocks (DeepGEMM PR #440
+                                   "Ring sizing, recycling, and why that granularity"): 0 (default) =
+                                   the whole pool, one slot per block; R > 0 = R slots of 128 rows, block
+                                   b using slot b % R, for the MX fused stream with swap_ab = 0 only
+                                   (otherwise MM_MOE_ERR_UNSUPPORTED, as with retain_intermediate or
+                                   debug_flags bit 0).  R >= ceil(T / 128) is required (else
+                                   MM_MOE_ERR_INVALID_ARG).  A block's L1 tiles wait until every L2 tile
+                                   of the block R slots back has read it.  The kernel shortens lag_units,
+                                   for this launch, to the largest lag at which every lag + 1 consecutive
+                                   experts own at most R / 2 blocks (0 if one expert owns more), so each
+                                   of those waits points at tiles earlier in the stream and half the
+                                   ring is slack; results are bit-identical to R = 0.  Routing
+                                   that gives one expert more than R blocks (a token naming an expert
+                                   twice) ends with MM_MOE_ERR_BAD_ROUTING, site 114, and no output. */
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather
@@ -259,7 +273,9 @@ int mm_moe_workspace_region(const void* workspace, const mm_moe_options* opt, in
  *             tile-group queue, 109 an early-combine token's experts, 110 an
  *             early-combine deferred entry;
  *             111 / 112 the exit drain of bulk copies / MMAs (after an earlier
- *             error); swapped and paired kernels 121-152 likewise;
+ *             error), 113 a ring slot still read by the L2 tiles of the
+ *             block ring_blocks back; swapped and paired kernels 121-152
+ *             likewise;
  *   FP8 GEMM  201 a free pipeline stage, 202 a stage's data, 203 a free
  *             partial buffer, 204 a finished partial (the commit waiter), 205
  *             the epilogue's amax rendezvous, 211 / 212 the exit drains;

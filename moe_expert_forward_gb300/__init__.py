@@ -43,7 +43,7 @@ class mm_moe_options(ctypes.Structure):
                 ("partials_bf16", ctypes.c_int), ("activation_clamp", ctypes.c_float),
                 ("precise_swiglu", ctypes.c_int), ("x_bf16", ctypes.c_int), ("early_combine", ctypes.c_int),
                 ("swap_ab", ctypes.c_int), ("block_m", ctypes.c_int),
-                ("f8_act_gran", ctypes.c_int), ("shared_experts", ctypes.c_int),
+                ("f8_act_gran", ctypes.c_int), ("shared_experts", ctypes.c_int), ("ring_blocks", ctypes.c_int),
                 ("timing_events", ctypes.c_void_p)]
 
 

@@ -15,7 +15,7 @@ namespace mm {
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags, int partials_bf16, int BT,
-                   int act_gran, int S) {
+                   int act_gran, int S, int ring) {
   Layout L{};
   L.T = T; L.H = H; L.I = I; L.E = E; L.K = K; L.variant = variant; L.BT = BT; L.S = S;
   L.act_gran = variant == MM_MOE_VARIANT_MX ? 32 : act_gran;
@@ -26,6 +26,8 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.nblk_cap = L.P / BT;
   L.KB1 = H / 128;
   L.KB2 = I / 128;
+  L.ring = (ring > 0 && ring < L.nblk_cap) ? ring : 0;   // a ring as large as the pool never wraps
+  const int64_t islots = L.ring ? L.ring : L.nblk_cap;   // pool blocks the intermediate holds
   size_t o = 0;
   L.status = o; o += 256;
   L.cnt = o; o = align_up(o + sizeof(int) * E, 256);
@@ -40,9 +42,9 @@ Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_fla
   L.pool_x_sf = o;
   o = align_up(o + (variant == MM_MOE_VARIANT_MX ? chunks * (H / 128)
                                                  : static_cast<size_t>(L.P) * (H / 128) * sizeof(float)), 1024);
-  L.pool2 = o; o = align_up(o + static_cast<size_t>(L.P) * I, 1024);
+  L.pool2 = o; o = align_up(o + static_cast<size_t>(islots) * BT * I, 1024);
   L.pool2_sf = o;
-  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? chunks * (I / 128)
+  o = align_up(o + (variant == MM_MOE_VARIANT_MX ? static_cast<size_t>(islots) * L.CPB * kSFChunk * (I / 128)
                                                  : static_cast<size_t>(L.P) * (I / L.act_gran) * sizeof(float)), 1024);
   L.part_elem = partials_bf16 ? 2 : 4;
   L.part = o; o = align_up(o + static_cast<size_t>(pairs) * H * L.part_elem, 1024);
@@ -243,6 +245,14 @@ constexpr int kSwapLargeBlockTokens = 64;
 int make_plan(const mm_moe_options& o, int T, int K, int E, Plan* p) {
   if (o.f8_act_gran != 0 && o.f8_act_gran != -1 && o.f8_act_gran != 64 && o.f8_act_gran != 128)
     return MM_MOE_ERR_INVALID_ARG;
+  if (o.ring_blocks < 0) return MM_MOE_ERR_INVALID_ARG;
+  if (o.ring_blocks > 0) {
+    // the ring exists in the token-M MX kernel's fused stream, which reads each slot after its L1 tiles
+    if (o.variant != MM_MOE_VARIANT_MX || !o.fused || o.swap_ab > 0 || o.retain_intermediate || (o.debug_flags & 1))
+      return MM_MOE_ERR_UNSUPPORTED;
+    // one expert owns at most ceil(T / 128) blocks: the ring must hold them with lag 0
+    if (o.ring_blocks < (static_cast<int64_t>(T) + kBT - 1) / kBT) return MM_MOE_ERR_INVALID_ARG;
+  }
   if (o.variant == MM_MOE_VARIANT_F8) {
     if (o.swap_ab > 0 || (o.block_m != 0 && o.block_m != kBT)) return MM_MOE_ERR_UNSUPPORTED;
     *p = {false, false, kBT};
@@ -271,7 +281,8 @@ int f8_gran(const mm_moe_options& o, int H, int I) {
 // E and K are the caller's routed counts; the layout counts the shared experts in both.
 Layout layout_for(const mm_moe_options& o, int T, int H, int I, int E, int K, const Plan& p) {
   const int S = o.shared_experts;
-  return make_layout(T, H, I, E + S, K + S, o.variant, o.debug_flags, o.partials_bf16, p.BT, f8_gran(o, H, I), S);
+  return make_layout(T, H, I, E + S, K + S, o.variant, o.debug_flags, o.partials_bf16, p.BT, f8_gran(o, H, I), S,
+                     o.ring_blocks);
 }
 
 int device_supported() {
@@ -494,6 +505,7 @@ int mm_moe_read_intermediate(const void* workspace, const mm_moe_options* opt, i
   Plan plan;
   if (int r = make_plan(o, T, K, E, &plan)) return r;
   const Layout L = layout_for(o, T, H, I, E, K, plan);
+  if (L.ring) return MM_MOE_ERR_UNSUPPORTED;   // a ring keeps only its last R blocks
   if (rows > L.P) return MM_MOE_ERR_INVALID_ARG;
   if (rows == 0) return MM_MOE_OK;
   const WsPtrs W = ws_ptrs(const_cast<void*>(workspace), L);

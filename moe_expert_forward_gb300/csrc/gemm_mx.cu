@@ -88,7 +88,7 @@ constexpr int kSfColsPerStage = 12;    // 4 (tokens) + 8 (weights)
 enum : int {
   kSiteEmpty = 101, kSiteFull = 102, kSiteTmemEmpty = 103, kSiteTmemFull = 104,
   kSiteGathered = 105, kSiteL1Done = 106, kSiteQueueEmpty = 108,   // 109, 110: early combine (stream.cuh)
-  kSiteDrainCopies = 111, kSiteDrainMma = 112
+  kSiteDrainCopies = 111, kSiteDrainMma = 112, kSiteRingFree = 113, kSiteRingSize = 114
 };
 
 struct Args {
@@ -126,6 +126,8 @@ struct Args {
   int* cmb;                  // early combine counters: tokens taken, deferred, classified, deferred taken
   int* ctr_l2;               // [E] L2 epilogue warps finished per expert (early combine)
   int* deferred;             // [T] tokens pass 1 could not combine yet, as t + 1 (0: not written)
+  int ring;                  // mode 3: intermediate slots of a wrapping ring (block b in slot b % ring); 0 = none
+  int* ctr_l2r;              // [blocks] L2 tiles that have read a block's intermediate (ring reuse)
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;  // per-CTA wait/busy nanoseconds (debug_flags bit 1) or null
@@ -218,6 +220,43 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 __device__ __forceinline__ void regs_dec_mma() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kMmaRegs)); }
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs)); }
 
+// The lag of a fused stream whose intermediate is a ring of R pool blocks.
+// Block b's L1 tiles reuse the slot of block b - R only after the L2 tiles of
+// that block have read it.  If every l + 1 consecutive experts own at most R
+// blocks, block b - R belongs to an expert at least l + 1 before b's, whose L2
+// tiles sit in an earlier segment of the stream: every wait for a free slot
+// points at tiles dealt before it, so the stream cannot deadlock.  A window that
+// fills the ring leaves no slack, though: b's L1 tiles then wait for L2 tiles
+// dealt just before them.  So the lag is the largest l <= lag whose windows own
+// at most R / 2 blocks (PR #440 likewise sets the lag near 0.45 of the ring), or
+// 0 when one expert alone owns more.  All threads of the CTA call this (barriers
+// inside); every CTA reads the same block offsets and takes the same lag.  If
+// one expert alone owns more than R blocks (only possible when a token names an
+// expert twice) the routing is rejected and the CTA stops at once.
+__device__ int ring_lag(const int* blk, int E, int lag, int R, const Status& st, volatile int* s_abort) {
+  auto fits = [&](int l, int cap) {
+    bool bad = false;
+    for (int u = threadIdx.x; u < E; u += blockDim.x) bad |= blk[u + 1] - blk[u - l < 0 ? 0 : u - l] > cap;
+    return !__syncthreads_or(bad);
+  };
+  if (!fits(0, R)) {
+    if (threadIdx.x == 0) {
+      report_error(st, MM_MOE_ERR_BAD_ROUTING, kSiteRingSize);
+      *s_abort = 1;
+    }
+    __syncthreads();
+    return 0;
+  }
+  const int half = R / 2;
+  if (!fits(0, half)) return 0;
+  int lo = 0, hi = lag;   // fits(lo, half) holds; the answer lies in [lo, hi]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (fits(mid, half)) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // kProf: record per-role wait and busy times (debug_flags bit 1).  A separate
 // instantiation, because even untaken timing branches slow the MMA issue loop.
 template <bool kProf>
@@ -240,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Status st{args.status, args.timeout_ns};
-  const int lag = args.mode == 3 ? args.lag : 0;
+  int lag = args.mode == 3 ? args.lag : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -276,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
   const uint32_t tmem = *s_tmem;
 
   const int nblk = s_blk[E];
+  if (args.mode == 3 && args.ring > 0) lag = ring_lag(s_blk, E, lag, args.ring, st, s_abort);
   Sched sch{s_blk, s_cnt, E, args.NB1, args.NB2, args.mode, lag};
   sch.per_block = args.per_block != 0;
 
@@ -318,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const uint32_t bytes = rows * kBK + kWgtTxBytes + 2 * kSFChunk + kSFChunk;
         const uint8_t* sfw = (l1 ? args.sfw1 : args.sfw2) +
                              (static_cast<size_t>(t.e) * (l1 ? args.NB1 : args.NB2) + t.n) * KB * 2 * kSFChunk;
-        const uint8_t* sft = (l1 ? args.pool_x_sf : args.pool2_sf) + static_cast<size_t>(t.b) * KB * kSFChunk;
+        const int tb = (!l1 && args.ring) ? t.b % args.ring : t.b;   // the block's intermediate slot
+        const uint8_t* sft = (l1 ? args.pool_x_sf : args.pool2_sf) + static_cast<size_t>(tb) * KB * kSFChunk;
         for (; kb < KB; kb += kStages) {
           const uint32_t phase = ((step + kb) / kStages) & 1;
           const uint64_t t0 = kProf ? globaltimer() : 0;
@@ -329,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           armed_parity = phase;
           const int kbe = t.rev ? KB - 1 - kb : kb;   // the k-block this stage carries
           const int kc = kbe * kBK;
-          tma_load_2d(tk, tt, &full[p], kc, t.b * kBT, pol_t);
+          tma_load_2d(tk, tt, &full[p], kc, tb * kBT, pol_t);
           bulk_load(st_, sft + static_cast<size_t>(kbe) * kSFChunk, kSFChunk, &full[p]);
           const uint64_t pw = t.last ? pol_w : pol_wk;
           if (l1) tma_load_3d(wg, &maps.w1, &full[p], kc, t.e * 2 * args.I + t.n * 128, 0, pw);
@@ -441,6 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       const size_t row = static_cast<size_t>(t.b) * kBT + m;
       const int s = live ? __ldg(args.src + row) : 0;
       const float w = (t.type == 1 && live) ? __ldg(args.topk_w + s) : 0.f;   // loaded before the wait
+      if (t.type == 1 && args.ring && t.b >= args.ring) {
+        // the slot's previous block (ring blocks back) must have been read by all of its L2 tiles
+        bool ok = true;
+        if (lane == 0) ok = wait_counter_geq(args.ctr_l2r + (t.b - args.ring), args.NB2, st, s_abort, kSiteRingFree);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        __syncwarp();
+        if (!ok) break;
+      }
       const uint64_t t0 = kProf ? globaltimer() : 0;
       if (!mbar_wait(tfull, it & 1, st, s_abort, kSiteTmemFull)) break;
       const uint64_t t1 = kProf ? globaltimer() : 0;
@@ -460,9 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
+      if (t.type == 2 && args.ring && warp == kEpiWarp0 && lane == 0)
+        red_release_gpu_add(args.ctr_l2r + t.b, 1);   // the MMAs are done: the slot has been read
       if (t.type == 1) {
-        uint8_t* crow = args.pool2 + row * args.I + t.n * 128;
-        uint8_t* sfrow = args.pool2_sf + (static_cast<size_t>(t.b) * (args.I / 128) + t.n) * kSFChunk +
+        const int sb = args.ring ? t.b % args.ring : t.b;   // the block's intermediate slot
+        uint8_t* crow = args.pool2 + (static_cast<size_t>(sb) * kBT + m) * args.I + t.n * 128;
+        uint8_t* sfrow = args.pool2_sf + (static_cast<size_t>(sb) * (args.I / 128) + t.n) * kSFChunk +
                          (m & 31) * 16 + (m >> 5) * 4;
         l1_block(r0, r2, 2 * half, live, w, row, t.n, args, crow, sfrow);
         l1_block(r1, r3, 2 * half + 1, live, w, row, t.n, args, crow, sfrow);
@@ -561,6 +613,8 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.cmb = W.ctr + 2 * L.nblk_cap + kSchedCounters;
   a.ctr_l2 = a.cmb + kCombineCounters;
   a.deferred = a.ctr_l2 + L.E;
+  a.ring = mode == 3 ? static_cast<int>(L.ring) : 0;
+  a.ctr_l2r = a.deferred + L.T;
   a.status = W.status; a.timeout_ns = g.timeout_ns;
   a.prof = g.prof ? g.prof + (mode == 2 ? 8 * 1024 : 0) : nullptr;
   {
@@ -582,7 +636,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
     if (encode_tmap_2d(xm[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, W.pool_x, L.H, L.P, L.H, 128, 32u << i,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    if (encode_tmap_2d(am[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, W.pool2, L.I, L.P, L.I, 128, 32u << i,
+    if (encode_tmap_2d(am[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, W.pool2, L.I, L.ring ? L.ring * kBT : L.P, L.I, 128, 32u << i,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }

@@ -27,13 +27,14 @@ struct Layout {
   int part_elem;             // bytes of one partial: 4 (fp32) or 2 (bf16)
   int act_gran;              // F8: intermediate scale block along I (128 or 64); MX: 32
   int S;                     // shared experts (the last S of E and of K; 0 = none)
+  int64_t ring;              // intermediate slots (pool blocks) of a wrapping ring; 0 = one per pool block
   size_t ext_idx, ext_w;     // shared experts: the routing extended by S slots, int32 / fp32 [T, K]
   size_t status, cnt, blk_off, dscr, ctr, slot, src, pool_x, pool_x_sf, pool2, pool2_sf, part, dbg, dbg_bytes, prof, total;
 };
 
 // E and K count the shared experts: E = routed + S, K = routed slots + S.
 Layout make_layout(int T, int H, int I, int E, int K, int variant, int debug_flags = 0, int partials_bf16 = 0,
-                   int BT = kBT, int act_gran = 128, int S = 0);
+                   int BT = kBT, int act_gran = 128, int S = 0, int ring = 0);
 // The F8 intermediate's scale width by the shape rule of DeepGEMM PR #440 ("Ring
 // sizing, recycling, and why that granularity"): 128 when H % 512 == 0 and
 // 2I % 512 == 0, else 64.
@@ -49,9 +50,10 @@ __host__ __device__ __forceinline__ size_t pool_sf_word(int64_t b, int kb, int K
 
 // Ints of the counter region, zeroed before every forward: [2][nblk_cap]
 // per-block arrival counters, kSchedCounters, kCombineCounters, [E] L2
-// completions per expert, [T] deferred tokens of the early combine (t + 1).
+// completions per expert, [T] deferred tokens of the early combine (t + 1),
+// [nblk_cap] L2 tiles that have read each block's intermediate (ring reuse).
 inline size_t ctr_ints(const Layout& L) {
-  return 2 * static_cast<size_t>(L.nblk_cap) + kSchedCounters + kCombineCounters + L.E + L.T;
+  return 3 * static_cast<size_t>(L.nblk_cap) + kSchedCounters + kCombineCounters + L.E + L.T;
 }
 
 // Device pointers resolved from a workspace.

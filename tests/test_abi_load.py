@@ -154,9 +154,39 @@ def test_shared_experts_host_checks(M):
     assert cnt_bytes == 4 * (E + 3) and slot_bytes == 4 * T * (K + 3)
 
 
+def test_ring_host_checks(M):
+    """ring_blocks: 0 = the whole pool; R > 0 only for the token-M MX fused
+    stream (else UNSUPPORTED) and only with R >= ceil(T / 128) (else INVALID_ARG);
+    the intermediate then holds R blocks of codes and scales instead of one per
+    pool block, and a ring as large as the pool changes nothing."""
+    T, H, I, E, K = 2048, 4096, 2048, 256, 6
+    mx = lambda **kw: M.options(M.MM_MOE_VARIANT_MX, **kw)
+    full = M.mm_moe_workspace_size(mx(), T, H, I, E, K)
+    ring = M.mm_moe_workspace_size(mx(ring_blocks=64), T, H, I, E, K)
+    blocks = ((T * K + E * 127) + 127) // 128
+    assert full - ring >= (blocks - 64) * 128 * I * 33 // 32 - 4096
+    _, codes = M.mm_moe_workspace_region(0, mx(ring_blocks=64), T, H, I, E, K, 7)
+    assert 64 * 128 * I <= codes < 64 * 128 * I + 1024
+    assert M.mm_moe_workspace_size(mx(ring_blocks=blocks), T, H, I, E, K) == full
+    assert M.mm_moe_workspace_size(mx(ring_blocks=16), T, H, I, E, K) < ring
+    for bad, code in ((dict(ring_blocks=-1), M.MM_MOE_ERR_INVALID_ARG),
+                      (dict(ring_blocks=15), M.MM_MOE_ERR_INVALID_ARG),      # ceil(2048 / 128) = 16
+                      (dict(ring_blocks=64, fused=0), M.MM_MOE_ERR_UNSUPPORTED),
+                      (dict(ring_blocks=64, swap_ab=1), M.MM_MOE_ERR_UNSUPPORTED),
+                      (dict(ring_blocks=64, swap_ab=2), M.MM_MOE_ERR_UNSUPPORTED),
+                      (dict(ring_blocks=64, retain_intermediate=1), M.MM_MOE_ERR_UNSUPPORTED),
+                      (dict(ring_blocks=64, debug_flags=1), M.MM_MOE_ERR_UNSUPPORTED)):
+        with pytest.raises(M.MMError) as ei:
+            M.mm_moe_workspace_size(mx(**bad), T, H, I, E, K)
+        assert ei.value.code == code, bad
+    with pytest.raises(M.MMError) as ei:
+        M.mm_moe_workspace_size(M.options(M.MM_MOE_VARIANT_F8, ring_blocks=64), T, H, I, E, K)
+    assert ei.value.code == M.MM_MOE_ERR_UNSUPPORTED
+
+
 def test_default_options(M):
     o = M.mm_moe_default_options()
     assert (o.variant, o.fused, o.lag_units, o.wait_timeout_ms) == (M.MM_MOE_VARIANT_MX, 1, -1, 2000)
-    assert (o.f8_act_gran, o.shared_experts) == (0, 0)
+    assert (o.f8_act_gran, o.shared_experts, o.ring_blocks) == (0, 0, 0)
     assert (o.cta_pairs, o.partials_bf16, o.precise_swiglu, o.x_bf16, o.early_combine) == (0, 0, 0, 0, 0)
     assert o.activation_clamp == 0.0 and not o.timing_events
