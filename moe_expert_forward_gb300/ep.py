@@ -13,9 +13,12 @@ The combine comes in the pages' push form (each owner stores every received row'
 bf16 output into the token's rank, which then sums its slots locally) and a pull
 form (each rank reads its slots' outputs from their owners); both give the same
 bits.  `plan_distributed` is the host side of a multi-process run
-(torch.distributed: an all-gather of the counts).  `forward_on_one_device` runs N ranks whose buffers
-all live on one GPU, step by step from the host, which checks the whole data path
-on a single device; a multi-GPU run differs only in where the peers' buffers live.
+(torch.distributed: an all-gather of the counts).  `forward_distributed` is one
+rank's whole forward in a multi-process run: the peers' buffers are mapped into
+this process by CUDA IPC (`share_peers`), and a device synchronisation plus a
+process-group barrier separates the steps, so no kernel ever waits for another
+process.  `forward_on_one_device` runs N ranks whose buffers all live in one
+process, step by step from the host.
 """
 from __future__ import annotations
 
@@ -157,3 +160,107 @@ def forward_on_one_device(states: List[RankState], w1, w1_sf, w2, w2_sf, I: int,
             outs.append(out)
     torch.cuda.synchronize()
     return outs, plans
+
+
+def share_peers(tensors: Sequence, group=None):
+    """Every rank's copy of each tensor in `tensors`, mapped into this process.
+
+    The handles travel through the process group (an all-gather of picklable
+    objects); each peer allocation is opened with CUDA IPC by torch's own CUDA
+    tensor sharing, which also keeps the producer's block alive until every
+    consumer has released it.  This rank's entries are the tensors themselves.
+    Returns [len(tensors)][N] tensors; drop them (and barrier) before a peer
+    frees its buffers."""
+    import torch.distributed as dist
+    from torch.multiprocessing.reductions import rebuild_cuda_tensor, reduce_tensor
+    N = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    mine = [reduce_tensor(t)[1] for t in tensors]
+    every = [None] * N
+    dist.all_gather_object(every, mine, group=group)
+    return [[t if r == rank else rebuild_cuda_tensor(*every[r][i]) for r in range(N)] for i, t in enumerate(tensors)]
+
+
+def forward_distributed(st: RankState, w1, w1_sf, w2, w2_sf, I: int, opt=None, group=None, combine: str = "push",
+                        num_tokens_bound: Optional[int] = None):
+    """One rank's EP forward in a multi-process run (one process per rank; the
+    ranks may share a GPU or not).  st holds this rank's tokens; w1 / w1_sf / w2 /
+    w2_sf hold all E experts in the layouts of mm_moe.h, of which this rank uses
+    [rank*E/N, (rank+1)*E/N).  Steps: count -> all-gather the counts -> plan ->
+    exchange buffer addresses -> push metadata -> barrier -> pull rows and the
+    local forward -> barrier -> combine (push: store row outputs into the token
+    ranks, barrier, local sum; pull: read the slots from their owners) ->
+    barrier.  Returns this rank's bf16 output [T, H] and its plan (send_row,
+    recv_rows, recv_expert)."""
+    import torch
+    import torch.distributed as dist
+    N = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    assert rank == st.rank and N == st.N
+    E, H, K, T, variant = st.E, st.H, st.K, st.T, st.variant
+    Eloc = E // N
+    dev = st.x.device
+    s = torch.cuda.current_stream().cuda_stream
+    base_opt = opt if opt is not None else options(variant)
+
+    def barrier():
+        torch.cuda.synchronize()
+        dist.barrier(group=group)
+
+    # 1. counts, gathered on the host, and this rank's plan
+    c = torch.empty(E, dtype=torch.int32, device=dev)
+    _check(mm_moe_ep_count(st.topk_idx.data_ptr(), T, K, E, c.data_ptr(), s), "mm_moe_ep_count")
+    every = [None] * N
+    dist.all_gather_object(every, c.cpu().numpy(), group=group)
+    counts_all = np.stack(every)
+    cap = mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N) if num_tokens_bound is not None else None
+    send_row, rows, rex = mm_moe_ep_plan(counts_all, st.topk_idx.cpu().numpy(), T, K, E, N, rank, recv_capacity=cap)
+    R = rows
+    room = max(rows if cap is None else cap, 1)
+    send_row_d = torch.from_numpy(np.ascontiguousarray(send_row)).to(dev)
+    meta = torch.zeros(room, 4, dtype=torch.int32, device=dev)
+    out_recv = torch.zeros(room, H, dtype=torch.bfloat16, device=dev)
+    parts = torch.empty(max(T * K, 1), H, dtype=torch.bfloat16, device=dev)
+    # 2. every rank's buffers, mapped here
+    peer_meta, peer_x, peer_xsf, peer_out, peer_part = share_peers([meta, st.x, st.x_sf, out_recv, parts], group)
+    t_meta, t_x, t_xsf, t_out, t_part = (pointer_table(p, dev) for p in
+                                         (peer_meta, peer_x, peer_xsf, peer_out, peer_part))
+    # 3. metadata pushed into the owners' buffers
+    _check(mm_moe_ep_push_meta(st.topk_idx.data_ptr(), st.topk_w.data_ptr(), send_row_d.data_ptr(), T, K, E, N, rank,
+                               t_meta.data_ptr(), s), "mm_moe_ep_push_meta")
+    barrier()
+    # 4. rows pulled from their source ranks, then the local forward over them (K = 1)
+    if R > 0:
+        sf_row = H // 32 if variant == MM_MOE_VARIANT_MX else H // 128
+        sf_dtype = torch.uint8 if variant == MM_MOE_VARIANT_MX else torch.float32
+        x_recv = torch.empty(R, H, dtype=torch.uint8, device=dev)
+        xsf_recv = torch.empty(R, sf_row, dtype=sf_dtype, device=dev)
+        idx_recv = torch.empty(R, 1, dtype=torch.int32, device=dev)
+        w_recv = torch.empty(R, 1, dtype=torch.float32, device=dev)
+        _check(mm_moe_ep_pull(meta.data_ptr(), R, K, H, variant, t_x.data_ptr(), t_xsf.data_ptr(), x_recv.data_ptr(),
+                              xsf_recv.data_ptr(), idx_recv.data_ptr(), w_recv.data_ptr(), s), "mm_moe_ep_pull")
+        lo, hi = rank * Eloc, (rank + 1) * Eloc
+        w1p, w2p = prepare_weights(w1_sf[lo:hi].contiguous(), w2_sf[lo:hi].contiguous(), H, I, Eloc, base_opt)
+        ws = alloc_workspace(R, H, I, Eloc, 1, base_opt, dev)
+        forward(x_recv, xsf_recv, idx_recv, w_recv, w1[lo:hi].contiguous(), w1p, w2[lo:hi].contiguous(), w2p,
+                out_recv, H, I, Eloc, ws, base_opt)
+        code, where = sync_status(ws)
+        if code != 0:
+            raise MMError(code, f"rank {rank} local forward (site {where})")
+    barrier()
+    # 5. combine
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if combine == "push":
+        _check(mm_moe_ep_push_out(meta.data_ptr(), R, H, out_recv.data_ptr(), t_part.data_ptr(), s),
+               "mm_moe_ep_push_out")
+        barrier()
+        _check(mm_moe_ep_combine_local(st.topk_idx.data_ptr(), T, K, E, H, parts.data_ptr(), out.data_ptr(), s),
+               "mm_moe_ep_combine_local")
+    else:
+        _check(mm_moe_ep_combine(st.topk_idx.data_ptr(), send_row_d.data_ptr(), T, K, E, N, H, t_out.data_ptr(),
+                                 out.data_ptr(), s), "mm_moe_ep_combine")
+    # no rank frees a buffer while a peer may still read or write it
+    barrier()
+    del peer_meta, peer_x, peer_xsf, peer_out, peer_part
+    barrier()
+    return out, (send_row, rows, rex)
