@@ -175,10 +175,19 @@ def share_peers(tensors: Sequence, group=None):
     from torch.multiprocessing.reductions import rebuild_cuda_tensor, reduce_tensor
     N = dist.get_world_size(group)
     rank = dist.get_rank(group)
-    mine = [reduce_tensor(t)[1] for t in tensors]
+    import torch
+    # an empty tensor (a rank without tokens) has no allocation to share, and no
+    # kernel reads through its address: it travels as None and maps to an empty tensor
+    mine = [reduce_tensor(t)[1] if t.numel() else None for t in tensors]
     every = [None] * N
     dist.all_gather_object(every, mine, group=group)
-    return [[t if r == rank else rebuild_cuda_tensor(*every[r][i]) for r in range(N)] for i, t in enumerate(tensors)]
+
+    def peer(r, i, t):
+        if r == rank:
+            return t
+        h = every[r][i]
+        return rebuild_cuda_tensor(*h) if h is not None else torch.empty(0, dtype=t.dtype, device=t.device)
+    return [[peer(r, i, t) for r in range(N)] for i, t in enumerate(tensors)]
 
 
 def forward_distributed(st: RankState, w1, w1_sf, w2, w2_sf, I: int, opt=None, group=None, combine: str = "push",

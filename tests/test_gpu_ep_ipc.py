@@ -32,7 +32,7 @@ def _free_port() -> int:
         return s.getsockname()[1]
 
 
-def _rank_main(rank, N, port, cfg_kw, combine, bound, result_dir):
+def _rank_main(rank, N, port, cfg_kw, combine, bound, result_dir, splits):
     import sys
     sys.path.insert(0, ROOT)
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -49,8 +49,8 @@ def _rank_main(rank, N, port, cfg_kw, combine, bound, result_dir):
         from gpu_util import run_forward, to_dev
         cfg = W.Config(**cfg_kw)
         dev = to_dev(W.make_inputs(cfg, "cpu"))         # every rank generates the same seeded workload
-        Tr = cfg.T // N
-        sl = slice(rank * Tr, (rank + 1) * Tr)
+        lo = sum(splits[:rank])                          # this rank's tokens, rank-major
+        sl = slice(lo, lo + splits[rank])
         variant = M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8
         st = ep.RankState(rank, dev["x"][sl].contiguous(), dev["x_sf"][sl].contiguous(),
                           dev["topk_idx"][sl].contiguous(), dev["topk_w"][sl].contiguous(), cfg.E, N, variant)
@@ -58,7 +58,7 @@ def _rank_main(rank, N, port, cfg_kw, combine, bound, result_dir):
                                                              cfg.I, combine=combine, num_tokens_bound=bound)
         single, _, _, (code, _) = run_forward(M, cfg, dev, M.options(variant, partials_bf16=1))
         same = code == 0 and torch.equal(out, single[sl])
-        diff = float((out.float() - single[sl].float()).abs().max())
+        diff = float((out.float() - single[sl].float()).abs().max()) if out.numel() else 0.0
         dist.barrier()
         dist.destroy_process_group()
         with open(path, "w") as f:
@@ -68,12 +68,13 @@ def _rank_main(rank, N, port, cfg_kw, combine, bound, result_dir):
             f.write("error\n" + traceback.format_exc())
 
 
-def _run(cfg, N, combine="push", bound=None, tmp_path=None):
+def _run(cfg, N, combine="push", bound=None, tmp_path=None, splits=None):
     import multiprocessing as mp
     ctx = mp.get_context("spawn")
     port = _free_port()
     cfg_kw = dict(name=cfg.name, T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, variant=cfg.variant, seed=cfg.seed)
-    procs = [ctx.Process(target=_rank_main, args=(r, N, port, cfg_kw, combine, bound, str(tmp_path)))
+    splits = splits or [cfg.T // N] * N
+    procs = [ctx.Process(target=_rank_main, args=(r, N, port, cfg_kw, combine, bound, str(tmp_path), splits))
              for r in range(N)]
     for p in procs:
         p.start()
@@ -110,3 +111,13 @@ def test_ep_two_processes_pull_combine_with_bound(tmp_path):
     res = _run(cfg, 2, combine="pull", bound=cfg.T // 2, tmp_path=tmp_path)
     for r, parts in enumerate(res):
         assert parts[1] == "1", f"rank {r}: {' '.join(parts)}"
+
+
+def test_ep_two_processes_rank_without_tokens(tmp_path):
+    """Rank 1 holds no tokens: it still owns half of the experts, receives rank
+    0's pairs for them, and shares empty token buffers."""
+    cfg = CFGS[0].with_(seed=94)
+    res = _run(cfg, 2, tmp_path=tmp_path, splits=[cfg.T, 0])
+    for r, parts in enumerate(res):
+        assert parts[1] == "1", f"rank {r}: {' '.join(parts)}"
+    assert int(res[1][3]) > 0
