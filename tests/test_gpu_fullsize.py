@@ -1,7 +1,9 @@
-"""Parity at the workload sizes the benchmark times (flash, pro, decode), in the
-launch configuration bench.py uses: every output row of a seeded sample is
-checked against the oracle, the routing is checked in full, and the sampled
-rows' intermediate codes are compared."""
+"""Parity at the workload sizes the benchmark times (flash, pro, decode, FP8), in
+the launch configuration bench.py uses and in the other forms it can time (the
+two-launch path; the swapped and paired MX kernels at flash and decode): every
+output row of a seeded sample is checked against the oracle, the routing is
+checked in full at each form's block size, and the sampled rows' intermediate
+codes are compared."""
 import gc
 
 import numpy as np
@@ -18,8 +20,8 @@ pytestmark = pytest.mark.gpu
 # for decode); None = the whole subset.
 SAMPLE_ROWS = {"flash": None, "decode": None, "f8": None, "pro": None}
 # launch modes compared against the same oracle rows
-MODES = {"flash": [dict(fused=1), dict(fused=0)],
-         "decode": [dict(fused=1)],
+MODES = {"flash": [dict(fused=1), dict(fused=0), dict(swap_ab=1), dict(swap_ab=2)],
+         "decode": [dict(fused=1), dict(swap_ab=1), dict(swap_ab=2)],
          "pro": [dict(fused=1), dict(fused=0)],
          "f8": [dict()]}
 
@@ -40,13 +42,17 @@ def test_fullsize_sampled_rows(M, name):
         rng = np.random.default_rng(cfg.seed + 11)
         rows = np.sort(rng.choice(rows, min(SAMPLE_ROWS[name], len(rows)), replace=False))
     ref, inter = oracle_rows(cfg, dev, rows)
-    ref_route = O.route(dev["topk_idx"].cpu().numpy(), cfg.E, 128)
+    idx_host = dev["topk_idx"].cpu().numpy()
+    routes = {}
     for kw in MODES[name]:
         opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8, **kw)
         out, ws, prepared, (code, where) = run_forward(M, cfg, dev, opt)
         assert code == 0, f"{kw}: device status {code} at site {where}"
         cnt, blk, slot, src, bm = read_routing(M, cfg, ws, opt)
-        assert bm == 128
+        assert (bm in (80, 160)) if kw.get("swap_ab") else bm == 128
+        if bm not in routes:
+            routes[bm] = O.route(idx_host, cfg.E, bm)
+        ref_route = routes[bm]
         assert np.array_equal(cnt, ref_route["cnt"]) and np.array_equal(blk, ref_route["blk_off"])
         assert np.array_equal(slot, ref_route["slot"])
         assert np.array_equal(src[:len(ref_route["src"])], ref_route["src"])
