@@ -1,6 +1,7 @@
 """The forward inside a CUDA graph: mm_moe_forward allocates nothing and never
 synchronises, so a captured forward replays with the same results as the eager
-call, in both variants, the fused stream and the two-launch path."""
+call, in both variants, the fused stream (also with the intermediate ring) and
+the two-launch path."""
 import pytest
 import torch
 
@@ -20,10 +21,12 @@ def M():
 
 CASES = [(W.Config("g_mx", T=300, H=512, I=384, E=5, K=2, seed=91), dict(fused=1)),
          (W.Config("g_mx", T=300, H=512, I=384, E=5, K=2, seed=91), dict(fused=0)),
-         (W.Config("g_f8", T=200, H=512, I=256, E=6, K=2, variant="f8", seed=92), dict())]
+         (W.Config("g_f8", T=200, H=512, I=256, E=6, K=2, variant="f8", seed=92), dict()),
+         # the ring's lag is chosen on the device from each replay's routing
+         (W.Config("g_ring", T=256, H=256, I=256, E=64, K=6, seed=93), dict(fused=1, ring_blocks=5))]
 
 
-@pytest.mark.parametrize("cfg,kw", CASES, ids=["mx_fused", "mx_two_launch", "f8"])
+@pytest.mark.parametrize("cfg,kw", CASES, ids=["mx_fused", "mx_two_launch", "f8", "mx_ring"])
 def test_forward_replays_from_a_cuda_graph(M, cfg, kw):
     dev = to_dev(W.make_inputs(cfg, "cpu"))
     opt = M.options(M.MM_MOE_VARIANT_MX if cfg.variant == "mx" else M.MM_MOE_VARIANT_F8, **kw)
