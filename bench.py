@@ -275,6 +275,21 @@ def run_ours(args, ws_n, rank, local):
     torch.cuda.synchronize()
     stage_ms = np.array([[sev[i][j].elapsed_time(sev[i][j + 1]) for j in range(5)] for i in range(n_st)])
 
+    # optional per-task trace of one more step (the kernel's timing instantiation, after the timed steps)
+    trace_summary = None
+    if args.trace and cfg.variant == "mx" and not opt.swap_ab:
+        from moe_expert_forward_gb300 import trace as TR
+        launches = 1 if fused else 2
+        tbuf = torch.zeros(TR.buffer_bytes(torch.cuda.get_device_properties(dev).multi_processor_count, 4096,
+                                           launches), dtype=torch.uint8, device=dev)
+        o = M.mm_moe_options.from_buffer_copy(opt)
+        o.trace_buf, o.trace_bytes = tbuf.data_ptr(), tbuf.numel()
+        flush.zero_()
+        fwd(o)
+        torch.cuda.synchronize()
+        trace_summary = TR.summary(TR.records(tbuf))
+        del tbuf
+
     # end to end, as a serving loop runs it: every step copies its inputs from pinned host
     # memory and reads its output back to pinned host memory.  The copies run on streams of
     # their own with two buffer sets, so step i+1's inputs and step i-1's output move while
@@ -410,6 +425,8 @@ def run_ours(args, ws_n, rank, local):
         "gpu_launches": (3 if early else (4 if fused else 6)) * K,   # dispatch x2, [gather], GEMM(s), [combine]
         "clocks": clk,
     }
+    if trace_summary is not None:
+        result["trace"] = trace_summary
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(cfg, inp, args.cpu_tokens or CPU_TOKENS[cfg.name], args.f8_gran)
     return result
@@ -536,6 +553,8 @@ def main():
                     help="FP8: intermediate scale width (0: per 128, the library default; -1: the pages' shape rule)")
     ap.add_argument("--ring-blocks", type=int, default=0,
                     help="MX fused stream: the intermediate as a ring of this many pool blocks (0: the whole pool)")
+    ap.add_argument("--trace", action="store_true",
+                    help="MX token-M kernel: trace one extra step per task and add its phase summary ('trace')")
     ap.add_argument("--lag", type=int, default=-1,
                     help="fused stream: experts by which L2 trails L1 (-1: the library's choice)")
     ap.add_argument("--fused", type=int, choices=[0, 1], default=None,

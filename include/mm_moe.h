@@ -166,6 +166,24 @@ typedef struct mm_moe_options {
                                    ring is slack; results are bit-identical to R = 0.  Routing
                                    that gives one expert more than R blocks (a token naming an expert
                                    twice) ends with MM_MOE_ERR_BAD_ROUTING, site 114, and no output. */
+  void* trace_buf;              /* optional per-task trace (device memory, 16-byte aligned, zeroed by the
+                                   caller; NULL = off, the default).  The token-M MX kernel (swap_ab = 0)
+                                   then runs its timing instantiation (a few % slower) and writes one
+                                   64-byte record per task it runs: uint32 cta, task (its index within
+                                   the CTA), type (1 = L1, 2 = L2), expert, tile, pool block, valid rows,
+                                   launch mode (3 = fused stream, 1 / 2 = the L1 / L2 launch of the
+                                   two-launch path), then uint64 globaltimer nanoseconds: t_issue (the
+                                   MMA warp issued the task's first k-block), t_mma_done (the epilogue
+                                   saw the accumulator complete), t_epi_done (the first epilogue warp
+                                   finished the task's output), and one reserved word.  Layout:
+                                   [launch][CTA][cap] records with cap = trace_bytes / (64 * grid *
+                                   launches), grid = the persistent grid (num_sms or the SM count),
+                                   launches = 1 for the fused stream, 2 for two launches; tasks past
+                                   cap are not recorded, and unwritten records keep type 0.  A buffer
+                                   smaller than one record per CTA and launch: MM_MOE_ERR_INVALID_ARG;
+                                   with the F8 variant or swap_ab > 0: MM_MOE_ERR_UNSUPPORTED (the
+                                   pages' instrumented event traces; off the default path). */
+  size_t trace_bytes;
   void* timing_events;          /* optional array of MM_MOE_NUM_TIMING_EVENTS cudaEvent_t (created by the
                                    caller) that mm_moe_forward records on `stream` at the start, between
                                    its kernels and at the end: [0] start, [1] dispatch done, [2] gather

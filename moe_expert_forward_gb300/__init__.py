@@ -44,6 +44,7 @@ class mm_moe_options(ctypes.Structure):
                 ("precise_swiglu", ctypes.c_int), ("x_bf16", ctypes.c_int), ("early_combine", ctypes.c_int),
                 ("swap_ab", ctypes.c_int), ("block_m", ctypes.c_int),
                 ("f8_act_gran", ctypes.c_int), ("shared_experts", ctypes.c_int), ("ring_blocks", ctypes.c_int),
+                ("trace_buf", ctypes.c_void_p), ("trace_bytes", ctypes.c_size_t),
                 ("timing_events", ctypes.c_void_p)]
 
 

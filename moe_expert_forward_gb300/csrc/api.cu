@@ -403,13 +403,22 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
   if (int r = make_plan(o, T, K, E, &plan)) return r;
   // the fused stream exists for the MX format; F8 and the L1 debug dump run the two-launch path
   const bool fused = o.fused && o.variant == MM_MOE_VARIANT_MX && !(o.debug_flags & 1);
+  const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
+  // per-task trace: [launch][CTA][cap] records of the token-M MX kernel
+  int64_t trace_cap = 0;
+  if (o.trace_buf) {
+    if (o.variant != MM_MOE_VARIANT_MX || plan.swap) return MM_MOE_ERR_UNSUPPORTED;
+    if (!aligned(o.trace_buf, 16)) return MM_MOE_ERR_INVALID_ARG;
+    trace_cap = static_cast<int64_t>(o.trace_bytes / (sizeof(TraceRec) * grid * (fused ? 1 : 2)));
+    if (trace_cap < 1) return MM_MOE_ERR_INVALID_ARG;
+    if (trace_cap > (int64_t(1) << 30)) trace_cap = int64_t(1) << 30;
+  }
   const Layout L = layout_for(o, T, H, I, E, K, plan);
   if (workspace_bytes < L.total) return MM_MOE_ERR_WORKSPACE_TOO_SMALL;
   // early combine in the fused stream
   const bool early = fused && o.early_combine;
   const WsPtrs W = ws_ptrs(workspace, L);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int grid = (o.num_sms > 0 && o.num_sms < dev_info().sms) ? o.num_sms : dev_info().sms;
   // from here on the routing, the expert count and the slot count include the shared experts
   const int32_t* idx = L.S ? W.ext_idx : topk_idx;
   const float* wts = L.S ? W.ext_w : topk_w;
@@ -442,6 +451,8 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
                  clamp, o.precise_swiglu != 0, early, idx, out, pdl_gemm,
                  // a shared expert has T / 128 blocks: deal them one by one, not as one CTA's run
                  (o.debug_flags & 8) != 0 || L.S > 0};
+    g.trace = static_cast<uint8_t*>(o.trace_buf);
+    g.trace_cap = static_cast<int>(trace_cap);
     auto gemm = plan.pair ? launch_gemm_mx_pair : (plan.swap ? launch_gemm_mx_sw : launch_gemm_mx);
     if (fused) {
       // one lag-ordered stream: gather, L1 and L2 in a single persistent launch
@@ -452,6 +463,7 @@ int mm_moe_forward(const void* x, const void* x_sf, const int32_t* topk_idx, con
       if (e == cudaSuccess) e = gemm(g, 1, 0, 0, s);
       if (e == cudaSuccess) e = mark(3);
       if (o.debug_flags & 1) return e == cudaSuccess ? MM_MOE_OK : MM_MOE_ERR_CUDA;
+      if (g.trace) g.trace += static_cast<size_t>(grid) * trace_cap * sizeof(TraceRec);   // the L2 launch's slice
       if (e == cudaSuccess) e = gemm(g, 2, 0, 0, s);
     }
   } else {

@@ -131,6 +131,8 @@ struct Args {
   int* status;
   uint64_t timeout_ns;
   unsigned long long* prof;  // per-CTA wait/busy nanoseconds (debug_flags bit 1) or null
+  TraceRec* trace;           // per-task records, trace_cap per CTA, or null
+  int trace_cap;
 };
 
 struct Maps {
@@ -257,8 +259,9 @@ __device__ int ring_lag(const int* blk, int E, int lag, int R, const Status& st,
   return lo;
 }
 
-// kProf: record per-role wait and busy times (debug_flags bit 1).  A separate
-// instantiation, because even untaken timing branches slow the MMA issue loop.
+// kProf: record per-role wait and busy times (debug_flags bit 1) and/or per-task
+// trace records (Options.trace_buf).  A separate instantiation, because even
+// untaken timing branches slow the MMA issue loop.
 template <bool kProf>
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ Maps maps, const Args args) {
   extern __shared__ uint8_t smem_raw[];
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       // the copies of the last armed phase have landed before the shared memory goes away
       // (at once on a normal exit, where the MMA issuer consumed every phase)
       if (armed) mbar_wait_drain(&full[p], armed_parity, st, kSiteDrainCopies);
-      if (kProf) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
+      if (kProf && args.prof) atomicAdd(&args.prof[blockIdx.x * 8 + 0], static_cast<unsigned long long>(w_empty));
     }
   } else if (wg == 3) {
     regs_dec_mma();
@@ -422,7 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             if (!mbar_wait(&full[s], phase, st, s_abort, kSiteFull)) {
               live = false;
             } else {
-              if (kProf) w_full += clock64() - t1;
+              if (kProf) {
+                w_full += clock64() - t1;
+                if (args.trace && kb == 0 && it < args.trace_cap)
+                  args.trace[static_cast<size_t>(blockIdx.x) * args.trace_cap + it].t_issue = globaltimer();
+              }
               tc_fence_after();
               const uint32_t sft_col = tmem + kSfCol0 + s * kSfColsPerStage;
               const uint32_t sfw_col = sft_col + 4;
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       // every MMA and scale copy this thread issued has completed before TMEM is freed
       tc_commit(drain);
       mbar_wait_drain(drain, 0, st, kSiteDrainMma);
-      if (kProf) {
+      if (kProf && args.prof) {
         args.prof[blockIdx.x * 8 + 1] = w_full;
         args.prof[blockIdx.x * 8 + 2] = w_tempty;
         args.prof[blockIdx.x * 8 + 3] = globaltimer() - t_start;
@@ -551,13 +558,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
           if (lane == 0) red_release_gpu_add(args.ctr_l2 + t.e, 1);
         }
       }
-      if (kProf) { w_tfull += t1 - t0; busy += globaltimer() - t1; }
+      if (kProf) {
+        const uint64_t t2 = globaltimer();
+        w_tfull += t1 - t0;
+        busy += t2 - t1;
+        if (args.trace && warp == kEpiWarp0 && lane == 0 && it < args.trace_cap) {
+          TraceRec& r = args.trace[static_cast<size_t>(blockIdx.x) * args.trace_cap + it];
+          r.cta = blockIdx.x; r.task = it; r.type = t.type; r.expert = t.e; r.tile = t.n; r.block = t.b;
+          r.valid = t.valid; r.mode = args.mode;
+          r.t_mma_done = t1;
+          r.t_epi_done = t2;
+        }
+      }
     }
     if (args.early_combine) {
       if (args.pbf16) early_combine<__nv_bfloat16>(args, kEpiWarps, args.NB2, s_blk, st, s_abort, lane);
       else early_combine<float>(args, kEpiWarps, args.NB2, s_blk, st, s_abort, lane);
     }
-    if (kProf && warp == kEpiWarp0 && lane == 0) {
+    if (kProf && args.prof && warp == kEpiWarp0 && lane == 0) {
       args.prof[blockIdx.x * 8 + 5] = w_tfull;
       args.prof[blockIdx.x * 8 + 6] = busy;
     }
@@ -617,6 +635,8 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
   a.ctr_l2r = a.deferred + L.T;
   a.status = W.status; a.timeout_ns = g.timeout_ns;
   a.prof = g.prof ? g.prof + (mode == 2 ? 8 * 1024 : 0) : nullptr;
+  a.trace = reinterpret_cast<TraceRec*>(g.trace);
+  a.trace_cap = g.trace ? g.trace_cap : 0;
   {
     // W1 as (k, row, half): half 1 is I rows below half 0, so one box of
     // {128 k, 128 rows, 2 halves} is 128 gate rows followed by the matching 128 up rows
@@ -641,7 +661,7 @@ cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra,
       return cudaErrorInvalidValue;
   }
   using KernelFn = void (*)(Maps, Args);
-  const bool prof = a.prof != nullptr;
+  const bool prof = a.prof != nullptr || a.trace != nullptr;
   const KernelFn kernels[2] = {gemm_mx_kernel<false>, gemm_mx_kernel<true>};
   const size_t smem = SmemLayout::total(L.E) + 1024;
   // the setmaxnreg split assumes exactly kLaunchRegs registers a thread at launch

@@ -136,7 +136,15 @@ struct GemmLaunch {
   void* out;
   bool pdl;                 // programmatic launch after the routing kernel
   bool per_block;           // token-M kernel: deal (weight tile, pool block) pairs as separate groups
+  uint8_t* trace;           // token-M kernel: per-task trace records of this launch ([grid][trace_cap] x 64 B) or null
+  int trace_cap;            // records per CTA
 };
+// One per-task trace record (64 bytes; mm_moe.h, Options.trace_buf).
+struct TraceRec {
+  uint32_t cta, task, type, expert, tile, block, valid, mode;
+  uint64_t t_issue, t_mma_done, t_epi_done, reserved;
+};
+static_assert(sizeof(TraceRec) == 64, "trace record");
 // mode 1: L1 tiles, mode 2: L2 tiles, mode 3: gather + lag-ordered L1/L2 stream
 cudaError_t launch_gemm_mx(const GemmLaunch& g, int mode, int lag, int l1_extra, cudaStream_t s);
 int mx_lag_auto(int E);
