@@ -117,3 +117,17 @@ def test_the_full_lag_would_break_the_order_without_the_rule():
 def test_an_expert_named_twice_overflows_the_smallest_ring():
     cnt = [400, 0, 0]                               # T = 200, K = 2, both slots on expert 0
     assert _check(cnt, 2, 2) is None
+
+
+def test_every_l2_group_follows_its_blocks_l1_groups():
+    """The stream's own dependency (an L2 tile reads blocks the expert's L1 tiles
+    wrote) points backwards for every lag, ring or not."""
+    rng = np.random.default_rng(11)
+    for _ in range(100):
+        E = int(rng.integers(1, 40))
+        nb = list(rng.integers(0, 4, size=E))
+        for lag in (0, 1, int(rng.integers(0, E + 1)), E):
+            order = _stream(nb, lag)
+            for v in range(E):
+                if nb[v]:
+                    assert max(order[(1, v, n)] for n in range(2)) < min(order[(2, v, n)] for n in range(2))
