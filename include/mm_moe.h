@@ -168,7 +168,8 @@ typedef struct mm_moe_options {
                                    twice) ends with MM_MOE_ERR_BAD_ROUTING, site 114, and no output. */
   void* trace_buf;              /* optional per-task trace (device memory, 16-byte aligned, zeroed by the
                                    caller; NULL = off, the default).  The token-M MX kernel (swap_ab = 0)
-                                   then runs its timing instantiation (a few % slower) and writes one
+                                   then runs its timing instantiation (its timing branches cost the MMA
+                                   issue loop some cycles; the trace itself is not timed) and writes one
                                    64-byte record per task it runs: uint32 cta, task (its index within
                                    the CTA), type (1 = L1, 2 = L2), expert, tile, pool block, valid rows,
                                    launch mode (3 = fused stream, 1 / 2 = the L1 / L2 launch of the
