@@ -273,3 +273,112 @@ def forward_distributed(st: RankState, w1, w1_sf, w2, w2_sf, I: int, opt=None, g
     del peer_meta, peer_x, peer_xsf, peer_out, peer_part
     barrier()
     return out, (send_row, rows, rex)
+
+
+class EPRank:
+    """One rank of a multi-process EP layer whose buffers outlive its forwards,
+    as the pages' symmetric buffer does (llm-infra-atlas "07 · MegaMoE" §3: one
+    buffer per rank with an input region for x and its scales; DeepGEMM PR #440:
+    receive space sized by `num_tokens_bound`).
+
+    The constructor allocates, for at most `num_tokens_bound` tokens a call: the
+    input region (x and its scales, which peers pull from), the metadata and row
+    output buffers of the pairs this rank receives (mm_moe_ep_recv_capacity
+    rows), the combine's slot buffer, and the local forward's receive rows and
+    workspace; it prepares the local experts' weight scales and exchanges every
+    peer-visible buffer's address once (`share_peers`, a collective: every rank
+    constructs its EPRank together).  `forward` then runs the steps of
+    `forward_distributed` on those buffers; every rank calls it together, each
+    with its own tokens.  `close` (collective) releases the peers' mappings."""
+
+    def __init__(self, rank: int, N: int, E: int, K: int, H: int, I: int, variant: int, num_tokens_bound: int,
+                 w1, w1_sf, w2, w2_sf, device, opt=None, group=None):
+        import torch
+        import torch.distributed as dist
+        assert dist.get_rank(group) == rank and dist.get_world_size(group) == N and E % N == 0
+        self.rank, self.N, self.E, self.K, self.H, self.I, self.variant = rank, N, E, K, H, I, variant
+        self.bound, self.group, self.dev = num_tokens_bound, group, device
+        self.opt = opt if opt is not None else options(variant)
+        self.Eloc = E // N
+        self.cap = mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N)
+        room = max(self.cap, 1)
+        B = max(num_tokens_bound, 1)
+        sf_row = H // 32 if variant == MM_MOE_VARIANT_MX else H // 128
+        sf_dtype = torch.uint8 if variant == MM_MOE_VARIANT_MX else torch.float32
+        # peer-visible: the input region, the metadata and row outputs this rank receives, its slot buffer
+        self.x_in = torch.zeros(B, H, dtype=torch.uint8, device=device)
+        self.xsf_in = torch.zeros(B, sf_row, dtype=sf_dtype, device=device)
+        self.meta = torch.zeros(room, 4, dtype=torch.int32, device=device)
+        self.out_recv = torch.zeros(room, H, dtype=torch.bfloat16, device=device)
+        self.parts = torch.zeros(B * K, H, dtype=torch.bfloat16, device=device)
+        # local: the pulled rows, their K = 1 routing, the local forward's workspace and weights
+        self.x_recv = torch.empty(room, H, dtype=torch.uint8, device=device)
+        self.xsf_recv = torch.empty(room, sf_row, dtype=sf_dtype, device=device)
+        self.idx_recv = torch.empty(room, 1, dtype=torch.int32, device=device)
+        self.w_recv = torch.empty(room, 1, dtype=torch.float32, device=device)
+        self.ws = alloc_workspace(room, H, I, self.Eloc, 1, self.opt, device)
+        lo, hi = rank * self.Eloc, (rank + 1) * self.Eloc
+        self.w1, self.w2 = w1[lo:hi].contiguous(), w2[lo:hi].contiguous()
+        self.w1p, self.w2p = prepare_weights(w1_sf[lo:hi].contiguous(), w2_sf[lo:hi].contiguous(), H, I, self.Eloc,
+                                             self.opt)
+        self._peers = share_peers([self.meta, self.x_in, self.xsf_in, self.out_recv, self.parts], group)
+        self.t_meta, self.t_x, self.t_xsf, self.t_out, self.t_part = (pointer_table(p, device) for p in self._peers)
+        self._barrier()
+
+    def _barrier(self):
+        import torch
+        import torch.distributed as dist
+        torch.cuda.synchronize()
+        dist.barrier(group=self.group)
+
+    def forward(self, x, x_sf, topk_idx, topk_w, combine: str = "push"):
+        """This rank's bf16 output [T, H] for its T <= num_tokens_bound tokens, and
+        its plan (send_row, recv_rows, recv_expert)."""
+        import torch
+        import torch.distributed as dist
+        T, K = topk_idx.shape
+        assert K == self.K and T <= self.bound and x.shape == (T, self.H)
+        N, E, H, rank, dev = self.N, self.E, self.H, self.rank, self.dev
+        s = torch.cuda.current_stream().cuda_stream
+        if T:
+            self.x_in[:T].copy_(x)
+            self.xsf_in[:T].copy_(x_sf)
+        c = torch.empty(E, dtype=torch.int32, device=dev)
+        _check(mm_moe_ep_count(topk_idx.data_ptr(), T, K, E, c.data_ptr(), s), "mm_moe_ep_count")
+        every = [None] * N
+        dist.all_gather_object(every, c.cpu().numpy(), group=self.group)
+        send_row, rows, rex = mm_moe_ep_plan(np.stack(every), topk_idx.cpu().numpy(), T, K, E, N, rank,
+                                             recv_capacity=self.cap)
+        send_row_d = torch.from_numpy(np.ascontiguousarray(send_row)).to(dev)
+        _check(mm_moe_ep_push_meta(topk_idx.data_ptr(), topk_w.data_ptr(), send_row_d.data_ptr(), T, K, E, N, rank,
+                                   self.t_meta.data_ptr(), s), "mm_moe_ep_push_meta")
+        self._barrier()
+        R = rows
+        if R > 0:
+            _check(mm_moe_ep_pull(self.meta.data_ptr(), R, K, H, self.variant, self.t_x.data_ptr(),
+                                  self.t_xsf.data_ptr(), self.x_recv.data_ptr(), self.xsf_recv.data_ptr(),
+                                  self.idx_recv.data_ptr(), self.w_recv.data_ptr(), s), "mm_moe_ep_pull")
+            forward(self.x_recv[:R], self.xsf_recv[:R], self.idx_recv[:R], self.w_recv[:R], self.w1, self.w1p,
+                    self.w2, self.w2p, self.out_recv[:R], H, self.I, self.Eloc, self.ws, self.opt)
+            code, where = sync_status(self.ws)
+            if code != 0:
+                raise MMError(code, f"rank {rank} local forward (site {where})")
+        self._barrier()
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        if combine == "push":
+            _check(mm_moe_ep_push_out(self.meta.data_ptr(), R, H, self.out_recv.data_ptr(), self.t_part.data_ptr(),
+                                      s), "mm_moe_ep_push_out")
+            self._barrier()
+            _check(mm_moe_ep_combine_local(topk_idx.data_ptr(), T, K, E, H, self.parts.data_ptr(), out.data_ptr(),
+                                           s), "mm_moe_ep_combine_local")
+        else:
+            _check(mm_moe_ep_combine(topk_idx.data_ptr(), send_row_d.data_ptr(), T, K, E, N, H,
+                                     self.t_out.data_ptr(), out.data_ptr(), s), "mm_moe_ep_combine")
+        # the next call overwrites buffers that peers read in this one
+        self._barrier()
+        return out, (send_row, rows, rex)
+
+    def close(self):
+        self._barrier()
+        self._peers = None
+        self._barrier()
