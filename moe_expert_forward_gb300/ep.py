@@ -17,8 +17,10 @@ bits.  `plan_distributed` is the host side of a multi-process run
 rank's whole forward in a multi-process run: the peers' buffers are mapped into
 this process by CUDA IPC (`share_peers`), and a device synchronisation plus a
 process-group barrier separates the steps, so no kernel ever waits for another
-process.  `forward_on_one_device` runs N ranks whose buffers all live in one
-process, step by step from the host.
+process.  `EPRank` is the same rank with its buffers and the peers' addresses
+set up once and kept across calls (inputs copied into a bound-sized input
+region each call).  `forward_on_one_device` runs N ranks whose buffers all live
+in one process, step by step from the host.
 """
 from __future__ import annotations
 
