@@ -195,86 +195,27 @@ def share_peers(tensors: Sequence, group=None):
 def forward_distributed(st: RankState, w1, w1_sf, w2, w2_sf, I: int, opt=None, group=None, combine: str = "push",
                         num_tokens_bound: Optional[int] = None):
     """One rank's EP forward in a multi-process run (one process per rank; the
-    ranks may share a GPU or not).  st holds this rank's tokens; w1 / w1_sf / w2 /
-    w2_sf hold all E experts in the layouts of mm_moe.h, of which this rank uses
-    [rank*E/N, (rank+1)*E/N).  Steps: count -> all-gather the counts -> plan ->
-    exchange buffer addresses -> push metadata -> barrier -> pull rows and the
+    ranks may share a GPU or not): an `EPRank` sized for `num_tokens_bound` tokens
+    (default: the largest rank's token count, gathered here), one call of its
+    forward, and its release.  st holds this rank's tokens; w1 / w1_sf / w2 /
+    w2_sf hold all E experts in the layouts of mm_moe.h.  Steps: count ->
+    all-gather the counts -> plan -> push metadata -> barrier -> pull rows and the
     local forward -> barrier -> combine (push: store row outputs into the token
     ranks, barrier, local sum; pull: read the slots from their owners) ->
     barrier.  Returns this rank's bf16 output [T, H] and its plan (send_row,
-    recv_rows, recv_expert)."""
-    import torch
+    recv_rows, recv_expert).  Collective: every rank calls it together."""
     import torch.distributed as dist
     N = dist.get_world_size(group)
-    rank = dist.get_rank(group)
-    assert rank == st.rank and N == st.N
-    E, H, K, T, variant = st.E, st.H, st.K, st.T, st.variant
-    Eloc = E // N
-    dev = st.x.device
-    s = torch.cuda.current_stream().cuda_stream
-    base_opt = opt if opt is not None else options(variant)
-
-    def barrier():
-        torch.cuda.synchronize()
-        dist.barrier(group=group)
-
-    # 1. counts, gathered on the host, and this rank's plan
-    c = torch.empty(E, dtype=torch.int32, device=dev)
-    _check(mm_moe_ep_count(st.topk_idx.data_ptr(), T, K, E, c.data_ptr(), s), "mm_moe_ep_count")
-    every = [None] * N
-    dist.all_gather_object(every, c.cpu().numpy(), group=group)
-    counts_all = np.stack(every)
-    cap = mm_moe_ep_recv_capacity(num_tokens_bound, K, E, N) if num_tokens_bound is not None else None
-    send_row, rows, rex = mm_moe_ep_plan(counts_all, st.topk_idx.cpu().numpy(), T, K, E, N, rank, recv_capacity=cap)
-    R = rows
-    room = max(rows if cap is None else cap, 1)
-    send_row_d = torch.from_numpy(np.ascontiguousarray(send_row)).to(dev)
-    meta = torch.zeros(room, 4, dtype=torch.int32, device=dev)
-    out_recv = torch.zeros(room, H, dtype=torch.bfloat16, device=dev)
-    parts = torch.empty(max(T * K, 1), H, dtype=torch.bfloat16, device=dev)
-    # 2. every rank's buffers, mapped here
-    peer_meta, peer_x, peer_xsf, peer_out, peer_part = share_peers([meta, st.x, st.x_sf, out_recv, parts], group)
-    t_meta, t_x, t_xsf, t_out, t_part = (pointer_table(p, dev) for p in
-                                         (peer_meta, peer_x, peer_xsf, peer_out, peer_part))
-    # 3. metadata pushed into the owners' buffers
-    _check(mm_moe_ep_push_meta(st.topk_idx.data_ptr(), st.topk_w.data_ptr(), send_row_d.data_ptr(), T, K, E, N, rank,
-                               t_meta.data_ptr(), s), "mm_moe_ep_push_meta")
-    barrier()
-    # 4. rows pulled from their source ranks, then the local forward over them (K = 1)
-    if R > 0:
-        sf_row = H // 32 if variant == MM_MOE_VARIANT_MX else H // 128
-        sf_dtype = torch.uint8 if variant == MM_MOE_VARIANT_MX else torch.float32
-        x_recv = torch.empty(R, H, dtype=torch.uint8, device=dev)
-        xsf_recv = torch.empty(R, sf_row, dtype=sf_dtype, device=dev)
-        idx_recv = torch.empty(R, 1, dtype=torch.int32, device=dev)
-        w_recv = torch.empty(R, 1, dtype=torch.float32, device=dev)
-        _check(mm_moe_ep_pull(meta.data_ptr(), R, K, H, variant, t_x.data_ptr(), t_xsf.data_ptr(), x_recv.data_ptr(),
-                              xsf_recv.data_ptr(), idx_recv.data_ptr(), w_recv.data_ptr(), s), "mm_moe_ep_pull")
-        lo, hi = rank * Eloc, (rank + 1) * Eloc
-        w1p, w2p = prepare_weights(w1_sf[lo:hi].contiguous(), w2_sf[lo:hi].contiguous(), H, I, Eloc, base_opt)
-        ws = alloc_workspace(R, H, I, Eloc, 1, base_opt, dev)
-        forward(x_recv, xsf_recv, idx_recv, w_recv, w1[lo:hi].contiguous(), w1p, w2[lo:hi].contiguous(), w2p,
-                out_recv, H, I, Eloc, ws, base_opt)
-        code, where = sync_status(ws)
-        if code != 0:
-            raise MMError(code, f"rank {rank} local forward (site {where})")
-    barrier()
-    # 5. combine
-    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    if combine == "push":
-        _check(mm_moe_ep_push_out(meta.data_ptr(), R, H, out_recv.data_ptr(), t_part.data_ptr(), s),
-               "mm_moe_ep_push_out")
-        barrier()
-        _check(mm_moe_ep_combine_local(st.topk_idx.data_ptr(), T, K, E, H, parts.data_ptr(), out.data_ptr(), s),
-               "mm_moe_ep_combine_local")
-    else:
-        _check(mm_moe_ep_combine(st.topk_idx.data_ptr(), send_row_d.data_ptr(), T, K, E, N, H, t_out.data_ptr(),
-                                 out.data_ptr(), s), "mm_moe_ep_combine")
-    # no rank frees a buffer while a peer may still read or write it
-    barrier()
-    del peer_meta, peer_x, peer_xsf, peer_out, peer_part
-    barrier()
-    return out, (send_row, rows, rex)
+    if num_tokens_bound is None:
+        every = [None] * N
+        dist.all_gather_object(every, int(st.T), group=group)
+        num_tokens_bound = max(every)
+    ctx = EPRank(st.rank, N, st.E, st.K, st.H, I, st.variant, num_tokens_bound, w1, w1_sf, w2, w2_sf, st.x.device,
+                 opt, group)
+    try:
+        return ctx.forward(st.x, st.x_sf, st.topk_idx, st.topk_w, combine=combine)
+    finally:
+        ctx.close()
 
 
 class EPRank:
